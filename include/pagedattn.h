@@ -1,0 +1,218 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 paged KV-cache decode library.
+ *
+ * The library keeps a transformer's KV cache in ONE preallocated device tensor
+ * of fixed-size physical blocks and runs decode attention directly on it,
+ * resolving every token through a per-sequence block table.
+ *
+ * Sources of the semantics (page title, section):
+ *  - "Paged KV-Cache Memory Management" (mini-infer), "The Solution" and
+ *    "Python Implementation: Physical Block Pool": the pool tensor
+ *    [num_blocks, 2 (K/V), num_layers, num_kv_heads, block_size, head_dim],
+ *    zero-initialised once, and the free-block stack allocator
+ *    (ids 0..n-1, allocation pops from the end, exhaustion is an error).
+ *  - "vllmini", "PagedAttention Metaphor" and "The CUDA Block Kernel": logical
+ *    block i of a sequence lives in physical block block_table[i]; the kernel
+ *    resolves token t to (block_table[t / B], t % B) on the fly; the kernel's
+ *    argument list (out, q, caches, block_tables, context_lens, block_size,
+ *    num_heads, head_size).
+ *  - "kv-cache" skill, section 2 "PagedAttention Architecture": blocks are
+ *    taken one at a time as a sequence grows; only the last block is partly
+ *    filled.
+ *
+ * Conventions for every call:
+ *  - Return value: PA_OK (0) or a PA_ERR_* code; pa_last_error_string() then
+ *    describes the failure (per calling thread).  Nothing throws across the ABI.
+ *  - Device pointers are plain CUDA device addresses on the CURRENT device.
+ *    The caller owns every device buffer (pool, q, k, v, out, tables, lengths,
+ *    positions, workspace); the library owns only the pool handle and its
+ *    host-side free stack.
+ *  - Kernels are enqueued asynchronously on `stream` (NULL = legacy default
+ *    stream).  Buffers must stay valid until the stream reaches the call.
+ *  - Argument checks that need no device data happen on the host before any
+ *    launch and return PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED.  Checks that
+ *    need device data (block ids, lengths, positions) happen in the kernels:
+ *    an offending row is skipped (never read or written out of bounds) and a
+ *    bit is set in the device status word, read with pa_get_status().
+ *  - The first launching call on a device looks up the device status word; do
+ *    that call (or pa_get_status) once before capturing a stream into a graph.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque pool handle: geometry + device pointer + host free-block stack. */
+typedef struct pa_pool pa_pool;
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* pa_stream_t;
+
+/* Element type of the pool, q, k and v. */
+typedef enum pa_dtype { PA_DTYPE_F32 = 0, PA_DTYPE_BF16 = 1 } pa_dtype;
+
+/* Return codes. */
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, geometry mismatch */
+    PA_ERR_NO_FREE_BLOCKS = 2, /* allocator exhausted ("Out of KV-Cache Physical Blocks") */
+    PA_ERR_DOUBLE_FREE = 3,    /* freeing a block that is not allocated */
+    PA_ERR_CUDA = 4,           /* a CUDA runtime call failed (message has the CUDA error) */
+    PA_ERR_UNSUPPORTED = 5,    /* valid arguments, but no kernel is built for this shape */
+    PA_ERR_WORKSPACE = 6       /* workspace missing, misaligned or smaller than required */
+};
+
+/* Bits of the device status word (pa_get_status). */
+#define PA_STATUS_BAD_BLOCK_ID 0x1u /* a table entry read was outside [0, num_blocks) */
+#define PA_STATUS_BAD_LENGTH 0x2u   /* a context length / position outside the table */
+#define PA_STATUS_TIMEOUT 0x4u      /* a bounded wait for a shared-memory copy gave up */
+
+/* Human-readable description of the calling thread's last error ("" if none). */
+const char* pa_last_error_string(void);
+
+/* ----------------------------------------------------------------------------
+ * Pool and allocator (host only; none of these calls touches the GPU).
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Wrap an existing device tensor as a block pool (mini-infer BlockPool).
+ *   pool_dev   device pointer to num_blocks * 2 * num_layers * num_kv_heads *
+ *              block_size * head_dim elements of `dtype`, row-major in that
+ *              order, 16-byte aligned.  Caller-owned; never freed here.
+ *   geometry   all > 0; head_dim * sizeof(dtype) must be a multiple of 16.
+ * The free stack starts as 0..num_blocks-1; pa_alloc_block pops the END, so
+ * the first id handed out is num_blocks-1.
+ */
+int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers,
+                   int num_kv_heads, int block_size, int head_dim, pa_dtype dtype);
+
+/* Release the handle (not the caller's device tensor).  NULL is accepted. */
+int pa_pool_destroy(pa_pool* pool);
+
+/* Bytes of one physical block: 2 * num_layers * num_kv_heads * block_size *
+ * head_dim * element size (K and V of every layer and KV head). */
+int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes);
+
+/* Replace the free stack by `order` (a permutation of 0..num_blocks-1, n ==
+ * num_blocks); allowed only while every block is free.  The LAST entry is
+ * handed out first. */
+int pa_pool_seed_free_stack(pa_pool* pool, const int* order, int n);
+
+/* Pop one block id from the free stack.  PA_ERR_NO_FREE_BLOCKS when empty
+ * ("Out of KV-Cache Physical Blocks"). */
+int pa_alloc_block(pa_pool* pool, int* block_id);
+
+/* Push `block_id` back; it becomes the next id handed out.  Ids outside the
+ * pool are PA_ERR_INVALID_ARG, ids not currently allocated PA_ERR_DOUBLE_FREE. */
+int pa_free_block(pa_pool* pool, int block_id);
+
+/* Number of ids on the free stack. */
+int pa_num_free(const pa_pool* pool, int* n);
+
+/* ----------------------------------------------------------------------------
+ * KV append (reshape-and-cache).
+ * ------------------------------------------------------------------------- */
+
+/*
+ * For every sequence b and KV head h, copy k[b][h][:] to pool[bt[b][p/B]][0]
+ * [layer][h][p % B][:] and v[b][h][:] to the same slot with K/V index 1, where
+ * p = positions[b] and B = block_size.  A bit copy: the stored bytes equal the
+ * input bytes.
+ *   k, v          device, [batch, num_kv_heads, head_dim] of the pool dtype,
+ *                 16-byte aligned.
+ *   block_tables  device int32 [batch, max_blocks_per_seq], row-major.
+ *   positions     device int32 [batch]; p/B < max_blocks_per_seq required.
+ * Rows whose position or block id is out of range are skipped and flagged in
+ * the status word (PA_STATUS_BAD_LENGTH / PA_STATUS_BAD_BLOCK_ID).
+ */
+int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
+                const int* block_tables, int max_blocks_per_seq, const int* positions,
+                int batch, pa_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Decode attention.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * out[b][h][:] = softmax_t(scale * q[b][h] . K_t) V_t over the n = context_lens[b]
+ * cached tokens t of sequence b, where K_t / V_t are the rows of KV head
+ * h / (num_heads / num_kv_heads) at slot (block_tables[b][t / B], t % B) of
+ * `layer`.  n = 0 yields a zero vector.  Scores and sums are fp32.
+ *   out           device fp32 [batch, num_heads, head_dim], 16-byte aligned.
+ *   q             device [batch, num_heads, head_dim] of the pool dtype, 16-byte aligned.
+ *   block_tables  device int32 [batch, max_blocks_per_seq]; entries past
+ *                 ceil(n / B) are never read (pad with -1).
+ *   context_lens  device int32 [batch], 0 <= n <= max_blocks_per_seq * B.
+ *   block_size, num_kv_heads, head_dim must equal the pool's; num_heads must be
+ *   a multiple of num_kv_heads.
+ *   workspace     device scratch of at least pa_decode_workspace_size() bytes,
+ *                 256-byte aligned (may be NULL when that size is 0).  Contents
+ *                 need no initialisation; concurrent calls need separate workspaces.
+ * The context of each (sequence, KV head) is split into partitions of a
+ * heuristically chosen number of blocks; with more than one partition a second
+ * kernel merges the per-partition results (log-sum-exp combine).
+ */
+int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int layer,
+                        const int* block_tables, int max_blocks_per_seq,
+                        const int* context_lens, int batch, int block_size, int num_heads,
+                        int num_kv_heads, int head_dim, float scale, void* workspace,
+                        size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * pa_decode_attention with an explicit partition size: `partition_blocks`
+ * physical blocks per partition (>= 1), or 0 for the heuristic choice.
+ * A partition covering the whole table (partition_blocks >= max_blocks_per_seq)
+ * runs a single kernel and needs no workspace.
+ */
+int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
+                                    const int* block_tables, int max_blocks_per_seq,
+                                    const int* context_lens, int batch, int block_size,
+                                    int num_heads, int num_kv_heads, int head_dim, float scale,
+                                    int partition_blocks, void* workspace,
+                                    size_t workspace_bytes, pa_stream_t stream);
+
+/* The partition size (in blocks) that pa_decode_attention picks for these
+ * sizes on the current device.  Queries the device's SM count. */
+int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_heads,
+                               int max_blocks_per_seq, int* partition_blocks);
+
+/* Workspace bytes needed by pa_decode_attention_partitioned with the same
+ * arguments (partition_blocks = 0: the heuristic choice, which queries the
+ * current device).  0 when a single partition covers the table. */
+int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
+                             int max_blocks_per_seq, int partition_blocks, size_t* bytes);
+
+/* ----------------------------------------------------------------------------
+ * Batched gather (mini-infer "Zero-Copy Batched Attention Gather").
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Copy the first context_lens[b] K and V rows of every sequence of `layer`
+ * into contiguous k_out / v_out [batch, max_len, num_kv_heads, head_dim] (pool
+ * dtype) and set mask[b][t] = 1 for t < context_lens[b], else 0 (rows past the
+ * length are zero-filled).  k_out, v_out 16-byte aligned; mask uint8
+ * [batch, max_len].  Lengths above max_len or above the table are flagged
+ * (PA_STATUS_BAD_LENGTH) and treated as 0.
+ */
+int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, int layer,
+                 const int* block_tables, int max_blocks_per_seq, const int* context_lens,
+                 int batch, int max_len, pa_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Device status.
+ * ------------------------------------------------------------------------- */
+
+/* Wait for `stream`, return the current device's status bits (PA_STATUS_*)
+ * accumulated since the last call, and clear them.  Blocking. */
+int pa_get_status(unsigned int* status, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,417 @@
+// pa_api.cpp -- the C ABI: pool handle, free-block stack allocator, argument
+// validation and kernel launches.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "pa_internal.h"
+#include "pagedattn.h"
+
+struct pa_pool {
+    pa::PoolGeom g;
+    std::vector<int> free_stack;        // allocation pops from the back
+    std::vector<unsigned char> in_use;  // 1 while a block is handed out
+    mutable std::mutex mu;
+};
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(e == cudaErrorNotSupported ? PA_ERR_UNSUPPORTED : PA_ERR_CUDA, "%s: %s (%s)",
+                what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int num_sms_current(int* out) {
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PA_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        int v = 0;
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiProcessorCount)");
+        cache[dev] = v;
+    }
+    *out = cache[dev];
+    return PA_OK;
+}
+
+// Partition size heuristic: about 256 KiB of K+V per CTA, shrunk (down to
+// 16 KiB) while the grid would hold fewer than four CTAs per SM.
+int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sms) {
+    const long long blk_bytes = 2LL * g.B * g.D * g.elt;
+    long long pb = (256LL * 1024) / blk_bytes;
+    if (pb < 1) pb = 1;
+    if (pb > maxb) pb = maxb;
+    while (pb > 1) {
+        const long long parts = (maxb + pb - 1) / pb;
+        if ((long long)batch * g.Hkv * parts >= 4LL * num_sms) break;
+        const long long half = pb / 2;
+        if (half * blk_bytes < 16 * 1024) break;
+        pb = half;
+    }
+    return (int)pb;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+size_t workspace_bytes_for(int batch, int H, int Cmax, int D) {
+    if (Cmax <= 1) return 0;
+    const size_t slots = (size_t)batch * H * Cmax;
+    return align256(slots * D * sizeof(float)) + slots * 2 * sizeof(float);
+}
+
+int check_pool(const pa_pool* pool) {
+    if (!pool) return fail(PA_ERR_INVALID_ARG, "pool handle is NULL");
+    return PA_OK;
+}
+
+int check_layer(const pa_pool* pool, int layer) {
+    if (layer < 0 || layer >= pool->g.L)
+        return fail(PA_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, pool->g.L);
+    return PA_OK;
+}
+
+struct DecodeShape {
+    int G, PB, Cmax;
+    size_t ws_bytes;
+};
+
+int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb,
+                         int partition_blocks, DecodeShape* out) {
+    if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (num_heads <= 0 || num_heads % pool->g.Hkv != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_heads %d is not a positive multiple of num_kv_heads %d",
+                    num_heads, pool->g.Hkv);
+    if (maxb <= 0) return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", maxb);
+    if ((long long)maxb * pool->g.B > INT_MAX)
+        return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq * block_size overflows int");
+    if (partition_blocks < 0)
+        return fail(PA_ERR_INVALID_ARG, "partition_blocks %d < 0", partition_blocks);
+    const int G = num_heads / pool->g.Hkv;
+    if (!pa::decode_supported(pool->g.dtype, pool->g.D, pool->g.B, G))
+        return fail(PA_ERR_UNSUPPORTED,
+                    "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
+                    "(built: head_dim 64/128, block_size 16/32, group 1/2/4/8)",
+                    pool->g.dtype, pool->g.D, pool->g.B, G);
+    int pb = partition_blocks;
+    if (pb == 0) {
+        int sms = 0;
+        int rc = num_sms_current(&sms);
+        if (rc != PA_OK) return rc;
+        pb = auto_partition_blocks(pool->g, batch, maxb, sms);
+    }
+    if (pb > maxb) pb = maxb;
+    const int Cmax = (maxb + pb - 1) / pb;
+    if ((long long)batch * pool->g.Hkv * Cmax > INT_MAX)
+        return fail(PA_ERR_INVALID_ARG, "grid of %lld CTAs is too large",
+                    (long long)batch * pool->g.Hkv * Cmax);
+    out->G = G;
+    out->PB = pb;
+    out->Cmax = Cmax;
+    out->ws_bytes = workspace_bytes_for(batch, num_heads, Cmax, pool->g.D);
+    return PA_OK;
+}
+
+}  // namespace
+
+namespace pa {
+bool decode_supported(int dtype, int D, int B, int G) {
+    if (dtype != 0 && dtype != 1) return false;
+    if (D != 64 && D != 128) return false;
+    if (B != 16 && B != 32) return false;
+    return G == 1 || G == 2 || G == 4 || G == 8;
+}
+}  // namespace pa
+
+extern "C" {
+
+const char* pa_last_error_string(void) { return t_last_error.c_str(); }
+
+int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers,
+                   int num_kv_heads, int block_size, int head_dim, pa_dtype dtype) {
+    if (!out) return fail(PA_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!pool_dev) return fail(PA_ERR_INVALID_ARG, "pool_dev is NULL");
+    if (!aligned(pool_dev, 16)) return fail(PA_ERR_INVALID_ARG, "pool_dev is not 16-byte aligned");
+    if (num_blocks <= 0 || num_layers <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
+        head_dim <= 0)
+        return fail(PA_ERR_INVALID_ARG, "pool geometry must be positive (nb=%d L=%d Hkv=%d B=%d D=%d)",
+                    num_blocks, num_layers, num_kv_heads, block_size, head_dim);
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16)
+        return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    const int elt = dtype == PA_DTYPE_F32 ? 4 : 2;
+    if ((head_dim * elt) % 16 != 0)
+        return fail(PA_ERR_INVALID_ARG, "head_dim * element size (%d) must be a multiple of 16",
+                    head_dim * elt);
+    const double elems = (double)num_blocks * 2 * num_layers * num_kv_heads * block_size * head_dim;
+    if (elems > 4.0e18) return fail(PA_ERR_INVALID_ARG, "pool too large");
+    try {
+        pa_pool* p = new pa_pool();
+        p->g = pa::PoolGeom{pool_dev, num_blocks, num_layers, num_kv_heads, block_size, head_dim,
+                            elt, (int)dtype};
+        p->free_stack.resize(num_blocks);
+        for (int i = 0; i < num_blocks; ++i) p->free_stack[i] = i;
+        p->in_use.assign(num_blocks, 0);
+        *out = p;
+    } catch (const std::bad_alloc&) {
+        return fail(PA_ERR_INVALID_ARG, "host allocation failed for %d blocks", num_blocks);
+    }
+    return PA_OK;
+}
+
+int pa_pool_destroy(pa_pool* pool) {
+    delete pool;
+    return PA_OK;
+}
+
+int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = (size_t)2 * pool->g.L * pool->g.Hkv * pool->g.B * pool->g.D * pool->g.elt;
+    return PA_OK;
+}
+
+int pa_pool_seed_free_stack(pa_pool* pool, const int* order, int n) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!order) return fail(PA_ERR_INVALID_ARG, "order is NULL");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    const long long nb = pool->g.num_blocks;
+    if (n != nb) return fail(PA_ERR_INVALID_ARG, "order has %d entries, pool has %lld blocks", n, nb);
+    if ((long long)pool->free_stack.size() != nb)
+        return fail(PA_ERR_INVALID_ARG, "seeding requires every block to be free");
+    std::vector<unsigned char> seen(nb, 0);
+    for (int i = 0; i < n; ++i) {
+        if (order[i] < 0 || order[i] >= nb || seen[order[i]])
+            return fail(PA_ERR_INVALID_ARG, "order is not a permutation of 0..%lld (entry %d = %d)",
+                        nb - 1, i, order[i]);
+        seen[order[i]] = 1;
+    }
+    pool->free_stack.assign(order, order + n);
+    return PA_OK;
+}
+
+int pa_alloc_block(pa_pool* pool, int* block_id) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!block_id) return fail(PA_ERR_INVALID_ARG, "block_id is NULL");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    if (pool->free_stack.empty())
+        return fail(PA_ERR_NO_FREE_BLOCKS, "Out of KV-Cache Physical Blocks");
+    const int id = pool->free_stack.back();
+    pool->free_stack.pop_back();
+    pool->in_use[id] = 1;
+    *block_id = id;
+    return PA_OK;
+}
+
+int pa_free_block(pa_pool* pool, int block_id) {
+    if (int rc = check_pool(pool)) return rc;
+    std::lock_guard<std::mutex> lock(pool->mu);
+    if (block_id < 0 || block_id >= pool->g.num_blocks)
+        return fail(PA_ERR_INVALID_ARG, "block id %d outside [0, %lld)", block_id, pool->g.num_blocks);
+    if (!pool->in_use[block_id])
+        return fail(PA_ERR_DOUBLE_FREE, "block %d is not allocated", block_id);
+    pool->in_use[block_id] = 0;
+    pool->free_stack.push_back(block_id);
+    return PA_OK;
+}
+
+int pa_num_free(const pa_pool* pool, int* n) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!n) return fail(PA_ERR_INVALID_ARG, "n is NULL");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    *n = (int)pool->free_stack.size();
+    return PA_OK;
+}
+
+int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v, const int* block_tables,
+                int max_blocks_per_seq, const int* positions, int batch, pa_stream_t stream) {
+    if (int rc = check_pool(pool)) return rc;
+    if (int rc = check_layer(pool, layer)) return rc;
+    if (batch < 0) return fail(PA_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", max_blocks_per_seq);
+    if (batch == 0) return PA_OK;
+    if (!k || !v || !block_tables || !positions)
+        return fail(PA_ERR_INVALID_ARG, "k, v, block_tables and positions must be non-NULL");
+    if (!aligned(k, 16) || !aligned(v, 16))
+        return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    if (!aligned(block_tables, 4) || !aligned(positions, 4))
+        return fail(PA_ERR_INVALID_ARG, "block_tables and positions must be 4-byte aligned");
+    int sms = 0;
+    if (int rc = num_sms_current(&sms)) return rc;
+    unsigned* status = nullptr;
+    cudaError_t e = pa::status_word(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
+    pa::WriteParams p{pool->g.base, pool->g.num_blocks, pool->g.L, pool->g.Hkv, pool->g.B,
+                      pool->g.D * pool->g.elt, layer, k, v, block_tables, max_blocks_per_seq,
+                      positions, batch, status};
+    e = pa::launch_write_kv(p, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_write_kv launch");
+    return PA_OK;
+}
+
+int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_heads,
+                               int max_blocks_per_seq, int* partition_blocks) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!partition_blocks) return fail(PA_ERR_INVALID_ARG, "partition_blocks is NULL");
+    DecodeShape sh{};
+    if (int rc = resolve_decode_shape(pool, batch, num_heads, max_blocks_per_seq, 0, &sh)) return rc;
+    *partition_blocks = sh.PB;
+    return PA_OK;
+}
+
+int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
+                             int max_blocks_per_seq, int partition_blocks, size_t* bytes) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is NULL");
+    DecodeShape sh{};
+    if (int rc = resolve_decode_shape(pool, batch, num_heads, max_blocks_per_seq, partition_blocks,
+                                      &sh))
+        return rc;
+    *bytes = sh.ws_bytes;
+    return PA_OK;
+}
+
+int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
+                                    const int* block_tables, int max_blocks_per_seq,
+                                    const int* context_lens, int batch, int block_size,
+                                    int num_heads, int num_kv_heads, int head_dim, float scale,
+                                    int partition_blocks, void* workspace,
+                                    size_t workspace_bytes, pa_stream_t stream) {
+    if (int rc = check_pool(pool)) return rc;
+    if (int rc = check_layer(pool, layer)) return rc;
+    const pa::PoolGeom& g = pool->g;
+    if (block_size != g.B || num_kv_heads != g.Hkv || head_dim != g.D)
+        return fail(PA_ERR_INVALID_ARG,
+                    "block_size/num_kv_heads/head_dim (%d/%d/%d) do not match the pool (%d/%d/%d)",
+                    block_size, num_kv_heads, head_dim, g.B, g.Hkv, g.D);
+    if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "scale is not finite");
+    DecodeShape sh{};
+    if (int rc = resolve_decode_shape(pool, batch, num_heads, max_blocks_per_seq, partition_blocks,
+                                      &sh))
+        return rc;
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARG, "out, q, block_tables and context_lens must be non-NULL");
+    if (!aligned(out, 16) || !aligned(q, 16))
+        return fail(PA_ERR_INVALID_ARG, "out and q must be 16-byte aligned");
+    if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+    float* part_o = nullptr;
+    float* part_ml = nullptr;
+    if (sh.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < sh.ws_bytes || !aligned(workspace, 256))
+            return fail(PA_ERR_WORKSPACE,
+                        "workspace must be 256-byte aligned and hold %zu bytes (got %p, %zu)",
+                        sh.ws_bytes, workspace, workspace_bytes);
+        part_o = static_cast<float*>(workspace);
+        part_ml = reinterpret_cast<float*>(
+            static_cast<char*>(workspace) +
+            align256((size_t)batch * num_heads * sh.Cmax * g.D * sizeof(float)));
+    }
+    unsigned* status = nullptr;
+    cudaError_t e = pa::status_word(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
+    pa::DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.pool = g.base;
+    p.num_blocks = g.num_blocks;
+    p.L = g.L;
+    p.Hkv = g.Hkv;
+    p.layer = layer;
+    p.bt = block_tables;
+    p.maxb = max_blocks_per_seq;
+    p.lens = context_lens;
+    p.batch = batch;
+    p.H = num_heads;
+    p.qscale = scale * 1.4426950408889634f;  // log2(e): softmax evaluated with exp2
+    p.part_o = part_o;
+    p.part_ml = part_ml;
+    p.PB = sh.PB;
+    p.Cmax = sh.Cmax;
+    p.status = status;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    e = g.dtype == 1 ? pa::launch_decode_bf16(p, g.D, g.B, sh.G, s)
+                     : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    if (sh.Cmax > 1) {
+        e = pa::launch_combine(p, g.D, g.B, s);
+        if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    }
+    return PA_OK;
+}
+
+int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int layer,
+                        const int* block_tables, int max_blocks_per_seq, const int* context_lens,
+                        int batch, int block_size, int num_heads, int num_kv_heads, int head_dim,
+                        float scale, void* workspace, size_t workspace_bytes,
+                        pa_stream_t stream) {
+    return pa_decode_attention_partitioned(out, q, pool, layer, block_tables, max_blocks_per_seq,
+                                           context_lens, batch, block_size, num_heads,
+                                           num_kv_heads, head_dim, scale, 0, workspace,
+                                           workspace_bytes, stream);
+}
+
+int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, int layer,
+                 const int* block_tables, int max_blocks_per_seq, const int* context_lens,
+                 int batch, int max_len, pa_stream_t stream) {
+    if (int rc = check_pool(pool)) return rc;
+    if (int rc = check_layer(pool, layer)) return rc;
+    if (batch < 0 || max_len < 0)
+        return fail(PA_ERR_INVALID_ARG, "batch (%d) and max_len (%d) must be >= 0", batch, max_len);
+    if (max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq %d <= 0", max_blocks_per_seq);
+    if (batch == 0 || max_len == 0) return PA_OK;
+    if (!k_out || !v_out || !mask || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARG, "output and table pointers must be non-NULL");
+    if (!aligned(k_out, 16) || !aligned(v_out, 16))
+        return fail(PA_ERR_INVALID_ARG, "k_out and v_out must be 16-byte aligned");
+    int sms = 0;
+    if (int rc = num_sms_current(&sms)) return rc;
+    unsigned* status = nullptr;
+    cudaError_t e = pa::status_word(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
+    const pa::PoolGeom& g = pool->g;
+    pa::GatherParams p{k_out, v_out, mask, g.base, g.num_blocks, g.L, g.Hkv, g.B, g.D * g.elt,
+                       layer, block_tables, max_blocks_per_seq, context_lens, batch, max_len,
+                       status};
+    e = pa::launch_gather_kv(p, sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_gather_kv launch");
+    return PA_OK;
+}
+
+int pa_get_status(unsigned int* status, pa_stream_t stream) {
+    if (!status) return fail(PA_ERR_INVALID_ARG, "status is NULL");
+    cudaError_t e = pa::read_and_clear_status(status, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_get_status");
+    return PA_OK;
+}
+
+}  // extern "C"

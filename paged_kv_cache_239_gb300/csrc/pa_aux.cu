@@ -1,0 +1,159 @@
+// pa_aux.cu -- device status word, split-K combine launch, KV append and
+// batched gather kernels.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "pa_decode.cuh"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// One status word per device per loaded library (file-scope device variable:
+// no allocation).  Kernels OR PA_STATUS_* bits into it.
+__device__ unsigned int g_status_word = 0;
+
+cudaError_t status_word(unsigned** ptr) {
+    static std::mutex mu;
+    static unsigned* cached[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return e;
+        cached[dev] = static_cast<unsigned*>(p);
+    }
+    *ptr = cached[dev];
+    return cudaSuccess;
+}
+
+cudaError_t read_and_clear_status(unsigned* host_value, cudaStream_t s) {
+    unsigned* dptr = nullptr;
+    cudaError_t e = status_word(&dptr);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpy(host_value, dptr, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return e;
+    return cudaMemset(dptr, 0, sizeof(unsigned));
+}
+
+cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) {
+    const long long warps = (long long)p.batch * p.H;
+    if (warps <= 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((warps + 3) / 4);
+    if (D == 64)
+        pa_combine_kernel<64><<<grid, 128, 0, s>>>(p, B);
+    else if (D == 128)
+        pa_combine_kernel<128><<<grid, 128, 0, s>>>(p, B);
+    else
+        return cudaErrorNotSupported;
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// KV append: one thread per 16-byte chunk of every (sequence, K/V, kv head) row.
+// Consecutive threads cover consecutive chunks of one row, so both the read of
+// k/v and the write into the pool row are coalesced.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) pa_write_kv_kernel(const WriteParams p) {
+    const int cpr = p.row_bytes / 16;
+    const long long total = (long long)p.batch * 2 * p.Hkv * cpr;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int ci = (int)(i % cpr);
+        long long r = i / cpr;
+        const int kvh = (int)(r % p.Hkv);
+        r /= p.Hkv;
+        const int kv = (int)(r % 2);
+        const int b = (int)(r / 2);
+        const int pos = __ldg(p.positions + b);
+        if (pos < 0 || pos / p.B >= p.maxb) {
+            if (ci == 0 && kvh == 0 && kv == 0) atomicOr(p.status, kStatusBadLength);
+            continue;
+        }
+        const int blk = __ldg(p.bt + (long long)b * p.maxb + pos / p.B);
+        if (blk < 0 || blk >= p.num_blocks) {
+            if (ci == 0 && kvh == 0 && kv == 0) atomicOr(p.status, kStatusBadBlock);
+            continue;
+        }
+        const long long row = ((((long long)blk * 2 + kv) * p.L + p.layer) * p.Hkv + kvh) * p.B +
+                               (pos % p.B);
+        const unsigned char* src = static_cast<const unsigned char*>(kv ? p.v : p.k) +
+                                   ((long long)b * p.Hkv + kvh) * p.row_bytes + ci * 16;
+        unsigned char* dst = static_cast<unsigned char*>(p.pool) + row * p.row_bytes + ci * 16;
+        *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+    }
+}
+
+cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s) {
+    const long long total = (long long)p.batch * 2 * p.Hkv * (p.row_bytes / 16);
+    if (total <= 0) return cudaSuccess;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    pa_write_kv_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Batched gather: copies the first n rows of every sequence into contiguous
+// [batch, max_len, Hkv, D] K and V, zero-fills the rest, writes the mask.
+// One thread per 16-byte chunk of every output row (K and V).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) pa_gather_kv_kernel(const GatherParams p) {
+    const int cpr = p.row_bytes / 16;
+    const long long total = (long long)p.batch * p.max_len * p.Hkv * 2 * cpr;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int ci = (int)(i % cpr);
+        long long r = i / cpr;
+        const int kv = (int)(r % 2);
+        r /= 2;
+        const int kvh = (int)(r % p.Hkv);
+        r /= p.Hkv;
+        const int t = (int)(r % p.max_len);
+        const int b = (int)(r / p.max_len);
+        int n = __ldg(p.lens + b);
+        if (n < 0 || n > p.max_len || n > p.maxb * p.B) {
+            if (t == 0 && kvh == 0 && kv == 0 && ci == 0) atomicOr(p.status, kStatusBadLength);
+            n = 0;
+        }
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        bool valid = t < n;
+        if (valid) {
+            const int blk = __ldg(p.bt + (long long)b * p.maxb + t / p.B);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (kvh == 0 && kv == 0 && ci == 0) atomicOr(p.status, kStatusBadBlock);
+            } else {
+                const long long row =
+                    ((((long long)blk * 2 + kv) * p.L + p.layer) * p.Hkv + kvh) * p.B + (t % p.B);
+                val = __ldg(reinterpret_cast<const uint4*>(
+                    static_cast<const unsigned char*>(p.pool) + row * p.row_bytes + ci * 16));
+            }
+        }
+        const long long orow = ((long long)b * p.max_len + t) * p.Hkv + kvh;
+        unsigned char* dst = static_cast<unsigned char*>(kv ? p.v_out : p.k_out) +
+                             orow * p.row_bytes + ci * 16;
+        *reinterpret_cast<uint4*>(dst) = val;
+        if (kvh == 0 && kv == 0 && ci == 0) p.mask[(long long)b * p.max_len + t] = valid ? 1 : 0;
+    }
+}
+
+cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s) {
+    const long long total = (long long)p.batch * p.max_len * p.Hkv * 2 * (p.row_bytes / 16);
+    if (total <= 0) return cudaSuccess;
+    long long blocks = (total + 255) / 256;
+    const long long cap = (long long)num_sms * 16;
+    if (blocks > cap) blocks = cap;
+    pa_gather_kv_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,83 @@
+// pa_internal.h -- launch interface between the C ABI layer and the kernels.
+// Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// Device status bits (mirror of the public PA_STATUS_* values).
+constexpr unsigned kStatusBadBlock = 0x1u;
+constexpr unsigned kStatusBadLength = 0x2u;
+constexpr unsigned kStatusTimeout = 0x4u;
+
+// Geometry of one pool tensor [num_blocks, 2, L, Hkv, B, D].
+struct PoolGeom {
+    void* base;
+    long long num_blocks;
+    int L, Hkv, B, D;
+    int elt;    // bytes per element (4 = fp32, 2 = bf16)
+    int dtype;  // 0 = fp32, 1 = bf16
+};
+
+struct DecodeParams {
+    float* out;           // [batch, H, D] fp32
+    const void* q;        // [batch, H, D] pool dtype
+    const void* pool;     // pool base
+    long long num_blocks;
+    int L, Hkv, layer;
+    const int* bt;        // [batch, maxb]
+    int maxb;
+    const int* lens;      // [batch]
+    int batch, H;
+    float qscale;         // softmax scale * log2(e): scores live in the base-2 domain
+    float* part_o;        // [batch, H, Cmax, D] unnormalised partial outputs
+    float* part_ml;       // [batch, H, Cmax, 2] (running max, sum of weights)
+    int PB;               // blocks per partition
+    int Cmax;             // partitions per (sequence, kv head) grid slot
+    unsigned* status;     // device status word
+};
+
+struct WriteParams {
+    void* pool;
+    long long num_blocks;
+    int L, Hkv, B, row_bytes, layer;
+    const void* k;
+    const void* v;
+    const int* bt;
+    int maxb;
+    const int* positions;
+    int batch;
+    unsigned* status;
+};
+
+struct GatherParams {
+    void* k_out;
+    void* v_out;
+    uint8_t* mask;
+    const void* pool;
+    long long num_blocks;
+    int L, Hkv, B, row_bytes, layer;
+    const int* bt;
+    int maxb;
+    const int* lens;
+    int batch, max_len;
+    unsigned* status;
+};
+
+// Returns cudaErrorNotSupported (without launching) when no kernel is built
+// for (dtype, D, B, G).
+cudaError_t launch_decode_bf16(const DecodeParams& p, int D, int B, int G, cudaStream_t s);
+cudaError_t launch_decode_f32(const DecodeParams& p, int D, int B, int G, cudaStream_t s);
+bool decode_supported(int dtype, int D, int B, int G);
+
+cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s);
+cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s);
+
+// Device address of the status word of the current device (looked up once per device).
+cudaError_t status_word(unsigned** ptr);
+cudaError_t read_and_clear_status(unsigned* host_value, cudaStream_t s);
+
+}  // namespace pa

@@ -1,0 +1,80 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI
+and the oracle on the same seeded inputs."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from paged_kv_cache_239_gb300 import binding as B
+from paged_kv_cache_239_gb300 import workloads as W
+
+TOL = {"f32": 1e-5, "bf16": 2e-3}
+
+
+class GpuPool:
+    """A pool tensor on the GPU wrapped by a library handle."""
+
+    def __init__(self, wl, pool_t):
+        self.wl = wl
+        self.t = pool_t
+        self.h = B.pa_pool_create(pool_t, wl.num_blocks, wl.num_layers, wl.num_kv_heads,
+                                  wl.block_size, wl.head_dim, pool_t.dtype)
+
+    def close(self):
+        if self.h:
+            B.pa_pool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        self.close()
+
+
+def device_tables(wl, device):
+    bt = torch.from_numpy(np.ascontiguousarray(wl.block_tables)).to(device)
+    lens = torch.from_numpy(np.ascontiguousarray(wl.context_lens)).to(device)
+    return bt, lens
+
+
+def gpu_decode(gp, q, layer, bt, lens, scale=None, partition_blocks=0, stream=None, out=None):
+    wl = gp.wl
+    batch, H, D = q.shape
+    if out is None:
+        out = torch.full((batch, H, D), float("nan"), dtype=torch.float32, device=q.device)
+    need = B.pa_decode_workspace_size(gp.h, batch, H, bt.shape[1], partition_blocks)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device) if need else None
+    B.pa_decode_attention_partitioned(out, q, gp.h, layer, bt, bt.shape[1], lens, batch,
+                                      wl.block_size, H, wl.num_kv_heads, D,
+                                      wl.scale if scale is None else scale, partition_blocks,
+                                      ws, need, stream)
+    return out
+
+
+def oracle_decode(wl, pool_t, q_t, layer, tables=None, lens=None, scale=None):
+    return oracle.decode_attention(W.as_oracle_array(q_t), W.as_oracle_array(pool_t), layer,
+                                   wl.block_tables if tables is None else tables,
+                                   wl.context_lens if lens is None else lens, wl.num_heads,
+                                   wl.scale if scale is None else scale)
+
+
+def oracle_decode_sampled(wl, pool_gpu, q_gpu, layer, seqs, tables=None, lens=None):
+    """Oracle for a few sequences of a pool too large to copy: the blocks each
+    sequence uses (one layer) are copied to the host and the table renumbered."""
+    tables = wl.block_tables if tables is None else tables
+    lens = wl.context_lens if lens is None else lens
+    res = {}
+    for b in seqs:
+        n = int(lens[b])
+        nblk = max(1, -(-n // wl.block_size))
+        ids = torch.from_numpy(tables[b, :nblk].astype(np.int64)).to(pool_gpu.device)
+        sub = pool_gpu.index_select(0, ids)[:, :, layer:layer + 1].contiguous().cpu()
+        q = q_gpu[b:b + 1].cpu()
+        res[b] = oracle.decode_attention(W.as_oracle_array(q), W.as_oracle_array(sub), 0,
+                                         np.arange(nblk, dtype=np.int32)[None], [n],
+                                         wl.num_heads, wl.scale)[0]
+    return res
+
+
+def max_abs_err(gpu_out, ref):
+    g = gpu_out.detach().cpu().double().numpy() if torch.is_tensor(gpu_out) else gpu_out
+    return float(np.max(np.abs(g - ref))) if g.size else 0.0

@@ -1,0 +1,321 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Attention within 1e-5 (fp32 inputs) / 2e-3 (bf16 inputs,
+fp32 accumulation) max-abs; append and gather bit-exact."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.allocator import FreeBlockStack
+from paged_kv_cache_239_gb300 import binding as B
+from paged_kv_cache_239_gb300 import workloads as W
+from gpu_helpers import (TOL, GpuPool, device_tables, gpu_decode, max_abs_err, oracle_decode,
+                         oracle_decode_sampled)
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_status(expected=0):
+    st = B.pa_get_status()
+    assert st == expected, f"device status {st:#x}, expected {expected:#x}"
+
+
+# ---------------------------------------------------------------- small grid
+
+GRID = []
+for dtype in ("f32", "bf16"):
+    for D in (64, 128):
+        for Bs in (16, 32):
+            for G in (1, 2, 4, 8):
+                GRID.append((dtype, D, Bs, G))
+
+
+@pytest.mark.parametrize("dtype,D,Bs,G", GRID)
+def test_decode_grid_all_partitionings(cuda_device, dtype, D, Bs, G):
+    Hkv = 2
+    lens = [1, Bs - 1, Bs, Bs + 1, 3 * Bs + 5, 9 * Bs, 9 * Bs + 7, 0, 2]
+    wl = W.custom("grid", dtype, 2, Hkv * G, Hkv, D, Bs, lens, seed=D + Bs + G, spare_blocks=5,
+                  interleave=True)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    qd = q.to(cuda_device)
+    ref = oracle_decode(wl, pool, q, 1)
+    for pb in (0, 1, 2, 3, wl.max_blocks):
+        out = gpu_decode(gp, qd, 1, bt, ln, partition_blocks=pb)
+        torch.cuda.synchronize()
+        err = max_abs_err(out, ref)
+        assert err <= TOL[dtype], f"partition_blocks={pb}: max abs err {err}"
+        assert torch.isfinite(out).all()
+    _check_status()
+    gp.close()
+
+
+def test_decode_tiny_f32_named(cuda_device):
+    wl = W.named(1)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
+    ref = oracle_decode(wl, pool, q, 0)
+    assert max_abs_err(out, ref) <= 1e-5
+    _check_status()
+
+
+def test_decode_mini_infer_all_layers(cuda_device):
+    wl = W.named(2)
+    pool = W.make_pool(wl)
+    qs = W.make_queries(wl, wl.num_layers)
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    qd = qs.to(cuda_device)
+    worst = 0.0
+    for layer in range(wl.num_layers):
+        out = gpu_decode(gp, qd[layer], layer, bt, ln)
+        ref = oracle_decode(wl, pool, qs[layer], layer)
+        worst = max(worst, max_abs_err(out, ref))
+    assert worst <= 2e-3, worst
+    _check_status()
+
+
+def test_decode_long_context_split(cuda_device):
+    wl = W.named(4)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    pb = B.pa_decode_partition_blocks(gp.h, wl.batch, wl.num_heads, wl.max_blocks)
+    assert pb < wl.max_blocks, "the long-context workload must take the split path"
+    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
+    ref = oracle_decode(wl, pool, q, 0)
+    assert max_abs_err(out, ref) <= 2e-3
+    _check_status()
+
+
+@pytest.mark.slow
+def test_decode_large_batch_sampled(cuda_device):
+    """Full-size large-batch workload (about 71 GB of pool) in the launch
+    configuration the benchmark times; sampled sequences against the oracle."""
+    wl = W.named(3)
+    pool = W.make_pool(wl, device=cuda_device)
+    qs = W.make_queries(wl, 2, device=cuda_device)
+    gp = GpuPool(wl, pool)
+    bt, ln = device_tables(wl, cuda_device)
+    rng = np.random.default_rng(0)
+    order = np.argsort(wl.context_lens)
+    seqs = sorted(set([int(order[0]), int(order[-1])] + [int(x) for x in rng.choice(wl.batch, 10,
+                                                                                     replace=False)]))
+    for layer in (0, wl.num_layers - 1):
+        out = gpu_decode(gp, qs[layer % 2], layer, bt, ln)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out).all()
+        refs = oracle_decode_sampled(wl, pool, qs[layer % 2], layer, seqs)
+        for b, ref in refs.items():
+            assert max_abs_err(out[b], ref) <= 2e-3, (layer, b)
+    _check_status()
+    gp.close()
+    del pool
+    torch.cuda.empty_cache()
+
+
+def test_append_decode_loop(cuda_device):
+    """Workload 5: per step, take a block on a boundary crossing (library
+    allocator on GPU side, oracle free stack on CPU side), append one token,
+    decode over n+1 tokens."""
+    wl = W.named(5)
+    pool = W.make_pool(wl)
+    ks, vs = W.make_new_tokens(wl, wl.steps)
+    qs = W.make_queries(wl, wl.steps)
+    gp = GpuPool(wl, pool.to(cuda_device))
+    host_pool = W.as_oracle_array(pool).copy()
+    # both allocators start from the same free stack (ids still free, pop order)
+    # (the stack's END is popped first: the in-use ids go last and are popped away)
+    used = sorted(int(x) for x in wl.block_tables[wl.block_tables >= 0])
+    full_order = list(wl.free_stack) + used
+    B.pa_pool_seed_free_stack(gp.h, full_order)
+    for _ in range(len(used)):
+        B.pa_alloc_block(gp.h)
+    ref_alloc = FreeBlockStack(wl.num_blocks)
+    ref_alloc.seed(full_order)
+    for _ in range(len(used)):
+        ref_alloc.allocate_block()
+    tables = wl.block_tables.copy()
+    lens = wl.context_lens.copy()
+    bt = torch.from_numpy(tables).to(cuda_device)
+    kd, vd, qd = ks.to(cuda_device), vs.to(cuda_device), qs.to(cuda_device)
+    check_steps = {0, 1, 30, 31, 32, 33, 63}
+    for step in range(wl.steps):
+        for b in range(wl.batch):
+            if lens[b] % wl.block_size == 0:
+                gid = B.pa_alloc_block(gp.h)
+                assert gid == ref_alloc.allocate_block()
+                tables[b, lens[b] // wl.block_size] = gid
+        bt.copy_(torch.from_numpy(tables))
+        pos = torch.from_numpy(lens.copy()).to(cuda_device)
+        B.pa_write_kv(gp.h, 0, kd[step], vd[step], bt, wl.max_blocks, pos, wl.batch)
+        oracle.write_kv(host_pool, 0, W.as_oracle_array(ks[step]), W.as_oracle_array(vs[step]),
+                        tables, lens)
+        lens = lens + 1
+        ln = torch.from_numpy(lens.copy()).to(cuda_device)
+        out = gpu_decode(gp, qd[step], 0, bt, ln)
+        if step in check_steps:
+            ref = oracle.decode_attention(W.as_oracle_array(qs[step]), host_pool, 0, tables, lens,
+                                          wl.num_heads, wl.scale)
+            assert max_abs_err(out, ref) <= 2e-3, step
+    torch.cuda.synchronize()
+    assert np.array_equal(W.as_oracle_array(gp.t), host_pool), "pool bytes differ after appends"
+    _check_status()
+
+
+# ---------------------------------------------------------------- append / gather
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+def test_write_kv_bit_exact(cuda_device, cfg):
+    wl = W.named(cfg)
+    if cfg == 3:  # same geometry, small pool: the append does not depend on pool size
+        wl = W.custom("wk3", "bf16", 32, 32, 8, 128, 16, wl.context_lens[:64], seed=5)
+    pool = W.make_pool(wl)
+    ks, vs = W.make_new_tokens(wl, 1)
+    layer = wl.num_layers - 1
+    # positions: the last cached slot of each sequence (always inside its table)
+    pos = np.maximum(wl.context_lens - 1, 0).astype(np.int32)
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, _ = device_tables(wl, cuda_device)
+    B.pa_write_kv(gp.h, layer, ks[0].to(cuda_device), vs[0].to(cuda_device), bt, wl.max_blocks,
+                  torch.from_numpy(pos).to(cuda_device), wl.batch)
+    host = W.as_oracle_array(pool).copy()
+    oracle.write_kv(host, layer, W.as_oracle_array(ks[0]), W.as_oracle_array(vs[0]),
+                    wl.block_tables, pos)
+    torch.cuda.synchronize()
+    assert np.array_equal(W.as_oracle_array(gp.t), host)
+    _check_status()
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 5])
+def test_gather_kv_bit_exact(cuda_device, cfg):
+    wl = W.named(cfg)
+    pool = W.make_pool(wl)
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    T = int(wl.context_lens.max()) + 3
+    layer = wl.num_layers // 2
+    k_ref, v_ref, m_ref = oracle.gather_kv(W.as_oracle_array(pool), layer, wl.block_tables,
+                                           wl.context_lens, T)
+    dt = W.torch_dtype(wl)
+    shape = (wl.batch, T, wl.num_kv_heads, wl.head_dim)
+    k = torch.full(shape, 7, dtype=dt, device=cuda_device)
+    v = torch.full(shape, 7, dtype=dt, device=cuda_device)
+    m = torch.full((wl.batch, T), 9, dtype=torch.uint8, device=cuda_device)
+    B.pa_gather_kv(k, v, m, gp.h, layer, bt, wl.max_blocks, ln, wl.batch, T)
+    torch.cuda.synchronize()
+    assert np.array_equal(W.as_oracle_array(k), k_ref)
+    assert np.array_equal(W.as_oracle_array(v), v_ref)
+    assert np.array_equal(m.cpu().numpy().astype(bool), m_ref)
+    _check_status()
+
+
+# ---------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_single_token_is_exact(cuda_device, dtype):
+    wl = W.custom("one", dtype, 1, 8, 2, 128, 16, [1, 1, 1, 1], seed=3, spare_blocks=3)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln).cpu()
+    ref = oracle_decode(wl, pool, q, 0)
+    assert np.array_equal(out.double().numpy(), ref)
+
+
+def test_empty_and_full_tables(cuda_device):
+    Bs, maxb = 16, 6
+    lens = [0, maxb * Bs, 0, maxb * Bs - 1]
+    wl = W.custom("edge", "bf16", 1, 8, 2, 64, Bs, lens, seed=12, max_blocks=maxb)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    ref = oracle_decode(wl, pool, q, 0)
+    for pb in (0, 1, 4):
+        out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln, partition_blocks=pb)
+        o = out.cpu()
+        assert torch.all(o[0] == 0) and torch.all(o[2] == 0)
+        assert max_abs_err(o, ref) <= 2e-3
+    _check_status()
+
+
+def test_zero_scale_and_batch_zero(cuda_device):
+    wl = W.custom("z", "f32", 1, 4, 2, 64, 16, [5, 40], seed=2)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln, scale=0.0)
+    ref = oracle_decode(wl, pool, q, 0, scale=0.0)
+    assert max_abs_err(out, ref) <= 1e-5
+    # batch 0 launches nothing
+    B.pa_decode_attention(None, None, gp.h, 0, None, 4, None, 0, 16, 4, 2, 64, 1.0, None, 0)
+    _check_status()
+
+
+def test_bad_block_id_is_flagged_not_faulted(cuda_device):
+    wl = W.custom("bad", "bf16", 1, 4, 2, 64, 16, [40, 40, 40], seed=6, spare_blocks=2)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    tables = wl.block_tables.copy()
+    tables[1, 1] = wl.num_blocks + 1000   # out of range
+    tables[2, 2] = -5
+    bt = torch.from_numpy(tables).to(cuda_device)
+    ln = torch.from_numpy(wl.context_lens).to(cuda_device)
+    _check_status()
+    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln).cpu()
+    st = B.pa_get_status()
+    assert st & B.PA_STATUS_BAD_BLOCK_ID
+    ref = oracle_decode(wl, pool, q, 0)
+    assert max_abs_err(out[0], ref[0]) <= 2e-3   # untouched sequence is still right
+    assert torch.isfinite(out).all()
+    # append through a bad id is skipped and flagged
+    k, v = W.make_new_tokens(wl, 1)
+    before = gp.t.clone()
+    B.pa_write_kv(gp.h, 0, k[0].to(cuda_device), v[0].to(cuda_device), bt, wl.max_blocks,
+                  torch.tensor([20, 20, 39], dtype=torch.int32, device=cuda_device), 3)
+    st = B.pa_get_status()
+    assert st & B.PA_STATUS_BAD_BLOCK_ID
+    changed = (gp.t != before).reshape(wl.num_blocks, -1).any(dim=1).nonzero().flatten().tolist()
+    assert changed == [int(tables[0, 1])]
+
+
+def test_bad_length_is_flagged(cuda_device):
+    wl = W.custom("len", "bf16", 1, 4, 2, 64, 16, [20, 20], seed=7)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, _ = device_tables(wl, cuda_device)
+    ln = torch.tensor([20, wl.max_blocks * 16 + 1], dtype=torch.int32, device=cuda_device)
+    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln).cpu()
+    assert B.pa_get_status() & B.PA_STATUS_BAD_LENGTH
+    assert torch.all(out[1] == 0)
+
+
+def test_decode_on_side_stream_matches(cuda_device):
+    wl = W.custom("stream", "bf16", 2, 16, 4, 128, 32, [100, 250, 3, 64], seed=13)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    s = torch.cuda.Stream()
+    qd = q.to(cuda_device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        out = gpu_decode(gp, qd, 1, bt, ln, stream=s, partition_blocks=2)
+    s.synchronize()
+    assert max_abs_err(out, oracle_decode(wl, pool, q, 1)) <= 2e-3
+    _check_status()
