@@ -187,6 +187,37 @@ int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_heads,
 int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
                              int max_blocks_per_seq, int partition_blocks, size_t* bytes);
 
+/*
+ * Decode attention for callers that cannot allocate device memory while they
+ * run -- e.g. an operator called from another engine's execution step, where
+ * that engine owns all device memory and forbids cudaMalloc (which can block on
+ * the device and fails once the memory has been reserved).  The source pages
+ * have no counterpart to this call; it exists for such callers only.
+ *
+ * Same arguments and results as pa_decode_attention_partitioned, without the
+ * workspace: the split-K partials go to a fixed device array of
+ * PA_NOALLOC_SCRATCH_BYTES compiled into the library, which every device that
+ * loads the library's kernels holds until the process exits.  The call makes
+ * no cudaMalloc/cudaFree and no allocating library call.
+ *  - A call that needs more scratch than PA_NOALLOC_SCRATCH_BYTES (see
+ *    pa_decode_workspace_size) fails with PA_ERR_WORKSPACE before any launch;
+ *    a larger partition_blocks needs less.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array and it keeps the last call's contents.
+ *    Nothing in it needs clearing: every partial a call reads was written
+ *    earlier in the same call.  Calls that overlap on the GPU (other streams,
+ *    other host threads) race on it: serialise them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+int pa_decode_attention_noalloc(float* out, const void* q, const pa_pool* pool, int layer,
+                                const int* block_tables, int max_blocks_per_seq,
+                                const int* context_lens, int batch, int block_size,
+                                int num_heads, int num_kv_heads, int head_dim, float scale,
+                                int partition_blocks, pa_stream_t stream);
+
 /* ----------------------------------------------------------------------------
  * Batched gather (mini-infer "Zero-Copy Batched Attention Gather").
  * ------------------------------------------------------------------------- */

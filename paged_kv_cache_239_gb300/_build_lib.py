@@ -20,7 +20,8 @@ LIB_NAME = "libpagedattn.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["pa_api.cpp", "pa_aux.cu", "pa_decode_bf16.cu", "pa_decode_f32.cu"]
+SOURCES = ["pa_api.cpp", "pa_aux.cu", "pa_decode_bf16.cu", "pa_decode_f32.cu",
+           "pa_decode_noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -75,6 +75,8 @@ _SIGNATURES = {
         [_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
     "pa_decode_partition_blocks": ([_P, _I, _I, _I, _PI], _I),
     "pa_decode_workspace_size": ([_P, _I, _I, _I, _I, _PSZ], _I),
+    "pa_decode_attention_noalloc": (
+        [_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pa_gather_kv": ([_P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P], _I),
     "pa_get_status": ([_PU, _P], _I),
 }
@@ -248,6 +250,21 @@ def pa_decode_attention_partitioned(out, q, pool: int, layer: int, block_tables,
         _ptr(context_lens), batch, block_size, num_heads, num_kv_heads, head_dim, float(scale),
         partition_blocks, _ptr(workspace), workspace_bytes, _stream(stream)),
         "pa_decode_attention_partitioned")
+
+
+PA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def pa_decode_attention_noalloc(out, q, pool: int, layer: int, block_tables,
+                                max_blocks_per_seq: int, context_lens, batch: int,
+                                block_size: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                                scale: float, partition_blocks: int = 0, stream=None) -> None:
+    """Decode attention whose split-K scratch is the library's fixed device
+    array (no device allocation by this call); see the header for its limits."""
+    _check(lib().pa_decode_attention_noalloc(
+        _ptr(out), _ptr(q), pool, layer, _ptr(block_tables), max_blocks_per_seq,
+        _ptr(context_lens), batch, block_size, num_heads, num_kv_heads, head_dim, float(scale),
+        partition_blocks, _stream(stream)), "pa_decode_attention_noalloc")
 
 
 def pa_gather_kv(k_out, v_out, mask, pool: int, layer: int, block_tables, max_blocks_per_seq: int,

@@ -141,6 +141,8 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
 }  // namespace
 
 namespace pa {
+int set_last_error(int code, const char* message) { return fail(code, "%s", message); }
+
 bool decode_supported(int dtype, int D, int B, int G) {
     if (dtype != 0 && dtype != 1) return false;
     if (D != 64 && D != 128) return false;

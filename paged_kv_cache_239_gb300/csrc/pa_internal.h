@@ -76,6 +76,9 @@ cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s);
 cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s);
 
+// Records `message` as the calling thread's last error; returns `code`.
+int set_last_error(int code, const char* message);
+
 // Device address of the status word of the current device (looked up once per device).
 cudaError_t status_word(unsigned** ptr);
 cudaError_t read_and_clear_status(unsigned* host_value, cudaStream_t s);

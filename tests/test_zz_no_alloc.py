@@ -1,0 +1,75 @@
+"""pa_decode_attention_noalloc: decode for callers that cannot allocate device
+memory while they run (an operator inside another engine that owns all device
+memory and forbids cudaMalloc during its execution step).  Its split-K partials
+live in a fixed device array compiled into the library instead of a caller's
+workspace.  The source pages have no counterpart to this call.
+
+The test compares it, through the C ABI, with pa_decode_attention_partitioned
+given an ordinary workspace, on two calls in a row (the second call must not be
+disturbed by what the first left in the shared array), and checks that a call
+needing more than the fixed array is refused before anything is launched.
+This file is named to be collected last."""
+import numpy as np
+import pytest
+import torch
+
+from paged_kv_cache_239_gb300 import binding as B
+from paged_kv_cache_239_gb300 import workloads as W
+from gpu_helpers import TOL, GpuPool, device_tables, gpu_decode, max_abs_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(gp, q, layer, bt, ln, partition_blocks):
+    wl = gp.wl
+    batch, H, D = q.shape
+    out = torch.full((batch, H, D), float("nan"), dtype=torch.float32, device=q.device)
+    B.pa_decode_attention_noalloc(out, q, gp.h, layer, bt, bt.shape[1], ln, batch,
+                                  wl.block_size, H, wl.num_kv_heads, D, wl.scale,
+                                  partition_blocks)
+    return out
+
+
+@pytest.mark.parametrize("partition_blocks", [3, 0])
+def test_noalloc_matches_workspace_entry_point(cuda_device, partition_blocks):
+    wl = W.custom("noalloc", "bf16", 2, 32, 8, 128, 32, [4000, 9000, 1, 700, 0, 2048, 33],
+                  seed=77, spare_blocks=9)
+    pool = W.make_pool(wl)
+    qs = W.make_queries(wl, 2)
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    qd = qs.to(cuda_device)
+    need = B.pa_decode_workspace_size(gp.h, wl.batch, wl.num_heads, wl.max_blocks,
+                                      partition_blocks)
+    assert 0 < need <= B.PA_NOALLOC_SCRATCH_BYTES, "the case must use split-K scratch"
+    # two calls in a row: different layer and query, the array is reused
+    for layer in (0, 1):
+        ref = gpu_decode(gp, qd[layer], layer, bt, ln, partition_blocks=partition_blocks)
+        got = _noalloc(gp, qd[layer], layer, bt, ln, partition_blocks)
+        torch.cuda.synchronize()
+        assert torch.isfinite(got).all()
+        assert max_abs_err(got, ref.cpu().double().numpy()) <= TOL["bf16"], layer
+    assert B.pa_get_status() == 0
+    gp.close()
+
+
+def test_noalloc_refuses_oversized_scratch(cuda_device):
+    wl = W.custom("big", "bf16", 1, 32, 8, 128, 32, [131072] * 4, seed=5)
+    pool = torch.zeros((1, 2, 1, 8, 32, 128), dtype=torch.bfloat16, device=cuda_device)
+    h = B.pa_pool_create(pool, 1, 1, 8, 32, 128, pool.dtype)
+    try:
+        bt = torch.zeros((4, wl.max_blocks), dtype=torch.int32, device=cuda_device)
+        ln = torch.zeros(4, dtype=torch.int32, device=cuda_device)
+        out = torch.zeros((4, 32, 128), dtype=torch.float32, device=cuda_device)
+        q = torch.zeros((4, 32, 128), dtype=torch.bfloat16, device=cuda_device)
+        need = B.pa_decode_workspace_size(h, 4, 32, wl.max_blocks, 1)
+        assert need > B.PA_NOALLOC_SCRATCH_BYTES
+        with pytest.raises(B.PagedAttnError) as e:
+            B.pa_decode_attention_noalloc(out, q, h, 0, bt, wl.max_blocks, ln, 4, 32, 32, 8,
+                                          128, 1.0, 1)
+        assert e.value.code == B.PA_ERR_WORKSPACE
+        assert "scratch" in str(e.value)
+        torch.cuda.synchronize()
+        assert bool((out == 0).all())
+    finally:
+        B.pa_pool_destroy(h)
