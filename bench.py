@@ -18,6 +18,7 @@ max over ranks is reported.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -55,6 +56,31 @@ def decode_bytes(wl) -> int:
 
 def decode_flops(wl) -> int:
     return int(wl.context_lens.astype(np.int64).sum()) * 4 * wl.num_heads * wl.head_dim
+
+
+# DRAM bytes (read + write) of one pa_decode_kernel launch on this workload,
+# from `ncu --set full` (profiles/pa_decode_kernel__large_batch_*.md), valid only
+# for the kernel sources they were taken from.
+DECODE_TRAFFIC = {
+    "bytes_per_launch": 2223014000 + 6228480,
+    "sources_sha256": "d472b81370cc6a2abb2460c285814a52cd86a657cb4dfc3aef8672e6c3a4cbce",
+}
+DECODE_SOURCES = ["pa_decode.cuh", "pa_decode_launch.cuh", "pa_decode_bf16.cu", "pa_device.cuh"]
+
+
+def decode_sources_sha256() -> str:
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        with open(os.path.join(REPO, "paged_kv_cache_239_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def decode_traffic():
+    """Per-launch DRAM traffic of the decode kernel, or None if it changed since the capture."""
+    if decode_sources_sha256() == DECODE_TRAFFIC["sources_sha256"]:
+        return DECODE_TRAFFIC["bytes_per_launch"]
+    return None
 
 
 def measured_peaks():
@@ -406,7 +432,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "decode_tokens_per_s": wl.batch * steps * world / (total_ms / 1e3),
         "roofline": {"bound": "hbm", "kernel": "pa_decode_attention (decode + combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": decode_traffic(),
+                     "traffic_kernel": "pa_decode_kernel (ncu dram read+write per launch)",
                      "algorithmic_bytes_per_call": per_call,
                      "avg_call_ms": call_avg_ms},
         "cpu_baseline": cpu,

@@ -47,6 +47,13 @@
 extern "C" {
 #endif
 
+/* Every entry point below is exported; the library hides all other symbols. */
+#if defined(__GNUC__) || defined(__clang__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
 /* Opaque pool handle: geometry + device pointer + host free-block stack. */
 typedef struct pa_pool pa_pool;
 
@@ -73,7 +80,7 @@ enum {
 #define PA_STATUS_TIMEOUT 0x4u      /* a bounded wait for a shared-memory copy gave up */
 
 /* Human-readable description of the calling thread's last error ("" if none). */
-const char* pa_last_error_string(void);
+PA_API const char* pa_last_error_string(void);
 
 /* ----------------------------------------------------------------------------
  * Pool and allocator (host only; none of these calls touches the GPU).
@@ -88,31 +95,31 @@ const char* pa_last_error_string(void);
  * The free stack starts as 0..num_blocks-1; pa_alloc_block pops the END, so
  * the first id handed out is num_blocks-1.
  */
-int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers,
+PA_API int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers,
                    int num_kv_heads, int block_size, int head_dim, pa_dtype dtype);
 
 /* Release the handle (not the caller's device tensor).  NULL is accepted. */
-int pa_pool_destroy(pa_pool* pool);
+PA_API int pa_pool_destroy(pa_pool* pool);
 
 /* Bytes of one physical block: 2 * num_layers * num_kv_heads * block_size *
  * head_dim * element size (K and V of every layer and KV head). */
-int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes);
+PA_API int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes);
 
 /* Replace the free stack by `order` (a permutation of 0..num_blocks-1, n ==
  * num_blocks); allowed only while every block is free.  The LAST entry is
  * handed out first. */
-int pa_pool_seed_free_stack(pa_pool* pool, const int* order, int n);
+PA_API int pa_pool_seed_free_stack(pa_pool* pool, const int* order, int n);
 
 /* Pop one block id from the free stack.  PA_ERR_NO_FREE_BLOCKS when empty
  * ("Out of KV-Cache Physical Blocks"). */
-int pa_alloc_block(pa_pool* pool, int* block_id);
+PA_API int pa_alloc_block(pa_pool* pool, int* block_id);
 
 /* Push `block_id` back; it becomes the next id handed out.  Ids outside the
  * pool are PA_ERR_INVALID_ARG, ids not currently allocated PA_ERR_DOUBLE_FREE. */
-int pa_free_block(pa_pool* pool, int block_id);
+PA_API int pa_free_block(pa_pool* pool, int block_id);
 
 /* Number of ids on the free stack. */
-int pa_num_free(const pa_pool* pool, int* n);
+PA_API int pa_num_free(const pa_pool* pool, int* n);
 
 /* ----------------------------------------------------------------------------
  * KV append (reshape-and-cache).
@@ -130,7 +137,7 @@ int pa_num_free(const pa_pool* pool, int* n);
  * Rows whose position or block id is out of range are skipped and flagged in
  * the status word (PA_STATUS_BAD_LENGTH / PA_STATUS_BAD_BLOCK_ID).
  */
-int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
+PA_API int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
                 const int* block_tables, int max_blocks_per_seq, const int* positions,
                 int batch, pa_stream_t stream);
 
@@ -157,7 +164,7 @@ int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
  * heuristically chosen number of blocks; with more than one partition a second
  * kernel merges the per-partition results (log-sum-exp combine).
  */
-int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int layer,
+PA_API int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int layer,
                         const int* block_tables, int max_blocks_per_seq,
                         const int* context_lens, int batch, int block_size, int num_heads,
                         int num_kv_heads, int head_dim, float scale, void* workspace,
@@ -169,7 +176,7 @@ int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int laye
  * A partition covering the whole table (partition_blocks >= max_blocks_per_seq)
  * runs a single kernel and needs no workspace.
  */
-int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
+PA_API int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
                                     const int* block_tables, int max_blocks_per_seq,
                                     const int* context_lens, int batch, int block_size,
                                     int num_heads, int num_kv_heads, int head_dim, float scale,
@@ -178,13 +185,13 @@ int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* po
 
 /* The partition size (in blocks) that pa_decode_attention picks for these
  * sizes on the current device.  Queries the device's SM count. */
-int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_heads,
+PA_API int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_heads,
                                int max_blocks_per_seq, int* partition_blocks);
 
 /* Workspace bytes needed by pa_decode_attention_partitioned with the same
  * arguments (partition_blocks = 0: the heuristic choice, which queries the
  * current device).  0 when a single partition covers the table. */
-int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
+PA_API int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
                              int max_blocks_per_seq, int partition_blocks, size_t* bytes);
 
 /*
@@ -212,7 +219,7 @@ int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
  */
 #define PA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
-int pa_decode_attention_noalloc(float* out, const void* q, const pa_pool* pool, int layer,
+PA_API int pa_decode_attention_noalloc(float* out, const void* q, const pa_pool* pool, int layer,
                                 const int* block_tables, int max_blocks_per_seq,
                                 const int* context_lens, int batch, int block_size,
                                 int num_heads, int num_kv_heads, int head_dim, float scale,
@@ -230,7 +237,7 @@ int pa_decode_attention_noalloc(float* out, const void* q, const pa_pool* pool, 
  * [batch, max_len].  Lengths above max_len or above the table are flagged
  * (PA_STATUS_BAD_LENGTH) and treated as 0.
  */
-int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, int layer,
+PA_API int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, int layer,
                  const int* block_tables, int max_blocks_per_seq, const int* context_lens,
                  int batch, int max_len, pa_stream_t stream);
 
@@ -240,7 +247,7 @@ int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, i
 
 /* Wait for `stream`, return the current device's status bits (PA_STATUS_*)
  * accumulated since the last call, and clear them.  Blocking. */
-int pa_get_status(unsigned int* status, pa_stream_t stream);
+PA_API int pa_get_status(unsigned int* status, pa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -50,7 +50,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)
     nvcc = _nvcc()
-    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
+    common = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+              "-I", INCLUDE, "-I", CSRC,
               *ARCH, *extra_flags]
     if verbose:
         common += ["-Xptxas", "-v"]

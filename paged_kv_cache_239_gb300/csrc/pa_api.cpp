@@ -61,11 +61,13 @@ int num_sms_current(int* out) {
     return PA_OK;
 }
 
-// Partition size heuristic: about 256 KiB of K+V per CTA, shrunk (down to
-// 16 KiB) while the grid would hold fewer than four CTAs per SM.
+// Partition size heuristic: about 512 KiB of K+V per CTA (on GB300 the
+// large-batch workload runs fastest at 256-1024 KiB per CTA: fewer partials to
+// combine, fewer idle grid slots), shrunk (down to 16 KiB) while the grid would
+// hold fewer than four CTAs per SM.
 int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sms) {
     const long long blk_bytes = 2LL * g.B * g.D * g.elt;
-    long long pb = (256LL * 1024) / blk_bytes;
+    long long pb = (512LL * 1024) / blk_bytes;
     if (pb < 1) pb = 1;
     if (pb > maxb) pb = maxb;
     while (pb > 1) {

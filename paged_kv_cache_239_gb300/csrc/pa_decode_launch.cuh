@@ -11,12 +11,15 @@ namespace pa {
 
 constexpr int kDecodeWarps = 4;
 
-// Pipeline depth from the stage size: keep roughly 24 KiB in flight per warp.
+// Pipeline depth per warp.  Two stages of >= 8 KiB keep a 4-warp CTA at about
+// 66 KiB of shared memory, so three CTAs (12 warps) fit on an SM; measured on
+// GB300 this beats three stages at two CTAs per SM by ~20% (the kernel is
+// latency-bound at 8 warps per SM).  Small stages (4 KiB) take four.
 template <typename T, int D, int B>
 constexpr int decode_stages() {
     constexpr int R = B < 16 ? B : 16;
     constexpr int stage = 2 * R * D * (int)sizeof(T);
-    return stage <= 4096 ? 4 : (stage <= 8192 ? 3 : 2);
+    return stage <= 4096 ? 4 : 2;
 }
 
 template <typename T, int D, int B, int G>
