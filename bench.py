@@ -163,6 +163,14 @@ def max_over_ranks(values, world: int, device="cpu"):
     return [float(x) for x in t.cpu()]
 
 
+def l2_note(wl, L) -> str:
+    kv = int(wl.context_lens.astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    if kv > 129e6:
+        return f"inputs larger than L2 ({kv / 1e9:.2f} GB of K/V per layer vs 129 MB L2), no flush"
+    return (f"K/V per layer {kv / 1e6:.1f} MB < L2; consecutive layers read disjoint pool "
+            f"slices ({kv * L / 1e6:.0f} MB per step), no flush")
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -266,7 +274,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     B.lib()
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
-    wl = W.named(WORKLOAD_CFG)
+    wl = W.named(args.workload)
     if args.pool_layers > 0:   # smaller pool (same lengths/tables) for profiler captures
         wl.num_layers = min(args.pool_layers, wl.num_layers)
     L = wl.num_layers if args.layers <= 0 else min(args.layers, wl.num_layers)
@@ -283,14 +291,28 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     outs = torch.empty((L, wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream
+    cur = {"sp": stream.cuda_stream}
     lib = B.lib()
     cmax = -(-wl.max_blocks // pb)
-    launches_per_step = L * (2 + (1 if cmax > 1 else 0))
+    launches_per_step = L * ((1 if args.fused else 2) + (1 if cmax > 1 else 0))
 
     def layer_call(l, ev=None):
+        if args.fused:
+            if ev is not None:
+                ev[0].record(stream)
+            rc = lib.pa_write_kv_and_decode(outs[l].data_ptr(), qs[l].data_ptr(), h, l,
+                                            ks[l].data_ptr(), vs[l].data_ptr(),
+                                            positions.data_ptr(), bt.data_ptr(), wl.max_blocks,
+                                            lens.data_ptr(), wl.batch, wl.block_size,
+                                            wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.scale,
+                                            0, ws.data_ptr(), ws_bytes, cur["sp"])
+            if rc:
+                raise RuntimeError(B.last_error())
+            if ev is not None:
+                ev[1].record(stream)
+            return
         rc = lib.pa_write_kv(h, l, ks[l].data_ptr(), vs[l].data_ptr(), bt.data_ptr(),
-                             wl.max_blocks, positions.data_ptr(), wl.batch, sp)
+                             wl.max_blocks, positions.data_ptr(), wl.batch, cur["sp"])
         if rc:
             raise RuntimeError(B.last_error())
         if ev is not None:
@@ -298,7 +320,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         rc = lib.pa_decode_attention(outs[l].data_ptr(), qs[l].data_ptr(), h, l, bt.data_ptr(),
                                      wl.max_blocks, lens.data_ptr(), wl.batch, wl.block_size,
                                      wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.scale,
-                                     ws.data_ptr(), ws_bytes, sp)
+                                     ws.data_ptr(), ws_bytes, cur["sp"])
         if rc:
             raise RuntimeError(B.last_error())
         if ev is not None:
@@ -317,6 +339,23 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     if st:
         raise RuntimeError(f"device status {st:#x} after warm-up")
 
+    # ---- optional: one whole step captured as a CUDA graph ----
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            cur["sp"] = side.cuda_stream
+            with torch.cuda.graph(graph, stream=side):
+                for l in range(L):
+                    layer_call(l)
+            cur["sp"] = stream.cuda_stream
+        stream.wait_stream(side)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
     # ---- timed region: device-resident inputs ----
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
             for _ in range(L)] for _ in range(args.steps)]
@@ -327,13 +366,19 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     with ClockSampler(torch.cuda.current_device()) as clocks:
         t_start.record(stream)
         for s in range(args.steps):
-            for l in range(L):
-                layer_call(l, evs[s][l])
+            if graph is not None:
+                graph.replay()
+            else:
+                for l in range(L):
+                    layer_call(l, evs[s][l])
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
     total_ms = t_start.elapsed_time(t_end)
-    call_ms = [a.elapsed_time(b) for row in evs for (a, b) in row]
+    if graph is not None:   # no per-call events inside a replay: the step bounds each call
+        call_ms = [total_ms / (args.steps * L)]
+    else:
+        call_ms = [a.elapsed_time(b) for row in evs for (a, b) in row]
     st = B.pa_get_status()
     if st:
         raise RuntimeError(f"device status {st:#x} after the timed region")
@@ -358,8 +403,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             bt.copy_(bt_h, non_blocking=True)
             lens.copy_(lens_h, non_blocking=True)
             positions.copy_(pos_h, non_blocking=True)
-            for l in range(L):
-                layer_call(l)
+            if graph is not None:
+                graph.replay()
+            else:
+                for l in range(L):
+                    layer_call(l)
             out_h.copy_(outs, non_blocking=True)
 
         for _ in range(max(1, args.warmup // 2)):
@@ -423,9 +471,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             "workload": wl.name, "batch": wl.batch, "num_heads": wl.num_heads,
             "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
             "block_size": wl.block_size, "num_layers": L,
-            "context_lens": f"U[128,4096] seed {wl.seed}, mean {wl.context_lens.mean():.0f}",
+            "context_lens": f"seed {wl.seed}, min {wl.context_lens.min()}, max "
+                            f"{wl.context_lens.max()}, mean {wl.context_lens.mean():.0f}",
+            "cuda_graph": bool(args.graph),
             "pool_gb": round(wl.pool_bytes() / 1e9, 1), "partition_blocks": pb,
-            "l2": "inputs larger than L2 (2.2 GB of K/V per layer vs 129 MB L2), no flush",
+            "l2": l2_note(wl, L),
             "parallelism": f"replicas x{world}",
         },
         "pct_hbm_peak": 100.0 * value / peak,
@@ -447,17 +497,244 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     B.pa_pool_destroy(h)
 
 
+def _setup(args, local_rank, cfg):
+    import torch
+
+    from paged_kv_cache_239_gb300 import _build_lib
+    from paged_kv_cache_239_gb300 import binding as B
+    from paged_kv_cache_239_gb300 import workloads as W
+
+    _build_lib.build()
+    B.lib()
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    return torch, B, W, dev, W.named(cfg)
+
+
+def run_gather(args, local_rank: int) -> None:
+    """Row N1: bandwidth of pa_gather_kv over every layer of a workload."""
+    torch, B, W, dev, wl = _setup(args, local_rank, args.workload)
+    pool = W.make_pool(wl, device=dev)
+    h = B.pa_pool_create(pool, wl.num_blocks, wl.num_layers, wl.num_kv_heads, wl.block_size,
+                         wl.head_dim, pool.dtype)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    lens = torch.from_numpy(wl.context_lens).to(dev)
+    T = int(wl.context_lens.max())
+    shape = (wl.batch, T, wl.num_kv_heads, wl.head_dim)
+    k = torch.empty(shape, dtype=pool.dtype, device=dev)
+    v = torch.empty(shape, dtype=pool.dtype, device=dev)
+    m = torch.empty((wl.batch, T), dtype=torch.uint8, device=dev)
+    L = wl.num_layers
+
+    def step():
+        for l in range(L):
+            B.pa_gather_kv(k, v, m, h, l, bt, wl.max_blocks, lens, wl.batch, T)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (args.steps * L)
+    rd = int(wl.context_lens.astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    wr = 2 * wl.batch * T * wl.num_kv_heads * wl.head_dim * wl.elem_bytes + wl.batch * T
+    nb = rd + wr + int(sum(-(-int(n) // wl.block_size) for n in wl.context_lens)) * 4
+    peak, kind = measured_peaks()
+    gbs = nb / (ms / 1e3) / 1e9
+    assert B.pa_get_status() == 0
+    print(json.dumps({"row": "gather", "workload": wl.name, "value": gbs, "unit": UNIT,
+                      "ms_per_call": ms, "bytes_per_call": nb, "read_bytes": rd,
+                      "write_bytes": wr, "frac_of_peak": gbs / peak,
+                      "peak": peak, "peak_source": f"{kind} hbm_gbs", "steps": args.steps,
+                      "layers": L}), flush=True)
+    B.pa_pool_destroy(h)
+
+
+def run_loop(args, local_rank: int) -> None:
+    """The append+decode loop (workload 5 by default): every step takes a block
+    for each sequence crossing a block boundary (host free stack), copies the
+    changed table rows, appends one token per sequence and decodes over n+1.
+    One run = `steps_per_run` steps from the initial state; the allocator and
+    tables are reset between runs (untimed)."""
+    torch, B, W, dev, wl = _setup(args, local_rank, 5 if args.workload == WORKLOAD_CFG
+                                  else args.workload)
+    nsteps = wl.steps or 64
+    pool = W.make_pool(wl, device=dev)
+    ks, vs = W.make_new_tokens(wl, nsteps, device=dev)
+    qs = W.make_queries(wl, nsteps, device=dev)
+    h = B.pa_pool_create(pool, wl.num_blocks, wl.num_layers, wl.num_kv_heads, wl.block_size,
+                         wl.head_dim, pool.dtype)
+    used = sorted(int(x) for x in wl.block_tables[wl.block_tables >= 0])
+    order = list(wl.free_stack) + used
+    bt = torch.from_numpy(wl.block_tables.copy()).to(dev)
+    lens_d = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+    pos_d = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    ws_b = B.pa_decode_workspace_size(h, wl.batch, wl.num_heads, wl.max_blocks, 0)
+    ws = torch.empty(max(ws_b, 1), dtype=torch.uint8, device=dev)
+    lens_pin = torch.empty(wl.batch, dtype=torch.int32).pin_memory()
+    pos_pin = torch.empty(wl.batch, dtype=torch.int32).pin_memory()
+    row_pin = torch.empty(wl.max_blocks, dtype=torch.int32).pin_memory()
+
+    def reset():
+        torch.cuda.synchronize()
+        nonlocal h
+        B.pa_pool_destroy(h)
+        h = B.pa_pool_create(pool, wl.num_blocks, wl.num_layers, wl.num_kv_heads,
+                             wl.block_size, wl.head_dim, pool.dtype)
+        B.pa_pool_seed_free_stack(h, order)
+        for _ in used:
+            B.pa_alloc_block(h)
+        bt.copy_(torch.from_numpy(wl.block_tables))
+        torch.cuda.synchronize()
+
+    def run():
+        lens = wl.context_lens.copy()
+        tables = wl.block_tables.copy()
+        for s in range(nsteps):
+            for b in np.nonzero(lens % wl.block_size == 0)[0]:
+                blk = B.pa_alloc_block(h)
+                j = lens[b] // wl.block_size
+                tables[b, j] = blk
+                bt[b, j:j + 1].copy_(torch.tensor([blk], dtype=torch.int32), non_blocking=True)
+            pos_pin.copy_(torch.from_numpy(lens))
+            pos_d.copy_(pos_pin, non_blocking=True)
+            B.pa_write_kv(h, 0, ks[s], vs[s], bt, wl.max_blocks, pos_d, wl.batch)
+            lens = lens + 1
+            lens_pin.copy_(torch.from_numpy(lens))
+            lens_d.copy_(lens_pin, non_blocking=True)
+            B.pa_decode_attention(out, qs[s], h, 0, bt, wl.max_blocks, lens_d, wl.batch,
+                                  wl.block_size, wl.num_heads, wl.num_kv_heads, wl.head_dim,
+                                  wl.scale, ws, ws_b)
+            torch.cuda.current_stream().synchronize()   # host reuses the pinned rows
+        return lens
+
+    if args.device_alloc:
+        return run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev)
+    for _ in range(max(1, args.warmup // 3)):
+        reset()
+        run()
+    times = []
+    for _ in range(max(1, args.steps // 8)):
+        reset()
+        t0 = time.perf_counter()
+        lens_end = run()
+        torch.cuda.synchronize()
+        times.append(time.perf_counter() - t0)
+    assert B.pa_get_status() == 0
+    tot = sum(times)
+    runs = len(times)
+    # decode bytes summed over the loop's growing lengths
+    kv = 0
+    for s in range(nsteps):
+        n = wl.context_lens.astype(np.int64) + s + 1
+        kv += int(n.sum()) * 2 * wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    peak, kind = measured_peaks()
+    print(json.dumps({"row": "loop", "workload": wl.name, "steps_per_run": nsteps, "runs": runs,
+                      "decode_tokens_per_s": wl.batch * nsteps * runs / tot,
+                      "kv_gbs_wall": kv * runs / tot / 1e9, "ms_per_step": 1e3 * tot / (runs * nsteps),
+                      "peak": peak, "timing": "host wall clock incl. allocation, H2D table "
+                      "updates and a stream sync per step"}), flush=True)
+    B.pa_pool_destroy(h)
+
+
+def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev):
+    """The same loop with the free stack on the device: each step is
+    pa_device_alloc_blocks + pa_write_kv_and_decode + a length increment, and a
+    whole run of `nsteps` steps is one CUDA graph replay (no host round trip)."""
+    B.pa_pool_seed_free_stack(h, order)
+    for _ in used:
+        B.pa_alloc_block(h)
+    stack = torch.empty(wl.num_blocks + 1, dtype=torch.int32, device=dev)
+    B.pa_device_stack_upload(h, stack)
+    stack0 = stack.clone()
+    bt0 = torch.from_numpy(wl.block_tables.copy()).to(dev)
+    lens0 = torch.from_numpy(wl.context_lens.copy()).to(dev)
+    bt, lens, lens1 = bt0.clone(), lens0.clone(), lens0.clone()
+    out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
+    maxlen_blocks = wl.max_blocks
+    pb = B.pa_decode_partition_blocks(h, wl.batch, wl.num_heads, maxlen_blocks)
+    need = B.pa_decode_workspace_size(h, wl.batch, wl.num_heads, maxlen_blocks, pb)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    B.pa_get_status()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for t in range(nsteps):
+                B.pa_device_alloc_blocks(h, stack, bt, wl.max_blocks, lens, wl.batch, stream=s)
+                torch.add(lens, 1, out=lens1)
+                B.pa_write_kv_and_decode(out, qs[t], h, 0, ks[t], vs[t], lens, bt, wl.max_blocks,
+                                         lens1, wl.batch, wl.block_size, wl.num_heads,
+                                         wl.num_kv_heads, wl.head_dim, wl.scale, pb, ws, need,
+                                         stream=s)
+                lens.copy_(lens1)
+    torch.cuda.current_stream(dev).wait_stream(s)
+
+    def reset():
+        stack.copy_(stack0)
+        bt.copy_(bt0)
+        lens.copy_(lens0)
+
+    for _ in range(max(1, args.warmup)):
+        reset()
+        g.replay()
+    torch.cuda.synchronize()
+    runs = max(1, args.steps // 4)
+    ms = 0.0
+    for _ in range(runs):
+        reset()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms += e0.elapsed_time(e1)
+    st = B.pa_get_status()
+    assert st == 0, st
+    kv = 0
+    for t in range(nsteps):
+        n = wl.context_lens.astype(np.int64) + t + 1
+        kv += int(n.sum()) * 2 * wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    peak, kind = measured_peaks()
+    gbs = kv * runs / (ms / 1e3) / 1e9
+    print(json.dumps({"row": "loop_device", "workload": wl.name, "steps_per_run": nsteps,
+                      "runs": runs, "decode_tokens_per_s": wl.batch * nsteps * runs / (ms / 1e3),
+                      "kv_gbs": gbs, "frac_of_peak": gbs / peak, "ms_per_step": ms / (runs * nsteps),
+                      "partition_blocks": pb,
+                      "timing": "CUDA events around one graph replay per run (device allocation, "
+                                "fused append+decode, length update)"}), flush=True)
+    B.pa_device_stack_download(h, stack)
+    B.pa_pool_destroy(h)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--layers", type=int, default=0, help="layers per step (0 = all 32)")
+    ap.add_argument("--layers", type=int, default=0, help="layers per step (0 = all)")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_CFG, choices=[1, 2, 3, 4, 5],
+                    help="named workload (default: the large-batch one, the headline)")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step (all layers) as a CUDA graph and replay it")
+    ap.add_argument("--row", choices=["step", "gather", "loop"], default="step",
+                    help="step: append+decode per layer (headline); gather: pa_gather_kv "
+                         "bandwidth; loop: the append+decode loop with block allocation")
     ap.add_argument("--cpu-seqs", type=int, default=256, help="sequences in the oracle sample")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate oracle time for the CPU baseline")
     ap.add_argument("--ref-seqs", type=int, default=96, help="sequences per reference step")
+    ap.add_argument("--device-alloc", action="store_true",
+                    help="with --row loop: free stack on the device, one CUDA graph per run")
+    ap.add_argument("--fused", action="store_true",
+                    help="step mode: pa_write_kv_and_decode instead of two calls per layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--pool-layers", type=int, default=0,
@@ -482,6 +759,10 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.row == "gather":
+            run_gather(args, local_rank)
+        elif args.row == "loop":
+            run_loop(args, local_rank)
         else:
             run_gpu(args, rank, world, local_rank)
     finally:

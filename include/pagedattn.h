@@ -78,6 +78,7 @@ enum {
 #define PA_STATUS_BAD_BLOCK_ID 0x1u /* a table entry read was outside [0, num_blocks) */
 #define PA_STATUS_BAD_LENGTH 0x2u   /* a context length / position outside the table */
 #define PA_STATUS_TIMEOUT 0x4u      /* a bounded wait for a shared-memory copy gave up */
+#define PA_STATUS_NO_FREE_BLOCKS 0x8u /* the device free stack ran dry during an allocation */
 
 /* Human-readable description of the calling thread's last error ("" if none). */
 PA_API const char* pa_last_error_string(void);
@@ -97,6 +98,32 @@ PA_API const char* pa_last_error_string(void);
  */
 PA_API int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers,
                    int num_kv_heads, int block_size, int head_dim, pa_dtype dtype);
+
+/*
+ * Any other layout whose B x D tile of one (physical block, layer, KV head) is
+ * a contiguous row-major [block_size, head_dim] array -- for instance vllmini's
+ * separate k_cache / v_cache tensors ("vllmini", "The CUDA Block Kernel"), or
+ * per-layer caches stacked layer-major.  K row t of the tile of (block, layer,
+ * head) starts at element
+ *     block*block_stride + layer*layer_stride + head*head_stride + t*head_dim
+ * from k_base, V rows likewise from v_base (strides in elements).
+ * Requirements: bases 16-byte aligned; strides >= 0 and multiples of 16 bytes;
+ * a stride may be 0 only for a dimension of extent 1; the tiles reachable
+ * from one base must not overlap (checked).  K and V tiles must not overlap
+ * each other (not checked).  pa_pool_create is this call with the fused
+ * layout's strides.
+ */
+typedef struct pa_pool_layout {
+    void* k_base;
+    void* v_base;
+    int64_t block_stride;
+    int64_t layer_stride;
+    int64_t head_stride;
+} pa_pool_layout;
+
+PA_API int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, int num_blocks,
+                                  int num_layers, int num_kv_heads, int block_size, int head_dim,
+                                  pa_dtype dtype);
 
 /* Release the handle (not the caller's device tensor).  NULL is accepted. */
 PA_API int pa_pool_destroy(pa_pool* pool);
@@ -120,6 +147,50 @@ PA_API int pa_free_block(pa_pool* pool, int block_id);
 
 /* Number of ids on the free stack. */
 PA_API int pa_num_free(const pa_pool* pool, int* n);
+
+/* ----------------------------------------------------------------------------
+ * The free stack on the device ("kv-cache" skill, section 3.1 "Cache Block
+ * Pool": one allocator hands out blocks as generation proceeds; mini-infer
+ * BlockPool semantics).  A caller-owned int32 array of num_blocks + 1 entries
+ * holds [height, id_0 (bottom), ..., id_{height-1} (top)].  While the stack is
+ * on the device the host calls pa_alloc_block / pa_free_block /
+ * pa_pool_seed_free_stack are refused.
+ * ------------------------------------------------------------------------- */
+
+/* Bytes of the device stack array: (num_blocks + 1) * 4. */
+PA_API int pa_device_stack_bytes(const pa_pool* pool, size_t* bytes);
+
+/* Copy the host free stack into dev_stack (waits for `stream`) and hand the
+ * stack to the device. */
+PA_API int pa_device_stack_upload(pa_pool* pool, void* dev_stack, pa_stream_t stream);
+
+/* Wait for `stream`, copy the device stack back into the host allocator
+ * (validating every id) and return the stack to the host. */
+PA_API int pa_device_stack_download(pa_pool* pool, const void* dev_stack, pa_stream_t stream);
+
+/*
+ * For every sequence b, in increasing b, whose next token starts a new block
+ * (positions[b] % block_size == 0), pop the top id of the device stack and
+ * store it at block_tables[b][positions[b] / block_size] -- the ids repeated
+ * pa_alloc_block calls would hand out in that order.  When the stack runs dry
+ * the remaining such entries are set to -1 and PA_STATUS_NO_FREE_BLOCKS is
+ * raised.  One kernel launch; no host round trip.
+ */
+PA_API int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
+                                  int max_blocks_per_seq, const int* positions, int batch,
+                                  pa_stream_t stream);
+
+/*
+ * For every sequence b with finished[b] != 0, in increasing b, push the ids of
+ * its ceil(context_lens[b] / block_size) blocks in table order (as repeated
+ * pa_free_block calls) and set those table entries to -1.  Out-of-range ids are
+ * skipped and flagged (PA_STATUS_BAD_BLOCK_ID); pushing an id that is already
+ * free is not detected on the device (pa_device_stack_download rejects the
+ * resulting stack).
+ */
+PA_API int pa_device_free_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
+                                 int max_blocks_per_seq, const int* context_lens,
+                                 const uint8_t* finished, int batch, pa_stream_t stream);
 
 /* ----------------------------------------------------------------------------
  * KV append (reshape-and-cache).
@@ -182,6 +253,24 @@ PA_API int pa_decode_attention_partitioned(float* out, const void* q, const pa_p
                                     int num_heads, int num_kv_heads, int head_dim, float scale,
                                     int partition_blocks, void* workspace,
                                     size_t workspace_bytes, pa_stream_t stream);
+
+/*
+ * KV append fused into decode: one launch that first stores k[b][h] / v[b][h]
+ * at slot (block_tables[b][p / B], p % B), p = positions[b] (exactly as
+ * pa_write_kv), then computes pa_decode_attention_partitioned over
+ * context_lens[b] tokens, which normally include the new one (n = p + 1).
+ * Within a sequence the store is ordered before the decode reads it.  The
+ * block receiving the new token must not be read by another sequence of the
+ * same call.  Bad positions / ids are flagged in the status word as for
+ * pa_write_kv.  Arguments as for pa_write_kv and pa_decode_attention_partitioned.
+ */
+PA_API int pa_write_kv_and_decode(float* out, const void* q, pa_pool* pool, int layer,
+                                  const void* k, const void* v, const int* positions,
+                                  const int* block_tables, int max_blocks_per_seq,
+                                  const int* context_lens, int batch, int block_size,
+                                  int num_heads, int num_kv_heads, int head_dim, float scale,
+                                  int partition_blocks, void* workspace, size_t workspace_bytes,
+                                  pa_stream_t stream);
 
 /* The partition size (in blocks) that pa_decode_attention picks for these
  * sizes on the current device.  Queries the device's SM count. */

@@ -29,6 +29,7 @@ PA_DTYPE_BF16 = 1
 PA_STATUS_BAD_BLOCK_ID = 0x1
 PA_STATUS_BAD_LENGTH = 0x2
 PA_STATUS_TIMEOUT = 0x4
+PA_STATUS_NO_FREE_BLOCKS = 0x8
 
 _ERR_NAMES = {
     PA_ERR_INVALID_ARG: "PA_ERR_INVALID_ARG",
@@ -52,6 +53,13 @@ class OutOfBlocksError(PagedAttnError, MemoryError):
 
 _lib: Optional[ctypes.CDLL] = None
 
+
+class pa_pool_layout(ctypes.Structure):
+    """Mirror of the C struct: K/V base addresses and element strides."""
+    _fields_ = [("k_base", ctypes.c_void_p), ("v_base", ctypes.c_void_p),
+                ("block_stride", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
+                ("head_stride", ctypes.c_int64)]
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SZ = ctypes.c_size_t
@@ -63,6 +71,8 @@ _PU = ctypes.POINTER(ctypes.c_uint)
 _SIGNATURES = {
     "pa_last_error_string": ([], ctypes.c_char_p),
     "pa_pool_create": ([ctypes.POINTER(_P), _P, _I, _I, _I, _I, _I, _I], _I),
+    "pa_pool_create_strided": ([ctypes.POINTER(_P), ctypes.POINTER(pa_pool_layout), _I, _I, _I,
+                                _I, _I, _I], _I),
     "pa_pool_destroy": ([_P], _I),
     "pa_pool_block_bytes": ([_P, _PSZ], _I),
     "pa_pool_seed_free_stack": ([_P, _P, _I], _I),
@@ -70,9 +80,16 @@ _SIGNATURES = {
     "pa_free_block": ([_P, _I], _I),
     "pa_num_free": ([_P, _PI], _I),
     "pa_write_kv": ([_P, _I, _P, _P, _P, _I, _P, _I, _P], _I),
+    "pa_device_stack_bytes": ([_P, _PSZ], _I),
+    "pa_device_stack_upload": ([_P, _P, _P], _I),
+    "pa_device_stack_download": ([_P, _P, _P], _I),
+    "pa_device_alloc_blocks": ([_P, _P, _P, _I, _P, _I, _P], _I),
+    "pa_device_free_blocks": ([_P, _P, _P, _I, _P, _P, _I, _P], _I),
     "pa_decode_attention": ([_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P], _I),
     "pa_decode_attention_partitioned": (
         [_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P], _I),
+    "pa_write_kv_and_decode": ([_P, _P, _P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F,
+                                _I, _P, _SZ, _P], _I),
     "pa_decode_partition_blocks": ([_P, _I, _I, _I, _PI], _I),
     "pa_decode_workspace_size": ([_P, _I, _I, _I, _I, _PSZ], _I),
     "pa_decode_attention_noalloc": (
@@ -169,6 +186,17 @@ def pa_pool_create(pool_dev, num_blocks: int, num_layers: int, num_kv_heads: int
     return h.value
 
 
+def pa_pool_create_strided(k_base, v_base, block_stride: int, layer_stride: int,
+                           head_stride: int, num_blocks: int, num_layers: int, num_kv_heads: int,
+                           block_size: int, head_dim: int, dtype) -> int:
+    lay = pa_pool_layout(_ptr(k_base), _ptr(v_base), block_stride, layer_stride, head_stride)
+    h = _P()
+    _check(lib().pa_pool_create_strided(ctypes.byref(h), ctypes.byref(lay), num_blocks,
+                                        num_layers, num_kv_heads, block_size, head_dim,
+                                        _dtype_code(dtype)), "pa_pool_create_strided")
+    return h.value
+
+
 def pa_pool_destroy(pool: int) -> None:
     _check(lib().pa_pool_destroy(pool), "pa_pool_destroy")
 
@@ -199,6 +227,39 @@ def pa_num_free(pool: int) -> int:
     v = ctypes.c_int()
     _check(lib().pa_num_free(pool, ctypes.byref(v)), "pa_num_free")
     return v.value
+
+
+# ------------------------------------------------------------ device stack
+
+
+def pa_device_stack_bytes(pool: int) -> int:
+    v = _SZ()
+    _check(lib().pa_device_stack_bytes(pool, ctypes.byref(v)), "pa_device_stack_bytes")
+    return v.value
+
+
+def pa_device_stack_upload(pool: int, dev_stack, stream=None) -> None:
+    _check(lib().pa_device_stack_upload(pool, _ptr(dev_stack), _stream(stream)),
+           "pa_device_stack_upload")
+
+
+def pa_device_stack_download(pool: int, dev_stack, stream=None) -> None:
+    _check(lib().pa_device_stack_download(pool, _ptr(dev_stack), _stream(stream)),
+           "pa_device_stack_download")
+
+
+def pa_device_alloc_blocks(pool: int, dev_stack, block_tables, max_blocks_per_seq: int, positions,
+                           batch: int, stream=None) -> None:
+    _check(lib().pa_device_alloc_blocks(pool, _ptr(dev_stack), _ptr(block_tables),
+                                        max_blocks_per_seq, _ptr(positions), batch,
+                                        _stream(stream)), "pa_device_alloc_blocks")
+
+
+def pa_device_free_blocks(pool: int, dev_stack, block_tables, max_blocks_per_seq: int,
+                          context_lens, finished, batch: int, stream=None) -> None:
+    _check(lib().pa_device_free_blocks(pool, _ptr(dev_stack), _ptr(block_tables),
+                                       max_blocks_per_seq, _ptr(context_lens), _ptr(finished),
+                                       batch, _stream(stream)), "pa_device_free_blocks")
 
 
 # ---------------------------------------------------------------- kernels
@@ -265,6 +326,18 @@ def pa_decode_attention_noalloc(out, q, pool: int, layer: int, block_tables,
         _ptr(out), _ptr(q), pool, layer, _ptr(block_tables), max_blocks_per_seq,
         _ptr(context_lens), batch, block_size, num_heads, num_kv_heads, head_dim, float(scale),
         partition_blocks, _stream(stream)), "pa_decode_attention_noalloc")
+
+
+def pa_write_kv_and_decode(out, q, pool: int, layer: int, k, v, positions, block_tables,
+                           max_blocks_per_seq: int, context_lens, batch: int, block_size: int,
+                           num_heads: int, num_kv_heads: int, head_dim: int, scale: float,
+                           partition_blocks: int = 0, workspace=None, workspace_bytes: int = 0,
+                           stream=None) -> None:
+    _check(lib().pa_write_kv_and_decode(
+        _ptr(out), _ptr(q), pool, layer, _ptr(k), _ptr(v), _ptr(positions), _ptr(block_tables),
+        max_blocks_per_seq, _ptr(context_lens), batch, block_size, num_heads, num_kv_heads,
+        head_dim, float(scale), partition_blocks, _ptr(workspace), workspace_bytes,
+        _stream(stream)), "pa_write_kv_and_decode")
 
 
 def pa_gather_kv(k_out, v_out, mask, pool: int, layer: int, block_tables, max_blocks_per_seq: int,

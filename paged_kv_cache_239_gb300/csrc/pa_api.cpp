@@ -2,6 +2,7 @@
 // validation and kernel launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
@@ -19,6 +20,7 @@ struct pa_pool {
     pa::PoolGeom g;
     std::vector<int> free_stack;        // allocation pops from the back
     std::vector<unsigned char> in_use;  // 1 while a block is handed out
+    bool on_device = false;             // the stack is held in a device copy
     mutable std::mutex mu;
 };
 
@@ -162,7 +164,35 @@ int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers
     if (!out) return fail(PA_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     if (!pool_dev) return fail(PA_ERR_INVALID_ARG, "pool_dev is NULL");
-    if (!aligned(pool_dev, 16)) return fail(PA_ERR_INVALID_ARG, "pool_dev is not 16-byte aligned");
+    if (num_blocks <= 0 || num_layers <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
+        head_dim <= 0)
+        return fail(PA_ERR_INVALID_ARG, "pool geometry must be positive (nb=%d L=%d Hkv=%d B=%d D=%d)",
+                    num_blocks, num_layers, num_kv_heads, block_size, head_dim);
+    if (dtype != PA_DTYPE_F32 && dtype != PA_DTYPE_BF16)
+        return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    // The fused mini-infer tensor [num_blocks, 2, L, Hkv, B, D] as strides.
+    const long long tile = (long long)block_size * head_dim;
+    const long long elt = dtype == PA_DTYPE_F32 ? 4 : 2;
+    pa_pool_layout lay;
+    lay.k_base = pool_dev;
+    lay.v_base = static_cast<char*>(pool_dev) + (long long)num_layers * num_kv_heads * tile * elt;
+    lay.block_stride = 2LL * num_layers * num_kv_heads * tile;
+    lay.layer_stride = (long long)num_kv_heads * tile;
+    lay.head_stride = tile;
+    return pa_pool_create_strided(out, &lay, num_blocks, num_layers, num_kv_heads, block_size,
+                                  head_dim, dtype);
+}
+
+int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, int num_blocks,
+                           int num_layers, int num_kv_heads, int block_size, int head_dim,
+                           pa_dtype dtype) {
+    if (!out) return fail(PA_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!layout) return fail(PA_ERR_INVALID_ARG, "layout is NULL");
+    if (!layout->k_base || !layout->v_base)
+        return fail(PA_ERR_INVALID_ARG, "k_base and v_base must be non-NULL");
+    if (!aligned(layout->k_base, 16) || !aligned(layout->v_base, 16))
+        return fail(PA_ERR_INVALID_ARG, "k_base and v_base must be 16-byte aligned");
     if (num_blocks <= 0 || num_layers <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
         head_dim <= 0)
         return fail(PA_ERR_INVALID_ARG, "pool geometry must be positive (nb=%d L=%d Hkv=%d B=%d D=%d)",
@@ -173,12 +203,59 @@ int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers
     if ((head_dim * elt) % 16 != 0)
         return fail(PA_ERR_INVALID_ARG, "head_dim * element size (%d) must be a multiple of 16",
                     head_dim * elt);
-    const double elems = (double)num_blocks * 2 * num_layers * num_kv_heads * block_size * head_dim;
-    if (elems > 4.0e18) return fail(PA_ERR_INVALID_ARG, "pool too large");
+    // Strides: non-negative, 16-byte multiples, zero only for a dimension of
+    // extent one, and tiles of one base must not overlap.
+    struct Dim {
+        long long stride, count;
+        const char* name;
+    } dims[3] = {{layout->block_stride, num_blocks, "block_stride"},
+                 {layout->layer_stride, num_layers, "layer_stride"},
+                 {layout->head_stride, num_kv_heads, "head_stride"}};
+    for (const Dim& d : dims) {
+        if (d.stride < 0) return fail(PA_ERR_INVALID_ARG, "%s is negative", d.name);
+        if ((d.stride * elt) % 16 != 0)
+            return fail(PA_ERR_INVALID_ARG, "%s * element size must be a multiple of 16 bytes",
+                        d.name);
+        if (d.stride == 0 && d.count > 1)
+            return fail(PA_ERR_INVALID_ARG, "%s is 0 but that dimension has %lld entries", d.name,
+                        d.count);
+    }
+    {
+        Dim live[3];
+        int n = 0;
+        for (const Dim& d : dims)
+            if (d.count > 1) live[n++] = d;
+        for (int a = 0; a < n; ++a)
+            for (int b = a + 1; b < n; ++b)
+                if (live[b].stride < live[a].stride) {
+                    Dim t = live[a];
+                    live[a] = live[b];
+                    live[b] = t;
+                }
+        long long extent = (long long)block_size * head_dim;  // one contiguous tile
+        for (int a = 0; a < n; ++a) {
+            if (live[a].stride < extent)
+                return fail(PA_ERR_INVALID_ARG, "%s = %lld makes tiles overlap (needs >= %lld)",
+                            live[a].name, live[a].stride, extent);
+            const double ext = (double)live[a].stride * (double)live[a].count;
+            if (ext > 4.0e18) return fail(PA_ERR_INVALID_ARG, "pool too large");
+            extent = live[a].stride * live[a].count;
+        }
+    }
     try {
         pa_pool* p = new pa_pool();
-        p->g = pa::PoolGeom{pool_dev, num_blocks, num_layers, num_kv_heads, block_size, head_dim,
-                            elt, (int)dtype};
+        p->g.k_base = layout->k_base;
+        p->g.v_base = layout->v_base;
+        p->g.s_blk = layout->block_stride;
+        p->g.s_layer = layout->layer_stride;
+        p->g.s_head = layout->head_stride;
+        p->g.num_blocks = num_blocks;
+        p->g.L = num_layers;
+        p->g.Hkv = num_kv_heads;
+        p->g.B = block_size;
+        p->g.D = head_dim;
+        p->g.elt = elt;
+        p->g.dtype = (int)dtype;
         p->free_stack.resize(num_blocks);
         for (int i = 0; i < num_blocks; ++i) p->free_stack[i] = i;
         p->in_use.assign(num_blocks, 0);
@@ -205,6 +282,8 @@ int pa_pool_seed_free_stack(pa_pool* pool, const int* order, int n) {
     if (int rc = check_pool(pool)) return rc;
     if (!order) return fail(PA_ERR_INVALID_ARG, "order is NULL");
     std::lock_guard<std::mutex> lock(pool->mu);
+    if (pool->on_device)
+        return fail(PA_ERR_INVALID_ARG, "the free stack is held on the device; download it first");
     const long long nb = pool->g.num_blocks;
     if (n != nb) return fail(PA_ERR_INVALID_ARG, "order has %d entries, pool has %lld blocks", n, nb);
     if ((long long)pool->free_stack.size() != nb)
@@ -224,6 +303,8 @@ int pa_alloc_block(pa_pool* pool, int* block_id) {
     if (int rc = check_pool(pool)) return rc;
     if (!block_id) return fail(PA_ERR_INVALID_ARG, "block_id is NULL");
     std::lock_guard<std::mutex> lock(pool->mu);
+    if (pool->on_device)
+        return fail(PA_ERR_INVALID_ARG, "the free stack is held on the device; download it first");
     if (pool->free_stack.empty())
         return fail(PA_ERR_NO_FREE_BLOCKS, "Out of KV-Cache Physical Blocks");
     const int id = pool->free_stack.back();
@@ -236,6 +317,8 @@ int pa_alloc_block(pa_pool* pool, int* block_id) {
 int pa_free_block(pa_pool* pool, int block_id) {
     if (int rc = check_pool(pool)) return rc;
     std::lock_guard<std::mutex> lock(pool->mu);
+    if (pool->on_device)
+        return fail(PA_ERR_INVALID_ARG, "the free stack is held on the device; download it first");
     if (block_id < 0 || block_id >= pool->g.num_blocks)
         return fail(PA_ERR_INVALID_ARG, "block id %d outside [0, %lld)", block_id, pool->g.num_blocks);
     if (!pool->in_use[block_id])
@@ -250,6 +333,104 @@ int pa_num_free(const pa_pool* pool, int* n) {
     if (!n) return fail(PA_ERR_INVALID_ARG, "n is NULL");
     std::lock_guard<std::mutex> lock(pool->mu);
     *n = (int)pool->free_stack.size();
+    return PA_OK;
+}
+
+int pa_device_stack_bytes(const pa_pool* pool, size_t* bytes) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = ((size_t)pool->g.num_blocks + 1) * sizeof(int);
+    return PA_OK;
+}
+
+int pa_device_stack_upload(pa_pool* pool, void* dev_stack, pa_stream_t stream) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!dev_stack || !aligned(dev_stack, 4))
+        return fail(PA_ERR_INVALID_ARG, "dev_stack must be non-NULL and 4-byte aligned");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    if (pool->on_device) return fail(PA_ERR_INVALID_ARG, "the free stack is already on the device");
+    std::vector<int> img(pool->free_stack.size() + 1);
+    img[0] = (int)pool->free_stack.size();
+    std::copy(pool->free_stack.begin(), pool->free_stack.end(), img.begin() + 1);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(dev_stack, img.data(), img.size() * sizeof(int),
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "pa_device_stack_upload");
+    pool->on_device = true;
+    return PA_OK;
+}
+
+int pa_device_stack_download(pa_pool* pool, const void* dev_stack, pa_stream_t stream) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!dev_stack || !aligned(dev_stack, 4))
+        return fail(PA_ERR_INVALID_ARG, "dev_stack must be non-NULL and 4-byte aligned");
+    std::lock_guard<std::mutex> lock(pool->mu);
+    if (!pool->on_device) return fail(PA_ERR_INVALID_ARG, "the free stack is not on the device");
+    const long long nb = pool->g.num_blocks;
+    std::vector<int> img(nb + 1);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(img.data(), dev_stack, img.size() * sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "pa_device_stack_download");
+    const int height = img[0];
+    if (height < 0 || height > nb)
+        return fail(PA_ERR_INVALID_ARG, "device stack height %d outside [0, %lld]", height, nb);
+    std::vector<unsigned char> in_stack(nb, 0);
+    for (int i = 0; i < height; ++i) {
+        const int id = img[1 + i];
+        if (id < 0 || id >= nb || in_stack[id])
+            return fail(PA_ERR_INVALID_ARG, "device stack entry %d (= %d) is invalid or repeated",
+                        i, id);
+        in_stack[id] = 1;
+    }
+    pool->free_stack.assign(img.begin() + 1, img.begin() + 1 + height);
+    for (long long i = 0; i < nb; ++i) pool->in_use[i] = in_stack[i] ? 0 : 1;
+    pool->on_device = false;
+    return PA_OK;
+}
+
+int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
+                           int max_blocks_per_seq, const int* positions, int batch,
+                           pa_stream_t stream) {
+    if (int rc = check_pool(pool)) return rc;
+    if (batch < 0 || max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID_ARG, "batch (%d) / max_blocks_per_seq (%d) out of range", batch,
+                    max_blocks_per_seq);
+    if (batch == 0) return PA_OK;
+    if (!dev_stack || !block_tables || !positions || !aligned(dev_stack, 4) ||
+        !aligned(block_tables, 4) || !aligned(positions, 4))
+        return fail(PA_ERR_INVALID_ARG, "dev_stack, block_tables, positions: non-NULL, 4-byte aligned");
+    unsigned* status = nullptr;
+    cudaError_t e = pa::status_word(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
+    e = pa::launch_device_alloc(static_cast<int*>(dev_stack), block_tables, max_blocks_per_seq,
+                                positions, batch, pool->g.B, status,
+                                reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_device_alloc_blocks launch");
+    return PA_OK;
+}
+
+int pa_device_free_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
+                          int max_blocks_per_seq, const int* context_lens, const uint8_t* finished,
+                          int batch, pa_stream_t stream) {
+    if (int rc = check_pool(pool)) return rc;
+    if (batch < 0 || max_blocks_per_seq <= 0)
+        return fail(PA_ERR_INVALID_ARG, "batch (%d) / max_blocks_per_seq (%d) out of range", batch,
+                    max_blocks_per_seq);
+    if (batch == 0) return PA_OK;
+    if (!dev_stack || !block_tables || !context_lens || !finished || !aligned(dev_stack, 4) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return fail(PA_ERR_INVALID_ARG,
+                    "dev_stack, block_tables, context_lens, finished: non-NULL, aligned");
+    unsigned* status = nullptr;
+    cudaError_t e = pa::status_word(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
+    e = pa::launch_device_free(static_cast<int*>(dev_stack), block_tables, max_blocks_per_seq,
+                               context_lens, finished, batch, pool->g.B, pool->g.num_blocks,
+                               status, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_device_free_blocks launch");
     return PA_OK;
 }
 
@@ -272,9 +453,10 @@ int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v, const in
     unsigned* status = nullptr;
     cudaError_t e = pa::status_word(&status);
     if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
-    pa::WriteParams p{pool->g.base, pool->g.num_blocks, pool->g.L, pool->g.Hkv, pool->g.B,
-                      pool->g.D * pool->g.elt, layer, k, v, block_tables, max_blocks_per_seq,
-                      positions, batch, status};
+    const pa::PoolGeom& g = pool->g;
+    pa::WriteParams p{g.k_base, g.v_base, g.s_blk, layer * g.s_layer, g.s_head, g.num_blocks,
+                      g.Hkv, g.B, g.D * g.elt, g.elt, layer, k, v, block_tables,
+                      max_blocks_per_seq, positions, batch, status};
     e = pa::launch_write_kv(p, sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pa_write_kv launch");
     return PA_OK;
@@ -302,12 +484,17 @@ int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
     return PA_OK;
 }
 
-int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
-                                    const int* block_tables, int max_blocks_per_seq,
-                                    const int* context_lens, int batch, int block_size,
-                                    int num_heads, int num_kv_heads, int head_dim, float scale,
-                                    int partition_blocks, void* workspace,
-                                    size_t workspace_bytes, pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Decode attention; with new_k/new_v/positions non-null the append of one
+// token per sequence is fused into the decode kernel.
+int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
+                const int* block_tables, int max_blocks_per_seq, const int* context_lens,
+                int batch, int block_size, int num_heads, int num_kv_heads, int head_dim,
+                float scale, int partition_blocks, void* workspace, size_t workspace_bytes,
+                pa_stream_t stream, const void* new_k, const void* new_v, const int* positions) {
     if (int rc = check_pool(pool)) return rc;
     if (int rc = check_layer(pool, layer)) return rc;
     const pa::PoolGeom& g = pool->g;
@@ -345,9 +532,12 @@ int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* po
     pa::DecodeParams p{};
     p.out = out;
     p.q = q;
-    p.pool = g.base;
+    p.k_base = g.k_base;
+    p.v_base = g.v_base;
+    p.s_blk = g.s_blk;
+    p.tile_off = layer * g.s_layer;
+    p.s_head = g.s_head;
     p.num_blocks = g.num_blocks;
-    p.L = g.L;
     p.Hkv = g.Hkv;
     p.layer = layer;
     p.bt = block_tables;
@@ -361,6 +551,9 @@ int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* po
     p.PB = sh.PB;
     p.Cmax = sh.Cmax;
     p.status = status;
+    p.new_k = new_k;
+    p.new_v = new_v;
+    p.positions = positions;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     e = g.dtype == 1 ? pa::launch_decode_bf16(p, g.D, g.B, sh.G, s)
                      : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);
@@ -370,6 +563,40 @@ int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* po
         if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     }
     return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
+                                    const int* block_tables, int max_blocks_per_seq,
+                                    const int* context_lens, int batch, int block_size,
+                                    int num_heads, int num_kv_heads, int head_dim, float scale,
+                                    int partition_blocks, void* workspace,
+                                    size_t workspace_bytes, pa_stream_t stream) {
+    return decode_impl(out, q, pool, layer, block_tables, max_blocks_per_seq, context_lens, batch,
+                       block_size, num_heads, num_kv_heads, head_dim, scale, partition_blocks,
+                       workspace, workspace_bytes, stream, nullptr, nullptr, nullptr);
+}
+
+int pa_write_kv_and_decode(float* out, const void* q, pa_pool* pool, int layer, const void* k,
+                           const void* v, const int* positions, const int* block_tables,
+                           int max_blocks_per_seq, const int* context_lens, int batch,
+                           int block_size, int num_heads, int num_kv_heads, int head_dim,
+                           float scale, int partition_blocks, void* workspace,
+                           size_t workspace_bytes, pa_stream_t stream) {
+    if (batch > 0) {
+        if (!k || !v || !positions)
+            return fail(PA_ERR_INVALID_ARG, "k, v and positions must be non-NULL");
+        if (!aligned(k, 16) || !aligned(v, 16))
+            return fail(PA_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+        if (!aligned(positions, 4))
+            return fail(PA_ERR_INVALID_ARG, "positions must be 4-byte aligned");
+    }
+    return decode_impl(out, q, pool, layer, block_tables, max_blocks_per_seq, context_lens, batch,
+                       block_size, num_heads, num_kv_heads, head_dim, scale, partition_blocks,
+                       workspace, workspace_bytes, stream, k, v, positions);
 }
 
 int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int layer,
@@ -403,9 +630,10 @@ int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, i
     cudaError_t e = pa::status_word(&status);
     if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
     const pa::PoolGeom& g = pool->g;
-    pa::GatherParams p{k_out, v_out, mask, g.base, g.num_blocks, g.L, g.Hkv, g.B, g.D * g.elt,
-                       layer, block_tables, max_blocks_per_seq, context_lens, batch, max_len,
-                       status};
+    pa::GatherParams p{k_out,       v_out,   mask,       g.k_base,     g.v_base,
+                       g.s_blk,     layer * g.s_layer, g.s_head, g.num_blocks, g.Hkv,
+                       g.B,         g.D * g.elt, g.elt,   layer,      block_tables,
+                       max_blocks_per_seq, context_lens, batch, max_len, status};
     e = pa::launch_gather_kv(p, sms, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pa_gather_kv launch");
     return PA_OK;

@@ -83,11 +83,13 @@ __global__ void __launch_bounds__(256) pa_write_kv_kernel(const WriteParams p) {
             if (ci == 0 && kvh == 0 && kv == 0) atomicOr(p.status, kStatusBadBlock);
             continue;
         }
-        const long long row = ((((long long)blk * 2 + kv) * p.L + p.layer) * p.Hkv + kvh) * p.B +
-                               (pos % p.B);
+        // element offset of the slot's row, then bytes
+        const long long off = (long long)blk * p.s_blk + p.tile_off + (long long)kvh * p.s_head +
+                              (long long)(pos % p.B) * (p.row_bytes / p.elt);
         const unsigned char* src = static_cast<const unsigned char*>(kv ? p.v : p.k) +
                                    ((long long)b * p.Hkv + kvh) * p.row_bytes + ci * 16;
-        unsigned char* dst = static_cast<unsigned char*>(p.pool) + row * p.row_bytes + ci * 16;
+        unsigned char* dst = static_cast<unsigned char*>(kv ? p.v_base : p.k_base) +
+                             off * p.elt + ci * 16;
         *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
     }
 }
@@ -132,10 +134,12 @@ __global__ void __launch_bounds__(256) pa_gather_kv_kernel(const GatherParams p)
             if (blk < 0 || blk >= p.num_blocks) {
                 if (kvh == 0 && kv == 0 && ci == 0) atomicOr(p.status, kStatusBadBlock);
             } else {
-                const long long row =
-                    ((((long long)blk * 2 + kv) * p.L + p.layer) * p.Hkv + kvh) * p.B + (t % p.B);
+                const long long off = (long long)blk * p.s_blk + p.tile_off +
+                                      (long long)kvh * p.s_head +
+                                      (long long)(t % p.B) * (p.row_bytes / p.elt);
                 val = __ldg(reinterpret_cast<const uint4*>(
-                    static_cast<const unsigned char*>(p.pool) + row * p.row_bytes + ci * 16));
+                    static_cast<const unsigned char*>(kv ? p.v_base : p.k_base) + off * p.elt +
+                    ci * 16));
             }
         }
         const long long orow = ((long long)b * p.max_len + t) * p.Hkv + kvh;

@@ -4,7 +4,8 @@
 // section 2 "Block Tables"; mini-infer, "The Solution"): for sequence b and
 // query head h, the n = context_lens[b] cached tokens are reached through the
 // block table -- token t lives in physical block bt[b][t / B] at offset t % B
-// of the pool [num_blocks, 2, L, Hkv, B, D] -- and
+// of the pool (the fused [num_blocks, 2, L, Hkv, B, D] tensor, or any layout
+// whose B x D tiles are contiguous, see PoolGeom) -- and
 //     out[b][h] = softmax_t(scale * q[b][h] . K_t) V_t .
 //
 // Work decomposition (GB300 design, not taken from the pages):
@@ -202,8 +203,39 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     }
 
     const int* bt_row = p.bt + (long long)b * p.maxb;
-    const T* pool = reinterpret_cast<const T*>(p.pool);
-    const long long kv_stride_rows = (long long)p.L * p.Hkv * B;  // K -> V rows
+    // This CTA's tiles: element offset of (block 0, layer, kvh) from each base.
+    const long long tile0 = p.tile_off + (long long)kvh * p.s_head;
+    const T* kpool = reinterpret_cast<const T*>(p.k_base) + tile0;
+    const T* vpool = reinterpret_cast<const T*>(p.v_base) + tile0;
+
+    // ---- fused append: the CTA whose partition holds the new token's block
+    //      (partition 0 when the position lies past the context) stores this
+    //      KV head's new K and V rows before any bulk copy is issued. ----
+    if (p.new_k != nullptr) {
+        const int pos = __ldg(p.positions + b);
+        if (pos < 0 || pos / B >= p.maxb) {
+            if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+        } else if (c == (pos < n ? (pos / B) / p.PB : 0)) {
+            constexpr int CPR = C::ROW_BYTES / 16;  // 16-byte chunks per row
+            const int blk = __ldg(bt_row + pos / B);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
+            } else if (threadIdx.x < 2 * CPR) {
+                const int kv = threadIdx.x / CPR;
+                const int ci = threadIdx.x % CPR;
+                const long long src = ((long long)b * p.Hkv + kvh) * C::ROW_BYTES + ci * 16;
+                const long long off = (long long)blk * p.s_blk + tile0 + (long long)(pos % B) * D;
+                const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                    static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src));
+                T* dst = const_cast<T*>(reinterpret_cast<const T*>(kv ? p.v_base : p.k_base)) +
+                         off;
+                reinterpret_cast<uint4*>(dst)[ci] = val;
+                // the stored row is read back below by the bulk-copy (async) proxy
+                fence_proxy_async_global();
+            }
+        }
+        __syncthreads();
+    }
     const uint64_t policy = l2_policy_evict_first();
 
     // Block ids of this warp's blocks kbase..kbase+31, one per lane.
@@ -229,12 +261,10 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
                 s_nvalid[stage] = rows;
                 const uint32_t bytes = (uint32_t)rows * C::ROW_BYTES;
                 mbar_arrive_expect_tx(bar, 2 * bytes);
-                const long long krow =
-                    (((long long)blk * 2 * p.L + p.layer) * p.Hkv + kvh) * B + row0;
+                const long long off = (long long)blk * p.s_blk + (long long)row0 * D;
                 const uint32_t dst = stage0 + stage * C::STAGE_BYTES;
-                bulk_copy_g2s(dst, pool + krow * D, bytes, bar, policy);
-                bulk_copy_g2s(dst + C::TILE_BYTES, pool + (krow + kv_stride_rows) * D, bytes, bar,
-                              policy);
+                bulk_copy_g2s(dst, kpool + off, bytes, bar, policy);
+                bulk_copy_g2s(dst + C::TILE_BYTES, vpool + off, bytes, bar, policy);
             } else {
                 s_nvalid[stage] = 0;
                 atomicOr(p.status, kStatusBadBlock);

@@ -11,10 +11,17 @@ namespace pa {
 constexpr unsigned kStatusBadBlock = 0x1u;
 constexpr unsigned kStatusBadLength = 0x2u;
 constexpr unsigned kStatusTimeout = 0x4u;
+constexpr unsigned kStatusNoFreeBlocks = 0x8u;
 
-// Geometry of one pool tensor [num_blocks, 2, L, Hkv, B, D].
+// Where a pool's rows live.  The B x D tile of (block, layer, kv head) is
+// contiguous and starts at element  blk*s_blk + layer*s_layer + head*s_head
+// from k_base (K rows) or v_base (V rows).  The fused tensor
+// [num_blocks, 2, L, Hkv, B, D] is the instance v_base = k_base + L*Hkv*B*D,
+// s_blk = 2*L*Hkv*B*D, s_layer = Hkv*B*D, s_head = B*D.
 struct PoolGeom {
-    void* base;
+    void* k_base;
+    void* v_base;
+    long long s_blk, s_layer, s_head;  // element strides
     long long num_blocks;
     int L, Hkv, B, D;
     int elt;    // bytes per element (4 = fp32, 2 = bf16)
@@ -24,9 +31,13 @@ struct PoolGeom {
 struct DecodeParams {
     float* out;           // [batch, H, D] fp32
     const void* q;        // [batch, H, D] pool dtype
-    const void* pool;     // pool base
+    const void* k_base;   // K rows (see PoolGeom)
+    const void* v_base;   // V rows
+    long long s_blk;      // element stride between physical blocks
+    long long tile_off;   // layer * s_layer (elements)
+    long long s_head;     // element stride between kv heads
     long long num_blocks;
-    int L, Hkv, layer;
+    int Hkv, layer;
     const int* bt;        // [batch, maxb]
     int maxb;
     const int* lens;      // [batch]
@@ -37,12 +48,19 @@ struct DecodeParams {
     int PB;               // blocks per partition
     int Cmax;             // partitions per (sequence, kv head) grid slot
     unsigned* status;     // device status word
+    // fused append (all null unless pa_write_kv_and_decode): new K/V rows
+    // [batch, Hkv, D] stored at slot positions[b] before the decode reads it
+    const void* new_k;
+    const void* new_v;
+    const int* positions;
 };
 
 struct WriteParams {
-    void* pool;
+    void* k_base;
+    void* v_base;
+    long long s_blk, tile_off, s_head;  // elements; tile_off = layer * s_layer
     long long num_blocks;
-    int L, Hkv, B, row_bytes, layer;
+    int Hkv, B, row_bytes, elt, layer;
     const void* k;
     const void* v;
     const int* bt;
@@ -56,9 +74,11 @@ struct GatherParams {
     void* k_out;
     void* v_out;
     uint8_t* mask;
-    const void* pool;
+    const void* k_base;
+    const void* v_base;
+    long long s_blk, tile_off, s_head;  // elements; tile_off = layer * s_layer
     long long num_blocks;
-    int L, Hkv, B, row_bytes, layer;
+    int Hkv, B, row_bytes, elt, layer;
     const int* bt;
     int maxb;
     const int* lens;
@@ -75,6 +95,12 @@ bool decode_supported(int dtype, int D, int B, int G);
 cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s);
 cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s);
+
+cudaError_t launch_device_alloc(int* stack, int* bt, int maxb, const int* positions, int batch,
+                                int B, unsigned* status, cudaStream_t s);
+cudaError_t launch_device_free(int* stack, int* bt, int maxb, const int* lens,
+                               const uint8_t* finished, int batch, int B, long long num_blocks,
+                               unsigned* status, cudaStream_t s);
 
 // Records `message` as the calling thread's last error; returns `code`.
 int set_last_error(int code, const char* message);

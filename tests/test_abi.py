@@ -184,3 +184,25 @@ def test_null_handle_and_error_string(pa_lib):
     assert "NULL" in pa_lib.last_error()
     pa_lib.pa_pool_destroy(None)
     assert isinstance(ctypes.c_int(pa_lib.PA_OK).value, int)
+
+
+def test_strided_pool_checks(pa_lib):
+    F = FAKE_DEV_PTR
+    D, Bs, Hkv, L, nb = 64, 16, 2, 3, 10
+    tile = Bs * D
+    ok = [(F, F + (1 << 30), Hkv * tile, 0, tile, nb, 1, Hkv),      # separate K / V caches, 1 layer
+          (F, F + (1 << 30), Hkv * tile, nb * Hkv * tile, tile, nb, L, Hkv)]  # layer-major stack
+    for kb, vb, sb, sl, sh, n, layers, heads in ok:
+        h = pa_lib.pa_pool_create_strided(kb, vb, sb, sl, sh, n, layers, heads, Bs, D, 1)
+        pa_lib.pa_pool_destroy(h)
+    bad = [(F + 8, F, Hkv * tile, 0, tile, nb, 1, Hkv),          # misaligned base
+           (F, F, Hkv * tile, 0, tile // 2, nb, 1, Hkv),          # heads overlap
+           (F, F, tile, 0, tile, nb, 1, Hkv),                     # blocks overlap heads
+           (F, F, Hkv * tile, 0, tile, nb, 2, Hkv),               # zero stride, two layers
+           (F, F, Hkv * tile + 1, 0, tile, nb, 1, Hkv),           # stride not 16-byte multiple
+           (F, F, -Hkv * tile, 0, tile, nb, 1, Hkv),              # negative
+           (F, None, Hkv * tile, 0, tile, nb, 1, Hkv)]            # NULL V base
+    for args in bad:
+        with pytest.raises(pa_lib.PagedAttnError) as e:
+            pa_lib.pa_pool_create_strided(*args, Bs, D, 1)
+        assert e.value.code == pa_lib.PA_ERR_INVALID_ARG, args

@@ -319,3 +319,55 @@ def test_decode_on_side_stream_matches(cuda_device):
     s.synchronize()
     assert max_abs_err(out, oracle_decode(wl, pool, q, 1)) <= 2e-3
     _check_status()
+
+
+def test_append_and_decode_captured_in_cuda_graph(cuda_device):
+    """One step (append + decode for every layer) captured into a CUDA graph
+    and replayed: same results as the oracle, status clean."""
+    wl = W.custom("graph", "bf16", 3, 16, 4, 128, 16, [40, 300, 17, 1000], seed=31, steps=1)
+    pool = W.make_pool(wl)
+    qs = W.make_queries(wl, 3)
+    ks, vs = W.make_new_tokens(wl, 3)
+    gp = GpuPool(wl, pool.to(cuda_device))
+    tables = wl.block_tables.copy()
+    for b, n in enumerate(wl.context_lens):
+        if n % wl.block_size == 0:
+            tables[b, n // wl.block_size] = wl.free_stack.pop()
+    bt = torch.from_numpy(tables).to(cuda_device)
+    pos = torch.from_numpy(wl.context_lens.copy()).to(cuda_device)
+    lens1 = torch.from_numpy(wl.context_lens + 1).to(cuda_device)
+    qd, kd, vd = qs.to(cuda_device), ks.to(cuda_device), vs.to(cuda_device)
+    outs = torch.zeros((3, wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32,
+                       device=cuda_device)
+    pb = 4
+    need = B.pa_decode_workspace_size(gp.h, wl.batch, wl.num_heads, wl.max_blocks, pb)
+    ws = torch.empty(need, dtype=torch.uint8, device=cuda_device)
+    B.pa_get_status()  # first launching-side call before capture (status word lookup)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for l in range(3):
+                B.pa_write_kv(gp.h, l, kd[l], vd[l], bt, wl.max_blocks, pos, wl.batch, stream=s)
+                B.pa_decode_attention_partitioned(outs[l], qd[l], gp.h, l, bt, wl.max_blocks,
+                                                  lens1, wl.batch, wl.block_size, wl.num_heads,
+                                                  wl.num_kv_heads, wl.head_dim, wl.scale, pb,
+                                                  ws, need, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.all(outs == 0), "capture must not execute the kernels"
+    g.replay()
+    g.replay()   # replaying twice rewrites the same slots: same result
+    torch.cuda.synchronize()
+    host = W.as_oracle_array(pool).copy()
+    for l in range(3):
+        oracle.write_kv(host, l, W.as_oracle_array(ks[l]), W.as_oracle_array(vs[l]), tables,
+                        wl.context_lens)
+    for l in range(3):
+        ref = oracle.decode_attention(W.as_oracle_array(qs[l]), host, l, tables,
+                                      wl.context_lens + 1, wl.num_heads, wl.scale)
+        assert max_abs_err(outs[l], ref) <= 2e-3, l
+    assert np.array_equal(W.as_oracle_array(gp.t), host)
+    _check_status()
