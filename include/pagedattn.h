@@ -128,6 +128,15 @@ PA_API int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, i
 /* Release the handle (not the caller's device tensor).  NULL is accepted. */
 PA_API int pa_pool_destroy(pa_pool* pool);
 
+/* Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
+ * the tensor-core kernel for bf16 pools (mma.sync, K/V staged by tensor-map
+ * TMA), the CUDA-core kernel for fp32 pools.  PA_DECODE_CUDA_CORES forces the
+ * CUDA-core kernel (fp32 FMA on every dtype); PA_DECODE_TENSOR_CORES makes
+ * calls that the tensor-core kernel cannot serve fail with PA_ERR_UNSUPPORTED.
+ * Both compute the same result within the stated tolerances. */
+enum { PA_DECODE_AUTO = 0, PA_DECODE_CUDA_CORES = 1, PA_DECODE_TENSOR_CORES = 2 };
+PA_API int pa_pool_set_decode_kernel(pa_pool* pool, int kind);
+
 /* Bytes of one physical block: 2 * num_layers * num_kv_heads * block_size *
  * head_dim * element size (K and V of every layer and KV head). */
 PA_API int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes);

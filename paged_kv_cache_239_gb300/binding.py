@@ -23,6 +23,10 @@ PA_ERR_CUDA = 4
 PA_ERR_UNSUPPORTED = 5
 PA_ERR_WORKSPACE = 6
 
+PA_DECODE_AUTO = 0
+PA_DECODE_CUDA_CORES = 1
+PA_DECODE_TENSOR_CORES = 2
+
 PA_DTYPE_F32 = 0
 PA_DTYPE_BF16 = 1
 
@@ -75,6 +79,7 @@ _SIGNATURES = {
                                 _I, _I, _I], _I),
     "pa_pool_destroy": ([_P], _I),
     "pa_pool_block_bytes": ([_P, _PSZ], _I),
+    "pa_pool_set_decode_kernel": ([_P, _I], _I),
     "pa_pool_seed_free_stack": ([_P, _P, _I], _I),
     "pa_alloc_block": ([_P, _PI], _I),
     "pa_free_block": ([_P, _I], _I),
@@ -199,6 +204,10 @@ def pa_pool_create_strided(k_base, v_base, block_stride: int, layer_stride: int,
 
 def pa_pool_destroy(pool: int) -> None:
     _check(lib().pa_pool_destroy(pool), "pa_pool_destroy")
+
+
+def pa_pool_set_decode_kernel(pool: int, kind: int) -> None:
+    _check(lib().pa_pool_set_decode_kernel(pool, kind), "pa_pool_set_decode_kernel")
 
 
 def pa_pool_block_bytes(pool: int) -> int:

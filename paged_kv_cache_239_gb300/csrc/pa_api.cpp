@@ -1,5 +1,6 @@
 // pa_api.cpp -- the C ABI: pool handle, free-block stack allocator, argument
 // validation and kernel launches.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -21,6 +22,12 @@ struct pa_pool {
     std::vector<int> free_stack;        // allocation pops from the back
     std::vector<unsigned char> in_use;  // 1 while a block is handed out
     bool on_device = false;             // the stack is held in a device copy
+    int decode_kernel = PA_DECODE_AUTO;
+    // tensor maps of the bf16 pool (K, V) for the tensor-core kernel, encoded
+    // on first use
+    mutable CUtensorMap tmaps[2];
+    mutable bool tmaps_ready = false;
+    mutable int tma_slots[3] = {2, 3, 4};
     mutable std::mutex mu;
 };
 
@@ -268,6 +275,15 @@ int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, int num_
 
 int pa_pool_destroy(pa_pool* pool) {
     delete pool;
+    return PA_OK;
+}
+
+int pa_pool_set_decode_kernel(pa_pool* pool, int kind) {
+    if (int rc = check_pool(pool)) return rc;
+    if (kind != PA_DECODE_AUTO && kind != PA_DECODE_CUDA_CORES && kind != PA_DECODE_TENSOR_CORES)
+        return fail(PA_ERR_INVALID_ARG, "unknown decode kernel kind %d", kind);
+    std::lock_guard<std::mutex> lock(pool->mu);
+    pool->decode_kernel = kind;
     return PA_OK;
 }
 
@@ -555,8 +571,27 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     p.new_v = new_v;
     p.positions = positions;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    e = g.dtype == 1 ? pa::launch_decode_bf16(p, g.D, g.B, sh.G, s)
-                     : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);
+    const bool mma_ok = g.dtype == 1 && pa::decode_mma_supported(g.D, g.B, sh.G);
+    if (pool->decode_kernel == PA_DECODE_TENSOR_CORES && !mma_ok)
+        return fail(PA_ERR_UNSUPPORTED, "no tensor-core decode kernel for this pool / group size");
+    if (mma_ok && pool->decode_kernel != PA_DECODE_CUDA_CORES) {
+        {
+            std::lock_guard<std::mutex> lock(pool->mu);
+            if (!pool->tmaps_ready) {
+                e = pa::encode_pool_tmaps(g, pool->tmaps, &pool->tma_slots[0],
+                                          &pool->tma_slots[1], &pool->tma_slots[2]);
+                if (e != cudaSuccess) return cuda_fail(e, "tensor map encoding");
+                pool->tmaps_ready = true;
+            }
+        }
+        p.tma_slot_blk = pool->tma_slots[0];
+        p.tma_slot_layer = pool->tma_slots[1];
+        p.tma_slot_head = pool->tma_slots[2];
+        e = pa::launch_decode_mma(p, pool->tmaps, g.D, g.B, sh.G, s);
+    } else {
+        e = g.dtype == 1 ? pa::launch_decode_bf16(p, g.D, g.B, sh.G, s)
+                         : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     if (sh.Cmax > 1) {
         e = pa::launch_combine(p, g.D, g.B, s);

@@ -1,0 +1,132 @@
+// bf16 tensor-core decode: instantiations, launch, and the tensor maps.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pa_decode_mma.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMmaWarps = 4;
+constexpr int kMmaStages = 2;
+
+template <int D, int B, int G>
+cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream_t stream) {
+    using Cfg = MmaCfg<D, B, G, kMmaWarps, kMmaStages>;
+    auto kern = pa_decode_mma_kernel<D, B, G, kMmaWarps, kMmaStages>;
+    static std::mutex mu;
+    static unsigned long long done_mask = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const unsigned long long bit = 1ull << (dev & 63);
+        if (!(done_mask & bit)) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            done_mask |= bit;
+        }
+    }
+    const long long grid = (long long)p.batch * p.Hkv * p.Cmax;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<(unsigned)grid, kMmaWarps * 32, Cfg::SMEM_BYTES, stream>>>(p, tm[0], tm[1]);
+    return cudaGetLastError();
+}
+
+template <int D, int B>
+cudaError_t launch_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_inst<D, B, 1>(p, tm, s);
+        case 2: return launch_inst<D, B, 2>(p, tm, s);
+        case 4: return launch_inst<D, B, 4>(p, tm, s);
+        case 8: return launch_inst<D, B, 8>(p, tm, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+}  // namespace
+
+bool decode_mma_supported(int D, int B, int G) {
+    if (D != 64 && D != 128) return false;
+    if (B != 16 && B != 32) return false;
+    return G == 1 || G == 2 || G == 4 || G == 8;
+}
+
+cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, int B, int G,
+                              cudaStream_t s) {
+    const CUtensorMap* tm = static_cast<const CUtensorMap*>(tmaps);
+    if (D == 64) {
+        if (B == 16) return launch_g<64, 16>(p, tm, G, s);
+        if (B == 32) return launch_g<64, 32>(p, tm, G, s);
+    } else if (D == 128) {
+        if (B == 16) return launch_g<128, 16>(p, tm, G, s);
+        if (B == 32) return launch_g<128, 32>(p, tm, G, s);
+    }
+    return cudaErrorNotSupported;
+}
+
+cudaError_t encode_pool_tmaps(const PoolGeom& g, void* tmaps, int* slot_blk, int* slot_layer,
+                              int* slot_head) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    // Outer dimensions (block, layer, kv head) ordered by increasing stride; a
+    // dimension of extent 1 gets the stride that follows the previous one.
+    struct Outer {
+        long long stride, count;
+        int which;  // 0 block, 1 layer, 2 head
+    } od[3] = {{g.s_blk, g.num_blocks, 0}, {g.s_layer, g.L, 1}, {g.s_head, g.Hkv, 2}};
+    std::sort(od, od + 3, [](const Outer& a, const Outer& b) {
+        const long long sa = a.count > 1 ? a.stride : (1LL << 62);
+        const long long sb = b.count > 1 ? b.stride : (1LL << 62);
+        return sa < sb;
+    });
+    const long long row = (long long)g.D * g.elt;  // bytes
+    cuuint64_t dims[5] = {(cuuint64_t)g.D, (cuuint64_t)g.B, 0, 0, 0};
+    cuuint64_t strides[4] = {(cuuint64_t)row, 0, 0, 0};
+    long long prev_extent = row * g.B;  // bytes of one tile
+    for (int i = 0; i < 3; ++i) {
+        long long st = od[i].stride * g.elt;
+        if (od[i].count <= 1) st = prev_extent;
+        dims[2 + i] = (cuuint64_t)od[i].count;
+        strides[1 + i] = (cuuint64_t)st;
+        prev_extent = st * od[i].count;
+        if (od[i].which == 0) *slot_blk = 2 + i;
+        if (od[i].which == 1) *slot_layer = 2 + i;
+        if (od[i].which == 2) *slot_head = 2 + i;
+    }
+    cuuint32_t box[5] = {64, 16, 1, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUtensorMap* tm = static_cast<CUtensorMap*>(tmaps);
+    void* bases[2] = {g.k_base, g.v_base};
+    for (int i = 0; i < 2; ++i) {
+        CUresult r = fn(&tm[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, bases[i], dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace pa

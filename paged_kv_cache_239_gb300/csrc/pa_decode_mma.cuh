@@ -1,0 +1,397 @@
+// pa_decode_mma.cuh -- paged decode attention for bf16 pools on the tensor
+// cores (mma.sync m16n8k16), K/V staged by 5-D tensor-map TMA with 128-byte
+// swizzle.
+//
+// Computes the same thing as pa_decode_kernel (see pa_decode.cuh): for sequence
+// b and query head h, out = softmax_t(scale * q . K_t) V_t over the tokens
+// reached through the block table ("vllmini", "PagedAttention Metaphor" / "The
+// CUDA Block Kernel"; mini-infer, "The Solution").
+//
+// Same work split as pa_decode_kernel: one CTA per (sequence, KV head,
+// partition), each warp streams every NW-th block of the partition through its
+// own S-stage pipeline.  What differs is the inner product machinery, chosen
+// to cut the instruction count per token (the CUDA-core kernel is issue-bound):
+//  * a stage holds 16 rows of K and 16 rows of V, each as D/64 TMA boxes of
+//    16 x 64 bf16 with SWIZZLE_128B, so ldmatrix reads are bank-conflict free;
+//  * S = K Q^T on mma.sync: M = 16 tokens, N = 8 query heads of the group
+//    (heads >= G are zero), K = head_dim; the scale is applied to S in fp32;
+//  * online softmax on the S fragments (a lane holds 2 tokens x 2 heads);
+//  * P is split into bf16 hi + lo parts (|P - hi - lo| <= 2^-16 P), transposed
+//    in registers with movmatrix, and O^T = V^T P accumulates on mma.sync with
+//    M = 16 head-dim rows, N = 8 heads, K = 16 tokens (V^T via ldmatrix.trans).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <int D_, int B_, int G_, int NW_, int S_>
+struct MmaCfg {
+    static constexpr int D = D_, B = B_, G = G_, NW = NW_, S = S_;
+    static constexpr int R = 16;                   // rows per stage
+    static constexpr int SPB = B / R;              // stages per block
+    static constexpr int NBOX = D / 64;            // 64-element (128-byte) boxes per row
+    static constexpr int BOX_BYTES = R * 128;      // one swizzled 16 x 128 B box
+    static constexpr int TILE_BYTES = NBOX * BOX_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile, then V tile
+    static constexpr int KS = D / 16;              // k-steps of S = K Q^T
+    static constexpr int MT = D / 16;              // m-tiles of O^T = V^T P
+    static constexpr int WARP_STAGE_BYTES = S * STAGE_BYTES;
+    static constexpr int META_BYTES = 64;          // per warp: nvalid[S], mbarriers[S]
+    static constexpr int SMEM_BYTES = NW * WARP_STAGE_BYTES + NW * META_BYTES + 1024;
+
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(B % R == 0, "block size must be a multiple of 16");
+    static_assert(G >= 1 && G <= 8, "GQA group of at most 8 query heads");
+    static_assert(S * 12 <= META_BYTES, "meta");
+    static_assert((2 * G + G * D) * 4 <= WARP_STAGE_BYTES, "merge area must fit in the stages");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// Byte offset of (row t, 16-byte chunk j) inside a K or V tile stored as D/64
+// boxes of 16 rows x 128 bytes with the 128-byte swizzle (chunk j of row t sits
+// at chunk j ^ (t % 8) of its 128-byte row).
+__device__ __forceinline__ uint32_t swz_offset(int t, int j) {
+    return (uint32_t)((j >> 3) * (16 * 128) + t * 128 + (((j & 7) ^ (t & 7)) << 4));
+}
+
+template <int D, int B, int G, int NW, int S>
+__global__ void __launch_bounds__(NW * 32)
+    pa_decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                         const __grid_constant__ CUtensorMap tmv) {
+    using C = MmaCfg<D, B, G, NW, S>;
+    extern __shared__ unsigned char smem_raw[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;  // mma group id
+    const int cq = lane & 3;  // thread within the group
+
+    int idx = blockIdx.x;
+    const int c = idx % p.Cmax;
+    idx /= p.Cmax;
+    const int kvh = idx % p.Hkv;
+    const int b = idx / p.Hkv;
+
+    int n = __ldg(p.lens + b);
+    if (n < 0 || n > p.maxb * B) {
+        if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+        n = 0;
+    }
+    const int nblk = (n + B - 1) / B;
+    const int nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
+    if (c >= nparts) return;
+    const int pb0 = c * p.PB;
+    const int pb1 = min(nblk, pb0 + p.PB);
+
+    // 1024-byte aligned stage area (swizzle atoms), then per-warp metadata.
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    unsigned char* smem = smem_raw + (base_addr - raw_addr);
+    unsigned char* wbase = smem + warp * C::WARP_STAGE_BYTES;
+    const uint32_t stage0 = base_addr + warp * C::WARP_STAGE_BYTES;
+    unsigned char* meta = smem + NW * C::WARP_STAGE_BYTES + warp * C::META_BYTES;
+    int* s_nvalid = reinterpret_cast<int*>(meta);
+    const uint32_t bars = smem_addr(meta + 16);
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
+        fence_mbar_init();
+        if (warp == 0) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+        }
+    }
+    __syncwarp();
+
+    const int span = pb1 - pb0;
+    const int nk = span > warp ? (span - warp + NW - 1) / NW : 0;
+    int U = 0;
+    if (nk > 0) {
+        const int jb_last = pb0 + warp + (nk - 1) * NW;
+        const int rows_last = min(B, n - jb_last * B);
+        U = (nk - 1) * C::SPB + (rows_last + C::R - 1) / C::R;
+    }
+
+    const int* bt_row = p.bt + (long long)b * p.maxb;
+    const long long tile0 = p.tile_off + (long long)kvh * p.s_head;
+
+    // fused append (see pa_decode_kernel): store the new row before any TMA read
+    if (p.new_k != nullptr) {
+        const int pos = __ldg(p.positions + b);
+        if (pos < 0 || pos / B >= p.maxb) {
+            if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+        } else if (c == (pos < n ? (pos / B) / p.PB : 0)) {
+            constexpr int CPR = D * 2 / 16;
+            const int blk = __ldg(bt_row + pos / B);
+            if (blk < 0 || blk >= p.num_blocks) {
+                if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
+            } else if (threadIdx.x < 2 * CPR) {
+                const int kv = threadIdx.x / CPR;
+                const int ci = threadIdx.x % CPR;
+                const long long src = ((long long)b * p.Hkv + kvh) * (D * 2) + ci * 16;
+                const long long off = (long long)blk * p.s_blk + tile0 + (long long)(pos % B) * D;
+                const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                    static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src));
+                unsigned short* dst = const_cast<unsigned short*>(
+                    reinterpret_cast<const unsigned short*>(kv ? p.v_base : p.k_base)) + off;
+                reinterpret_cast<uint4*>(dst)[ci] = val;
+                fence_proxy_async_global();
+            }
+        }
+        __syncthreads();
+    }
+
+    const uint64_t policy = l2_policy_evict_first();
+    int kbase = 0;
+    int myid = (lane < nk) ? __ldg(bt_row + pb0 + warp + lane * NW) : -1;
+
+    auto issue = [&](int u) {
+        const int k = u / C::SPB;
+        const int sub = u % C::SPB;
+        if (k >= kbase + 32) {
+            kbase += 32;
+            const int kk = kbase + lane;
+            myid = (kk < nk) ? __ldg(bt_row + pb0 + warp + kk * NW) : -1;
+        }
+        const int blk = __shfl_sync(kFullMask, myid, k - kbase);
+        const int jb = pb0 + warp + k * NW;
+        const int row0 = sub * C::R;
+        const int rows = min(C::R, n - (jb * B + row0));
+        const int stage = u % S;
+        if (lane == 0) {
+            const uint32_t bar = bars + 8 * stage;
+            if (blk >= 0 && blk < p.num_blocks) {
+                s_nvalid[stage] = rows;
+                mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+                // outer coordinates in the tensor map's dimension order
+                const int o2 = p.tma_slot_blk == 2 ? blk : (p.tma_slot_layer == 2 ? p.layer : kvh);
+                const int o3 = p.tma_slot_blk == 3 ? blk : (p.tma_slot_layer == 3 ? p.layer : kvh);
+                const int o4 = p.tma_slot_blk == 4 ? blk : (p.tma_slot_layer == 4 ? p.layer : kvh);
+                const uint32_t dst = stage0 + stage * C::STAGE_BYTES;
+#pragma unroll
+                for (int bx = 0; bx < C::NBOX; ++bx) {
+                    tma_load_5d(dst + bx * C::BOX_BYTES, &tmk, bar, bx * 64, row0, o2, o3, o4,
+                                policy);
+                    tma_load_5d(dst + C::TILE_BYTES + bx * C::BOX_BYTES, &tmv, bar, bx * 64, row0,
+                                o2, o3, o4, policy);
+                }
+            } else {
+                s_nvalid[stage] = 0;
+                atomicOr(p.status, kStatusBadBlock);
+                mbar_arrive(bar);
+            }
+        }
+    };
+
+    // q of the group as mma B fragments: b0 = q[g][16ks+2cq..+1], b1 = q[g][16ks+8+2cq..+1]
+    uint32_t qb[C::KS][2];
+    {
+        const unsigned short* qrow =
+            reinterpret_cast<const unsigned short*>(p.q) + ((long long)b * p.H + kvh * G + g) * D;
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+            if (g < G) {
+                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * cq);
+                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * cq);
+            } else {
+                qb[ks][0] = 0u;
+                qb[ks][1] = 0u;
+            }
+        }
+    }
+
+    float o[C::MT][4];
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
+    // running max / sum of heads 2cq and 2cq+1 (the sum is this lane's share)
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const bool h0_ok = 2 * cq < G;
+    const bool h1_ok = 2 * cq + 1 < G;
+
+    int u_issue = 0;
+    const int npro = U < S ? U : S;
+    for (; u_issue < npro; ++u_issue) issue(u_issue);
+
+    int u = 0;
+    bool timed_out = false;
+    for (; u < U; ++u) {
+        const int stage = u % S;
+        const bool ok = mbar_wait_bounded(bars + 8 * stage, (u / S) & 1);
+        if (__any_sync(kFullMask, !ok)) {
+            timed_out = true;
+            break;
+        }
+        const int rows = s_nvalid[stage];
+        if (rows > 0) {
+            const uint32_t ktile = stage0 + stage * C::STAGE_BYTES;
+            const uint32_t vtile = ktile + C::TILE_BYTES;
+            if (rows < C::R) {
+                // rows past the context are zeroed so that 0 * (stale value) stays 0
+                unsigned char* vt = wbase + stage * C::STAGE_BYTES + C::TILE_BYTES;
+                for (int i = lane; i < (C::R - rows) * 8 * C::NBOX; i += 32) {
+                    const int t = rows + i / (8 * C::NBOX);
+                    const int j = i % (8 * C::NBOX);
+                    *reinterpret_cast<uint4*>(vt + swz_offset(t, j)) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+
+            // ---- S = K Q^T (16 tokens x 8 heads) ----
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                const int mtx = lane >> 3;
+                const int t = (lane & 7) + 8 * (mtx & 1);
+#pragma unroll
+                for (int ks = 0; ks < C::KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(ktile + swz_offset(t, 2 * ks + (mtx >> 1)), a0, a1, a2, a3);
+                    mma_bf16_16816(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
+            }
+            // ---- online softmax: lane has tokens g, g+8 x heads 2cq, 2cq+1 ----
+            const bool t0_ok = g < rows;
+            const bool t1_ok = g + 8 < rows;
+            float s00 = (t0_ok && h0_ok) ? sacc[0] * p.qscale : -INFINITY;
+            float s01 = (t0_ok && h1_ok) ? sacc[1] * p.qscale : -INFINITY;
+            float s10 = (t1_ok && h0_ok) ? sacc[2] * p.qscale : -INFINITY;
+            float s11 = (t1_ok && h1_ok) ? sacc[3] * p.qscale : -INFINITY;
+            float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            // (heads past the group keep O = 0, so their factor is left at 1)
+            const float a0s = !h0_ok ? 1.f : (m0 == -INFINITY ? 0.f : exp2f(m0 - mn0));
+            const float a1s = !h1_ok ? 1.f : (m1 == -INFINITY ? 0.f : exp2f(m1 - mn1));
+            const float p00 = (s00 == -INFINITY) ? 0.f : exp2f(s00 - mn0);
+            const float p01 = (s01 == -INFINITY) ? 0.f : exp2f(s01 - mn1);
+            const float p10 = (s10 == -INFINITY) ? 0.f : exp2f(s10 - mn0);
+            const float p11 = (s11 == -INFINITY) ? 0.f : exp2f(s11 - mn1);
+            l0 = l0 * a0s + p00 + p10;
+            l1 = l1 * a1s + p01 + p11;
+            m0 = mn0;
+            m1 = mn1;
+            if (a0s != 1.f || a1s != 1.f) {
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    o[mt][0] *= a0s;
+                    o[mt][1] *= a1s;
+                    o[mt][2] *= a0s;
+                    o[mt][3] *= a1s;
+                }
+            }
+            // ---- P -> bf16 hi + lo, transposed into mma B fragments ----
+            const __nv_bfloat162 hi_t = __floats2bfloat162_rn(p00, p01);
+            const __nv_bfloat162 hi_b = __floats2bfloat162_rn(p10, p11);
+            const __nv_bfloat162 lo_t = __floats2bfloat162_rn(p00 - __low2float(hi_t),
+                                                              p01 - __high2float(hi_t));
+            const __nv_bfloat162 lo_b = __floats2bfloat162_rn(p10 - __low2float(hi_b),
+                                                              p11 - __high2float(hi_b));
+            const uint32_t bh0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&hi_t));
+            const uint32_t bh1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&hi_b));
+            const uint32_t bl0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&lo_t));
+            const uint32_t bl1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&lo_b));
+            // ---- O^T += V^T P ----
+            {
+                const int mtx = lane >> 3;
+                const int t = (lane & 7) + 8 * (mtx >> 1);
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    uint32_t v0, v1, v2, v3;
+                    ldmatrix_x4_trans(vtile + swz_offset(t, 2 * mt + (mtx & 1)), v0, v1, v2, v3);
+                    mma_bf16_16816(o[mt], v0, v1, v2, v3, bh0, bh1);
+                    mma_bf16_16816(o[mt], v0, v1, v2, v3, bl0, bl1);
+                }
+            }
+        }
+        __syncwarp();
+        if (u_issue < U) {
+            fence_proxy_async_smem();
+            issue(u_issue);
+            ++u_issue;
+        }
+    }
+    if (timed_out) {
+        if (lane == 0) atomicOr(p.status, kStatusTimeout);
+        for (int w = u; w < u_issue; ++w) (void)mbar_wait_bounded(bars + 8 * (w % S), (w / S) & 1);
+    }
+
+    // ---- warp totals: l over the 8 lanes sharing cq ----
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(kFullMask, l0, off);
+        l1 += __shfl_xor_sync(kFullMask, l1, off);
+    }
+    __syncwarp();
+    float* w_m = reinterpret_cast<float*>(wbase);
+    float* w_l = w_m + G;
+    float* w_acc = w_l + G;  // [G][D]
+    if (g == 0) {
+        if (h0_ok) {
+            w_m[2 * cq] = m0;
+            w_l[2 * cq] = l0;
+        }
+        if (h1_ok) {
+            w_m[2 * cq + 1] = m1;
+            w_l[2 * cq + 1] = l1;
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt) {
+        const int d = 16 * mt + g;
+        if (h0_ok) {
+            w_acc[(2 * cq) * D + d] = o[mt][0];
+            w_acc[(2 * cq) * D + d + 8] = o[mt][2];
+        }
+        if (h1_ok) {
+            w_acc[(2 * cq + 1) * D + d] = o[mt][1];
+            w_acc[(2 * cq + 1) * D + d + 8] = o[mt][3];
+        }
+    }
+    __syncthreads();
+
+    // ---- merge the NW warps (log-sum-exp) and write ----
+    const long long head0 = (long long)b * p.H + kvh * G;
+    for (int t = threadIdx.x; t < G * D; t += NW * 32) {
+        const int h = t / D;
+        const int d = t % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w)
+            M = fmaxf(M, reinterpret_cast<const float*>(smem + w * C::WARP_STAGE_BYTES)[h]);
+        float Lsum = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            const float* wm = reinterpret_cast<const float*>(smem + w * C::WARP_STAGE_BYTES);
+            const float mw = wm[h];
+            const float wt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            Lsum += wt * wm[G + h];
+            O += wt * wm[2 * G + h * D + d];
+        }
+        if (nparts == 1) {
+            p.out[(head0 + h) * D + d] = Lsum > 0.f ? O / Lsum : 0.f;
+        } else {
+            const long long slot = (head0 + h) * p.Cmax + c;
+            p.part_o[slot * D + d] = O;
+            if (d == 0) {
+                p.part_ml[slot * 2 + 0] = M;
+                p.part_ml[slot * 2 + 1] = Lsum;
+            }
+        }
+    }
+}
+
+}  // namespace pa

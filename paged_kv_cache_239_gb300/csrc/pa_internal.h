@@ -53,6 +53,9 @@ struct DecodeParams {
     const void* new_k;
     const void* new_v;
     const int* positions;
+    // tensor-core kernel only: which of the tensor maps' outer dimensions
+    // (2, 3, 4) index the physical block, the layer and the kv head
+    int tma_slot_blk, tma_slot_layer, tma_slot_head;
 };
 
 struct WriteParams {
@@ -91,6 +94,15 @@ struct GatherParams {
 cudaError_t launch_decode_bf16(const DecodeParams& p, int D, int B, int G, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeParams& p, int D, int B, int G, cudaStream_t s);
 bool decode_supported(int dtype, int D, int B, int G);
+
+// Tensor-core kernel for bf16 pools; `tmaps` points to two CUtensorMap (K, V).
+bool decode_mma_supported(int D, int B, int G);
+cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, int B, int G,
+                              cudaStream_t s);
+// Encodes the K and V tensor maps of a bf16 pool (5-D, box 64 x 16, 128-byte
+// swizzle) into tmaps[0..1]; slots receives the outer-dimension order.
+cudaError_t encode_pool_tmaps(const PoolGeom& g, void* tmaps, int* slot_blk, int* slot_layer,
+                              int* slot_head);
 
 cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s);
 cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);

@@ -44,12 +44,21 @@ def test_decode_grid_all_partitionings(cuda_device, dtype, D, Bs, G):
     bt, ln = device_tables(wl, cuda_device)
     qd = q.to(cuda_device)
     ref = oracle_decode(wl, pool, q, 1)
-    for pb in (0, 1, 2, 3, wl.max_blocks):
-        out = gpu_decode(gp, qd, 1, bt, ln, partition_blocks=pb)
-        torch.cuda.synchronize()
-        err = max_abs_err(out, ref)
-        assert err <= TOL[dtype], f"partition_blocks={pb}: max abs err {err}"
-        assert torch.isfinite(out).all()
+    kinds = [B.PA_DECODE_TENSOR_CORES, B.PA_DECODE_CUDA_CORES] if dtype == "bf16" else \
+        [B.PA_DECODE_AUTO]
+    for kind in kinds:
+        B.pa_pool_set_decode_kernel(gp.h, kind)
+        for pb in (0, 1, 2, 3, wl.max_blocks):
+            out = gpu_decode(gp, qd, 1, bt, ln, partition_blocks=pb)
+            torch.cuda.synchronize()
+            err = max_abs_err(out, ref)
+            assert err <= TOL[dtype], f"kernel {kind}, partition_blocks={pb}: max abs err {err}"
+            assert torch.isfinite(out).all()
+    if dtype == "f32":
+        B.pa_pool_set_decode_kernel(gp.h, B.PA_DECODE_TENSOR_CORES)
+        with pytest.raises(B.PagedAttnError) as e:
+            gpu_decode(gp, qd, 1, bt, ln)
+        assert e.value.code == B.PA_ERR_UNSUPPORTED
     _check_status()
     gp.close()
 
@@ -90,9 +99,11 @@ def test_decode_long_context_split(cuda_device):
     bt, ln = device_tables(wl, cuda_device)
     pb = B.pa_decode_partition_blocks(gp.h, wl.batch, wl.num_heads, wl.max_blocks)
     assert pb < wl.max_blocks, "the long-context workload must take the split path"
-    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
     ref = oracle_decode(wl, pool, q, 0)
-    assert max_abs_err(out, ref) <= 2e-3
+    for kind in (B.PA_DECODE_AUTO, B.PA_DECODE_CUDA_CORES):
+        B.pa_pool_set_decode_kernel(gp.h, kind)
+        out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
+        assert max_abs_err(out, ref) <= 2e-3, kind
     _check_status()
 
 
@@ -110,12 +121,14 @@ def test_decode_large_batch_sampled(cuda_device):
     seqs = sorted(set([int(order[0]), int(order[-1])] + [int(x) for x in rng.choice(wl.batch, 10,
                                                                                      replace=False)]))
     for layer in (0, wl.num_layers - 1):
-        out = gpu_decode(gp, qs[layer % 2], layer, bt, ln)
-        torch.cuda.synchronize()
-        assert torch.isfinite(out).all()
         refs = oracle_decode_sampled(wl, pool, qs[layer % 2], layer, seqs)
-        for b, ref in refs.items():
-            assert max_abs_err(out[b], ref) <= 2e-3, (layer, b)
+        for kind in (B.PA_DECODE_AUTO, B.PA_DECODE_CUDA_CORES):
+            B.pa_pool_set_decode_kernel(gp.h, kind)
+            out = gpu_decode(gp, qs[layer % 2], layer, bt, ln)
+            torch.cuda.synchronize()
+            assert torch.isfinite(out).all()
+            for b, ref in refs.items():
+                assert max_abs_err(out[b], ref) <= 2e-3, (layer, b, kind)
     _check_status()
     gp.close()
     del pool
