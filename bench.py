@@ -8,7 +8,9 @@ One step = one decode step of the whole model's attention: for each of the 32
 layers, append the new token's K/V (pa_write_kv, into the last context slot) and
 run pa_decode_attention over the context (split-K + combine when partitioned).
 Each layer reads ~2.2 GB of K/V, far more than the 129 MB L2, so no flush is
-needed between steps.
+needed between steps.  By default the K timed steps run as one CUDA graph
+replay (the calls captured once, each decode call bracketed by event-record
+nodes for its per-call time); --no-graph launches every call from the host.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 Under torchrun every rank runs an independent replica (weak scaling, no
@@ -58,14 +60,15 @@ def decode_flops(wl) -> int:
     return int(wl.context_lens.astype(np.int64).sum()) * 4 * wl.num_heads * wl.head_dim
 
 
-# DRAM bytes (read + write) of one pa_decode_kernel launch on this workload,
-# from `ncu --set full` (profiles/pa_decode_kernel__large_batch_*.md), valid only
-# for the kernel sources they were taken from.
+# DRAM bytes (read + write) of one pa_decode_attention call on this workload:
+# pa_decode_mma_kernel (ncu --set full) + pa_combine_kernel (ncu dram metrics),
+# see profiles/; valid only for the kernel sources they were taken from.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2223014000 + 6228480,
-    "sources_sha256": "d472b81370cc6a2abb2460c285814a52cd86a657cb4dfc3aef8672e6c3a4cbce",
+    "bytes_per_launch": 2231026000 + 6745856 + 9854464,
+    "sources_sha256": "f9f7c589f25a139ca9c91ba710653b5f4a46e8bac41ea64b2aa4b4855729d2f3",
 }
-DECODE_SOURCES = ["pa_decode.cuh", "pa_decode_launch.cuh", "pa_decode_bf16.cu", "pa_device.cuh"]
+DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
+                  "pa_internal.h"]
 
 
 def decode_sources_sha256() -> str:
@@ -291,7 +294,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     outs = torch.empty((L, wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    cur = {"sp": stream.cuda_stream}
+    cur = {"sp": stream.cuda_stream, "stream": stream}
     lib = B.lib()
     cmax = -(-wl.max_blocks // pb)
     launches_per_step = L * ((1 if args.fused else 2) + (1 if cmax > 1 else 0))
@@ -299,7 +302,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     def layer_call(l, ev=None):
         if args.fused:
             if ev is not None:
-                ev[0].record(stream)
+                ev[0].record(cur["stream"])
             rc = lib.pa_write_kv_and_decode(outs[l].data_ptr(), qs[l].data_ptr(), h, l,
                                             ks[l].data_ptr(), vs[l].data_ptr(),
                                             positions.data_ptr(), bt.data_ptr(), wl.max_blocks,
@@ -309,14 +312,14 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             if rc:
                 raise RuntimeError(B.last_error())
             if ev is not None:
-                ev[1].record(stream)
+                ev[1].record(cur["stream"])
             return
         rc = lib.pa_write_kv(h, l, ks[l].data_ptr(), vs[l].data_ptr(), bt.data_ptr(),
                              wl.max_blocks, positions.data_ptr(), wl.batch, cur["sp"])
         if rc:
             raise RuntimeError(B.last_error())
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(cur["stream"])
         rc = lib.pa_decode_attention(outs[l].data_ptr(), qs[l].data_ptr(), h, l, bt.data_ptr(),
                                      wl.max_blocks, lens.data_ptr(), wl.batch, wl.block_size,
                                      wl.num_heads, wl.num_kv_heads, wl.head_dim, wl.scale,
@@ -324,7 +327,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         if rc:
             raise RuntimeError(B.last_error())
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(cur["stream"])
 
     def barrier():
         if world > 1:
@@ -339,46 +342,64 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     if st:
         raise RuntimeError(f"device status {st:#x} after warm-up")
 
-    # ---- optional: one whole step captured as a CUDA graph ----
-    graph = None
-    if args.graph:
-        graph = torch.cuda.CUDAGraph()
+    # ---- CUDA graphs (default): the timed K steps as one graph whose decode
+    #      calls are bracketed by event-record nodes, and a one-step graph for
+    #      the end-to-end leg ----
+    use_graph = not args.no_graph
+    graph = step_graph = None
+    ev_kw = {"enable_timing": True, "external": True} if use_graph else {"enable_timing": True}
+    evs = [[(torch.cuda.Event(**ev_kw), torch.cuda.Event(**ev_kw)) for _ in range(L)]
+           for _ in range(args.steps)]
+
+    def capture(body):
+        g_ = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream(dev)
         side.wait_stream(stream)
         with torch.cuda.stream(side):
             cur["sp"] = side.cuda_stream
-            with torch.cuda.graph(graph, stream=side):
-                for l in range(L):
-                    layer_call(l)
+            cur["stream"] = side
+            with torch.cuda.graph(g_, stream=side):
+                body()
             cur["sp"] = stream.cuda_stream
+            cur["stream"] = stream
         stream.wait_stream(side)
+        return g_
+
+    if use_graph:
+        def all_steps():
+            for s in range(args.steps):
+                for l in range(L):
+                    layer_call(l, evs[s][l])
+
+        def one_step():
+            for l in range(L):
+                layer_call(l)
+
+        graph = capture(all_steps)
+        step_graph = capture(one_step)
         for _ in range(args.warmup):
-            graph.replay()
+            step_graph.replay()
+        graph.replay()   # untimed: the first launch of a graph uploads it to the device
         torch.cuda.synchronize()
 
     # ---- timed region: device-resident inputs ----
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(L)] for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clocks:
         t_start.record(stream)
-        for s in range(args.steps):
-            if graph is not None:
-                graph.replay()
-            else:
+        if graph is not None:
+            graph.replay()
+        else:
+            for s in range(args.steps):
                 for l in range(L):
                     layer_call(l, evs[s][l])
         t_end.record(stream)
         torch.cuda.synchronize()
     barrier()
     total_ms = t_start.elapsed_time(t_end)
-    if graph is not None:   # no per-call events inside a replay: the step bounds each call
-        call_ms = [total_ms / (args.steps * L)]
-    else:
-        call_ms = [a.elapsed_time(b) for row in evs for (a, b) in row]
+    call_ms = [a.elapsed_time(b) for row in evs for (a, b) in row]
     st = B.pa_get_status()
     if st:
         raise RuntimeError(f"device status {st:#x} after the timed region")
@@ -403,8 +424,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             bt.copy_(bt_h, non_blocking=True)
             lens.copy_(lens_h, non_blocking=True)
             positions.copy_(pos_h, non_blocking=True)
-            if graph is not None:
-                graph.replay()
+            if step_graph is not None:
+                step_graph.replay()
             else:
                 for l in range(L):
                     layer_call(l)
@@ -473,7 +494,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             "block_size": wl.block_size, "num_layers": L,
             "context_lens": f"seed {wl.seed}, min {wl.context_lens.min()}, max "
                             f"{wl.context_lens.max()}, mean {wl.context_lens.mean():.0f}",
-            "cuda_graph": bool(args.graph),
+            "cuda_graph": use_graph,
             "pool_gb": round(wl.pool_bytes() / 1e9, 1), "partition_blocks": pb,
             "l2": l2_note(wl, L),
             "parallelism": f"replicas x{world}",
@@ -483,7 +504,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "roofline": {"bound": "hbm", "kernel": "pa_decode_attention (decode + combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs", "traffic": decode_traffic(),
-                     "traffic_kernel": "pa_decode_kernel (ncu dram read+write per launch)",
+                     "traffic_kernel": "pa_decode_mma_kernel + pa_combine_kernel, ncu dram "
+                                       "read+write per call",
                      "algorithmic_bytes_per_call": per_call,
                      "avg_call_ms": call_avg_ms},
         "cpu_baseline": cpu,
@@ -722,8 +744,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="layers per step (0 = all)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_CFG, choices=[1, 2, 3, 4, 5],
                     help="named workload (default: the large-batch one, the headline)")
-    ap.add_argument("--graph", action="store_true",
-                    help="capture one step (all layers) as a CUDA graph and replay it")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every call from the host instead of replaying CUDA graphs")
     ap.add_argument("--row", choices=["step", "gather", "loop"], default="step",
                     help="step: append+decode per layer (headline); gather: pa_gather_kv "
                          "bandwidth; loop: the append+decode loop with block allocation")
