@@ -343,6 +343,13 @@ PA_API int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* 
  * Device status.
  * ------------------------------------------------------------------------- */
 
+/* Failure-detection self-test: launches one warp that waits on a shared-memory
+ * barrier no copy or thread ever completes.  The bounded wait used by every
+ * kernel of this library gives up (here after 20 ms), PA_STATUS_TIMEOUT is
+ * raised in the status word and the kernel returns; the context stays usable.
+ * No fault, trap or hang is involved. */
+PA_API int pa_selftest_wait_timeout(pa_stream_t stream);
+
 /* Wait for `stream`, return the current device's status bits (PA_STATUS_*)
  * accumulated since the last call, and clear them.  Blocking. */
 PA_API int pa_get_status(unsigned int* status, pa_stream_t stream);

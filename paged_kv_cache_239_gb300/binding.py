@@ -101,6 +101,7 @@ _SIGNATURES = {
         [_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _I, _P], _I),
     "pa_gather_kv": ([_P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P], _I),
     "pa_get_status": ([_PU, _P], _I),
+    "pa_selftest_wait_timeout": ([_P], _I),
 }
 
 
@@ -360,3 +361,7 @@ def pa_get_status(stream=None) -> int:
     v = ctypes.c_uint()
     _check(lib().pa_get_status(ctypes.byref(v), _stream(stream)), "pa_get_status")
     return v.value
+
+
+def pa_selftest_wait_timeout(stream=None) -> None:
+    _check(lib().pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")

@@ -674,6 +674,15 @@ int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, i
     return PA_OK;
 }
 
+int pa_selftest_wait_timeout(pa_stream_t stream) {
+    unsigned* status = nullptr;
+    cudaError_t e = pa::status_word(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
+    e = pa::launch_wait_selftest(status, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_selftest_wait_timeout launch");
+    return PA_OK;
+}
+
 int pa_get_status(unsigned int* status, pa_stream_t stream) {
     if (!status) return fail(PA_ERR_INVALID_ARG, "status is NULL");
     cudaError_t e = pa::read_and_clear_status(status, reinterpret_cast<cudaStream_t>(stream));

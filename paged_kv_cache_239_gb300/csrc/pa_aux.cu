@@ -44,6 +44,28 @@ cudaError_t read_and_clear_status(unsigned* host_value, cudaStream_t s) {
     return cudaMemset(dptr, 0, sizeof(unsigned));
 }
 
+// Self-test of the bounded wait: one warp waits on an mbarrier phase that no
+// thread or copy ever completes.  The wait gives up after 20 ms, the kernel
+// records PA_STATUS_TIMEOUT and returns; the context stays usable.
+constexpr unsigned long long kSelftestWaitNs = 20000000ull;
+
+__global__ void pa_wait_selftest_kernel(unsigned* status) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t a = smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(a, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded<kSelftestWaitNs>(a, 0);
+    if (!__all_sync(kFullMask, ok) && threadIdx.x == 0) atomicOr(status, kStatusTimeout);
+}
+
+cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s) {
+    pa_wait_selftest_kernel<<<1, 32, 0, s>>>(status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) {
     const long long warps = (long long)p.batch * p.H;
     if (warps <= 0) return cudaSuccess;
@@ -150,9 +172,80 @@ __global__ void __launch_bounds__(256) pa_gather_kv_kernel(const GatherParams p)
     }
 }
 
+// Tiled gather: one CTA per (logical block j, sequence b).  A thread owns one
+// 16-byte chunk of a row (CPR chunks per row, 256 / CPR rows per pass) and
+// walks the (K/V, kv head) pairs four at a time, so four independent loads are
+// in flight before the stores.  Rows past the length (or behind a bad block id)
+// are written as zeros; the mask rows of the block are written once.
+template <int CPR>
+__global__ void __launch_bounds__(256) pa_gather_kv_tiled(const GatherParams p) {
+    constexpr int RPP = 256 / CPR;  // rows per pass
+    const int j = blockIdx.x;
+    const int b = blockIdx.y;
+    const int t0 = j * p.B;
+    const int rows_here = min(p.B, p.max_len - t0);
+    int n = __ldg(p.lens + b);
+    if (n < 0 || n > p.max_len || n > p.maxb * p.B) {
+        if (j == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+        n = 0;
+    }
+    int valid = min(max(n - t0, 0), rows_here);
+    int blk = -1;
+    if (valid > 0) {
+        blk = __ldg(p.bt + (long long)b * p.maxb + j);
+        if (blk < 0 || blk >= p.num_blocks) {
+            if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
+            valid = 0;
+        }
+    }
+    if (threadIdx.x < rows_here)
+        p.mask[(long long)b * p.max_len + t0 + threadIdx.x] = threadIdx.x < valid ? 1 : 0;
+    const int ci = threadIdx.x % CPR;
+    const int elems_per_row = p.row_bytes / p.elt;
+    const long long head_bytes = p.s_head * p.elt;
+    for (int r = threadIdx.x / CPR; r < rows_here; r += RPP) {
+        const bool live = r < valid;
+        const long long src_row =
+            live ? ((long long)blk * p.s_blk + p.tile_off + (long long)r * elems_per_row) * p.elt : 0;
+        const long long dst_row = ((long long)b * p.max_len + t0 + r) * p.Hkv;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const unsigned char* sbase =
+                static_cast<const unsigned char*>(kv ? p.v_base : p.k_base) + src_row + ci * 16;
+            unsigned char* dbase = static_cast<unsigned char*>(kv ? p.v_out : p.k_out) +
+                                   dst_row * p.row_bytes + ci * 16;
+            for (int h0 = 0; h0 < p.Hkv; h0 += 4) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    v[u] = make_uint4(0u, 0u, 0u, 0u);
+                    if (live && h0 + u < p.Hkv)
+                        v[u] = __ldg(reinterpret_cast<const uint4*>(sbase + (h0 + u) * head_bytes));
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (h0 + u < p.Hkv)
+                        *reinterpret_cast<uint4*>(dbase + (long long)(h0 + u) * p.row_bytes) = v[u];
+            }
+        }
+    }
+}
+
 cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s) {
     const long long total = (long long)p.batch * p.max_len * p.Hkv * 2 * (p.row_bytes / 16);
     if (total <= 0) return cudaSuccess;
+    const long long nj = ((long long)p.max_len + p.B - 1) / p.B;
+    const int cpr = p.row_bytes / 16;
+    if (p.batch <= 65535 && nj <= 0x7fffffffLL && p.B <= 256 && (cpr == 8 || cpr == 16 || cpr == 32)) {
+        const dim3 grid((unsigned)nj, (unsigned)p.batch);
+        if (cpr == 8)
+            pa_gather_kv_tiled<8><<<grid, 256, 0, s>>>(p);
+        else if (cpr == 16)
+            pa_gather_kv_tiled<16><<<grid, 256, 0, s>>>(p);
+        else
+            pa_gather_kv_tiled<32><<<grid, 256, 0, s>>>(p);
+        return cudaGetLastError();
+    }
     long long blocks = (total + 255) / 256;
     const long long cap = (long long)num_sms * 16;
     if (blocks > cap) blocks = cap;

@@ -72,13 +72,14 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 // Waits for the barrier phase with the given parity.  Returns false (instead of
-// spinning forever) once kWaitLimitNs have passed.
+// spinning forever) once LimitNs nanoseconds have passed.
+template <unsigned long long LimitNs = kWaitLimitNs>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 0; it < (1u << 30); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > LimitNs) return false;
     }
     return false;
 }

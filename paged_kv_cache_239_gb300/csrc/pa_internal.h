@@ -105,6 +105,7 @@ cudaError_t encode_pool_tmaps(const PoolGeom& g, void* tmaps, int* slot_blk, int
                               int* slot_head);
 
 cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s);
 cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s);
 

@@ -384,3 +384,26 @@ def test_append_and_decode_captured_in_cuda_graph(cuda_device):
         assert max_abs_err(outs[l], ref) <= 2e-3, l
     assert np.array_equal(W.as_oracle_array(gp.t), host)
     _check_status()
+
+
+def test_bounded_wait_times_out_into_status(cuda_device):
+    """A barrier nothing completes: the bounded wait gives up, the status word
+    says PA_STATUS_TIMEOUT, and a following decode still works."""
+    assert B.pa_get_status() == 0
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    B.pa_selftest_wait_timeout()
+    t1.record()
+    assert B.pa_get_status() == B.PA_STATUS_TIMEOUT
+    assert 10.0 <= t0.elapsed_time(t1) < 2000.0     # about the 20 ms limit
+    assert B.pa_get_status() == 0                    # read-and-clear
+    wl = W.custom("after", "bf16", 1, 8, 2, 128, 16, [30, 100], seed=2)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
+    assert max_abs_err(out, oracle_decode(wl, pool, q, 0)) <= 2e-3
+    _check_status()
