@@ -70,20 +70,22 @@ int num_sms_current(int* out) {
     return PA_OK;
 }
 
-// Partition size heuristic: about 512 KiB of K+V per CTA (on GB300 the
-// large-batch workload runs fastest at 256-1024 KiB per CTA: fewer partials to
-// combine, fewer idle grid slots), shrunk (down to 16 KiB) while the grid would
-// hold fewer than four CTAs per SM.
+// Partition size heuristic: 64 blocks (at most 1 MiB of K+V) per CTA, shrunk
+// by halves (not below 32 KiB) while the grid would hold fewer than two CTAs
+// per SM.  Sweeps on GB300: 64 blocks is the fastest or within 1% of it for the
+// large-batch (B 16), long-context (B 32) and MHA workloads; the 6.7 MB-per-layer
+// mini-infer shape is fastest at 8 blocks, where the shrinking stops.
 int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sms) {
     const long long blk_bytes = 2LL * g.B * g.D * g.elt;
-    long long pb = (512LL * 1024) / blk_bytes;
+    long long pb = 64;
+    if (pb * blk_bytes > (1LL << 20)) pb = (1LL << 20) / blk_bytes;
     if (pb < 1) pb = 1;
     if (pb > maxb) pb = maxb;
     while (pb > 1) {
         const long long parts = (maxb + pb - 1) / pb;
-        if ((long long)batch * g.Hkv * parts >= 4LL * num_sms) break;
+        if ((long long)batch * g.Hkv * parts >= 2LL * num_sms) break;
         const long long half = pb / 2;
-        if (half * blk_bytes < 16 * 1024) break;
+        if (half * blk_bytes < 32 * 1024) break;
         pb = half;
     }
     return (int)pb;

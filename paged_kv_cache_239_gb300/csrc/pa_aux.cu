@@ -66,17 +66,28 @@ cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) {
-    const long long warps = (long long)p.batch * p.H;
-    if (warps <= 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((warps + 3) / 4);
-    if (D == 64)
-        pa_combine_kernel<64><<<grid, 128, 0, s>>>(p, B);
-    else if (D == 128)
-        pa_combine_kernel<128><<<grid, 128, 0, s>>>(p, B);
-    else
-        return cudaErrorNotSupported;
+template <int D>
+static cudaError_t launch_combine_d(const DecodeParams& p, int B, long long heads, cudaStream_t s) {
+    // warps per (sequence, head): enough to cover the partitions 4 at a time
+    const int W = p.Cmax >= 32 ? 8 : (p.Cmax >= 8 ? 4 : (p.Cmax >= 3 ? 2 : 1));
+    const long long hpc = 8 / W;
+    const long long grid = (heads + hpc - 1) / hpc;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    switch (W) {
+        case 8: pa_combine_kernel<D, 8><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
+        case 4: pa_combine_kernel<D, 4><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
+        case 2: pa_combine_kernel<D, 2><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
+        default: pa_combine_kernel<D, 1><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
+    }
     return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) {
+    const long long heads = (long long)p.batch * p.H;
+    if (heads <= 0) return cudaSuccess;
+    if (D == 64) return launch_combine_d<64>(p, B, heads, s);
+    if (D == 128) return launch_combine_d<128>(p, B, heads, s);
+    return cudaErrorNotSupported;
 }
 
 // ---------------------------------------------------------------------------

@@ -480,48 +480,97 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
 
 // Merges the partitions of every (sequence, query head) with more than one:
 //   M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c .
-// One warp per (sequence, head); lane owns D/32 consecutive elements.
-template <int D>
-__global__ void __launch_bounds__(128) pa_combine_kernel(const DecodeParams p, int B) {
+// W warps (1, 2, 4 or 8) serve one (sequence, head); a 256-thread CTA serves
+// 8 / W of them.  Warp w takes partitions w, w + W, ... four at a time (four
+// independent loads in flight per lane; a lane owns D/32 consecutive
+// elements), then the W partial sums are merged through shared memory.
+template <int D, int W>
+__global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, int B) {
     constexpr int PL = D / 32;
-    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+    constexpr int HPC = 8 / W;  // heads per CTA
+    __shared__ float s_acc[8][D];
+    __shared__ float s_l[8];
+    __shared__ float s_m[8];
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    if (gw >= p.batch * p.H) return;
-    const int b = gw / p.H;
-    int n = __ldg(p.lens + b);
-    if (n < 0 || n > p.maxb * B) n = 0;
-    const int nblk = (n + B - 1) / B;
-    const int nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
-    if (nparts <= 1) return;  // written directly by the decode kernel
-    const long long base = (long long)gw * p.Cmax;
+    const int hl = warp / W;    // head slot in this CTA
+    const int w = warp % W;     // warp within the head
+    const long long gh = (long long)blockIdx.x * HPC + hl;  // b * H + h
+    const bool live = gh < (long long)p.batch * p.H;
+    int nparts = 0;
+    if (live) {
+        const int b = (int)(gh / p.H);
+        int n = __ldg(p.lens + b);
+        if (n < 0 || n > p.maxb * B) n = 0;
+        const int nblk = (n + B - 1) / B;
+        nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
+    }
+    const long long base = gh * p.Cmax;
     const float* ml = p.part_ml + base * 2;
+    // running max over this head's partitions, per warp then across the W warps
     float M = -INFINITY;
-    for (int c = lane; c < nparts; c += 32) M = fmaxf(M, ml[2 * c]);
+    if (nparts > 1)
+        for (int c = w * 32 + lane; c < nparts; c += W * 32) M = fmaxf(M, __ldg(ml + 2 * c));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
-    float L = 0.f;
+    if (lane == 0) s_m[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < W; ++i) M = fmaxf(M, s_m[hl * W + i]);
+
     float acc[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) acc[i] = 0.f;
-    for (int c = 0; c < nparts; ++c) {
-        const float mc = ml[2 * c];
-        const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-        L += w * ml[2 * c + 1];
-        const float* oc = p.part_o + (base + c) * D + lane * PL;
-        if constexpr (PL == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(oc);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
-        } else {
+    float L = 0.f;
+    if (nparts > 1) {
+        for (int c0 = w; c0 < nparts; c0 += 4 * W) {
+            float wt[4], ov[4][PL];
 #pragma unroll
-            for (int i = 0; i < PL; ++i) acc[i] += w * oc[i];
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * W;
+                wt[u] = 0.f;
+#pragma unroll
+                for (int i = 0; i < PL; ++i) ov[u][i] = 0.f;
+                if (c < nparts) {
+                    const float mc = __ldg(ml + 2 * c);
+                    wt[u] = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+                    L += wt[u] * __ldg(ml + 2 * c + 1);
+                    const float* oc = p.part_o + (base + c) * D + lane * PL;
+                    if constexpr (PL == 4) {
+                        const float4 v = __ldg(reinterpret_cast<const float4*>(oc));
+                        ov[u][0] = v.x;
+                        ov[u][1] = v.y;
+                        ov[u][2] = v.z;
+                        ov[u][3] = v.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < PL; ++i) ov[u][i] = __ldg(oc + i);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < PL; ++i) acc[i] += wt[u] * ov[u][i];
         }
     }
-    float* o = p.out + (long long)gw * D + lane * PL;
 #pragma unroll
-    for (int i = 0; i < PL; ++i) o[i] = L > 0.f ? acc[i] / L : 0.f;
+    for (int i = 0; i < PL; ++i) s_acc[warp][lane * PL + i] = acc[i];
+    if (lane == 0) s_l[warp] = L;
+    __syncthreads();
+    if (nparts > 1 && w == 0) {
+        float Lt = 0.f;
+#pragma unroll
+        for (int i = 0; i < W; ++i) Lt += s_l[hl * W + i];
+        float* o = p.out + gh * D + lane * PL;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+            float a = 0.f;
+#pragma unroll
+            for (int k = 0; k < W; ++k) a += s_acc[hl * W + k][lane * PL + i];
+            o[i] = Lt > 0.f ? a / Lt : 0.f;
+        }
+    }
 }
 
 }  // namespace pa
