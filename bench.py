@@ -64,8 +64,8 @@ def decode_flops(wl) -> int:
 # pa_decode_mma_kernel (ncu --set full) + pa_combine_kernel (ncu dram metrics),
 # see profiles/; valid only for the kernel sources they were taken from.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231026000 + 6745856 + 9854464,
-    "sources_sha256": "f9f7c589f25a139ca9c91ba710653b5f4a46e8bac41ea64b2aa4b4855729d2f3",
+    "bytes_per_launch": 2230913000 + 6313728 + 9852032,
+    "sources_sha256": "734c0abbbff0ce316cd9ded39167217d2bf58cecee73e0b3015dadece5798438",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h"]

@@ -68,8 +68,10 @@ cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s) {
 
 template <int D>
 static cudaError_t launch_combine_d(const DecodeParams& p, int B, long long heads, cudaStream_t s) {
-    // warps per (sequence, head): enough to cover the partitions 4 at a time
-    const int W = p.Cmax >= 32 ? 8 : (p.Cmax >= 8 ? 4 : (p.Cmax >= 3 ? 2 : 1));
+    // warps per (sequence, head): one warp for up to 4 partials (one round of
+    // four loads), more as the partial count grows (ncu on GB300: with 4
+    // partials a single warp is faster than two; with 64-128, eight warps)
+    const int W = p.Cmax > 32 ? 8 : (p.Cmax > 8 ? 4 : (p.Cmax > 4 ? 2 : 1));
     const long long hpc = 8 / W;
     const long long grid = (heads + hpc - 1) / hpc;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
