@@ -128,7 +128,11 @@ PA_API int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, i
 /* Release the handle (not the caller's device tensor).  NULL is accepted. */
 PA_API int pa_pool_destroy(pa_pool* pool);
 
-/* Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
+/* Built shapes: head_dim 64 or 128, block_size 16 or 32; GQA group
+ * (num_heads / num_kv_heads) 1-8 on the tensor-core kernel (bf16 pools), 1, 2,
+ * 4 or 8 on the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
+ *
+ * Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
  * the tensor-core kernel for bf16 pools (mma.sync, K/V staged by tensor-map
  * TMA), the CUDA-core kernel for fp32 pools.  PA_DECODE_CUDA_CORES forces the
  * CUDA-core kernel (fp32 FMA on every dtype); PA_DECODE_TENSOR_CORES makes

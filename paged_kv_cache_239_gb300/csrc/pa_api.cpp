@@ -127,10 +127,12 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
     if (partition_blocks < 0)
         return fail(PA_ERR_INVALID_ARG, "partition_blocks %d < 0", partition_blocks);
     const int G = num_heads / pool->g.Hkv;
-    if (!pa::decode_supported(pool->g.dtype, pool->g.D, pool->g.B, G))
+    if (!pa::decode_supported(pool->g.dtype, pool->g.D, pool->g.B, G) &&
+        !(pool->g.dtype == 1 && pa::decode_mma_supported(pool->g.D, pool->g.B, G)))
         return fail(PA_ERR_UNSUPPORTED,
                     "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
-                    "(built: head_dim 64/128, block_size 16/32, group 1/2/4/8)",
+                    "(built: head_dim 64/128, block_size 16/32; group 1-8 for bf16 pools, "
+                    "1/2/4/8 for fp32 pools)",
                     pool->g.dtype, pool->g.D, pool->g.B, G);
     int pb = partition_blocks;
     if (pb == 0) {
@@ -576,6 +578,9 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     const bool mma_ok = g.dtype == 1 && pa::decode_mma_supported(g.D, g.B, sh.G);
     if (pool->decode_kernel == PA_DECODE_TENSOR_CORES && !mma_ok)
         return fail(PA_ERR_UNSUPPORTED, "no tensor-core decode kernel for this pool / group size");
+    if (!pa::decode_supported(g.dtype, g.D, g.B, sh.G) &&
+        (!mma_ok || pool->decode_kernel == PA_DECODE_CUDA_CORES))
+        return fail(PA_ERR_UNSUPPORTED, "no CUDA-core decode kernel for group size %d", sh.G);
     if (mma_ok && pool->decode_kernel != PA_DECODE_CUDA_CORES) {
         {
             std::lock_guard<std::mutex> lock(pool->mu);

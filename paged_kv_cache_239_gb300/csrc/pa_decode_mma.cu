@@ -46,7 +46,11 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaSt
     switch (G) {
         case 1: return launch_inst<D, B, 1>(p, tm, s);
         case 2: return launch_inst<D, B, 2>(p, tm, s);
+        case 3: return launch_inst<D, B, 3>(p, tm, s);
         case 4: return launch_inst<D, B, 4>(p, tm, s);
+        case 5: return launch_inst<D, B, 5>(p, tm, s);
+        case 6: return launch_inst<D, B, 6>(p, tm, s);
+        case 7: return launch_inst<D, B, 7>(p, tm, s);
         case 8: return launch_inst<D, B, 8>(p, tm, s);
         default: return cudaErrorNotSupported;
     }
@@ -71,7 +75,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool decode_mma_supported(int D, int B, int G) {
     if (D != 64 && D != 128) return false;
     if (B != 16 && B != 32) return false;
-    return G == 1 || G == 2 || G == 4 || G == 8;
+    return G >= 1 && G <= 8;  // heads past G in the 8-wide mma tile are masked
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, int B, int G,

@@ -1,0 +1,117 @@
+"""Seeded randomized parity sweep on the GPU: random shapes (dtype, head_dim,
+block size, GQA group 1-8, KV heads, batch, ragged lengths with 0 / 1 / block
+multiples), random layer, partition size, pool layout and decode kernel, plus
+the fused append path -- each case against the oracle on the same inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_239_gb300 import binding as B
+from paged_kv_cache_239_gb300 import workloads as W
+from gpu_helpers import TOL, max_abs_err
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 48
+
+
+def _case(i):
+    rng = np.random.default_rng(1000 + i)
+    dtype = "f32" if rng.random() < 0.25 else "bf16"
+    D = int(rng.choice([64, 128]))
+    Bs = int(rng.choice([16, 32]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    G = int(rng.choice([1, 2, 4, 8])) if dtype == "f32" else int(rng.integers(1, 9))
+    L = int(rng.integers(1, 4))
+    batch = int(rng.integers(1, 10))
+    special = [0, 1, Bs - 1, Bs, Bs + 1, 2 * Bs]
+    lens = [int(rng.choice(special)) if rng.random() < 0.4 else int(rng.integers(0, 20 * Bs))
+            for _ in range(batch)]
+    layout = str(rng.choice(["fused", "separate", "layer_major"]))
+    if layout == "separate":
+        L = 1
+    return rng, dtype, D, Bs, Hkv, G, L, lens, layout
+
+
+def _make_pool_handle(wl, fused, layout, dev):
+    """Device tensors holding the fused pool's rows in `layout`, and a handle."""
+    tile = wl.block_size * wl.head_dim
+    if layout == "fused":
+        t = fused.to(dev)
+        return (t,), B.pa_pool_create(t, wl.num_blocks, wl.num_layers, wl.num_kv_heads,
+                                      wl.block_size, wl.head_dim, t.dtype)
+    if layout == "separate":
+        kc, vc = fused[:, 0, 0].contiguous().to(dev), fused[:, 1, 0].contiguous().to(dev)
+        sb, sl = wl.num_kv_heads * tile, 0
+    else:
+        kc = fused[:, 0].permute(1, 0, 2, 3, 4).contiguous().to(dev)
+        vc = fused[:, 1].permute(1, 0, 2, 3, 4).contiguous().to(dev)
+        sb, sl = wl.num_kv_heads * tile, wl.num_blocks * wl.num_kv_heads * tile
+    h = B.pa_pool_create_strided(kc, vc, sb, sl, tile, wl.num_blocks, wl.num_layers,
+                                 wl.num_kv_heads, wl.block_size, wl.head_dim, kc.dtype)
+    return (kc, vc), h
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_case_matches_oracle(cuda_device, i):
+    rng, dtype, D, Bs, Hkv, G, L, lens, layout = _case(i)
+    H = Hkv * G
+    wl = W.custom(f"rnd{i}", dtype, L, H, Hkv, D, Bs, lens, seed=2000 + i,
+                  spare_blocks=int(rng.integers(0, 5)), interleave=bool(rng.random() < 0.5),
+                  steps=1)
+    fused = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    keep, h = _make_pool_handle(wl, fused, layout, cuda_device)
+    try:
+        kinds = [B.PA_DECODE_AUTO]
+        if dtype == "bf16" and G in (1, 2, 4, 8):
+            kinds.append(B.PA_DECODE_CUDA_CORES)
+        layer = int(rng.integers(0, L))
+        pb = int(rng.choice([0, 1, 2, 3, wl.max_blocks]))
+        bt = torch.from_numpy(wl.block_tables).to(cuda_device)
+        ln = torch.from_numpy(wl.context_lens).to(cuda_device)
+        qd = q.to(cuda_device)
+        ref = oracle.decode_attention(W.as_oracle_array(q), W.as_oracle_array(fused), layer,
+                                      wl.block_tables, wl.context_lens, H, wl.scale)
+        need = B.pa_decode_workspace_size(h, wl.batch, H, wl.max_blocks, pb)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=cuda_device)
+        for kind in kinds:
+            B.pa_pool_set_decode_kernel(h, kind)
+            out = torch.full((wl.batch, H, D), float("nan"), device=cuda_device)
+            B.pa_decode_attention_partitioned(out, qd, h, layer, bt, wl.max_blocks, ln, wl.batch,
+                                              Bs, H, Hkv, D, wl.scale, pb, ws, need)
+            torch.cuda.synchronize()
+            err = max_abs_err(out, ref)
+            assert err <= TOL[dtype], (i, kind, dtype, D, Bs, Hkv, G, layout, pb, err)
+        if dtype == "bf16" and G not in (1, 2, 4, 8):
+            B.pa_pool_set_decode_kernel(h, B.PA_DECODE_CUDA_CORES)
+            with pytest.raises(B.PagedAttnError) as e:
+                B.pa_decode_attention_partitioned(out, qd, h, layer, bt, wl.max_blocks, ln,
+                                                  wl.batch, Bs, H, Hkv, D, wl.scale, pb, ws, need)
+            assert e.value.code == B.PA_ERR_UNSUPPORTED
+        B.pa_pool_set_decode_kernel(h, B.PA_DECODE_AUTO)
+
+        # fused append at position n (a new block where n % B == 0), decode over n + 1
+        k, v = W.make_new_tokens(wl, 1)
+        tables = wl.block_tables.copy()
+        for b, n in enumerate(wl.context_lens):
+            if n % Bs == 0:
+                tables[b, n // Bs] = wl.free_stack.pop()
+        btn = torch.from_numpy(tables).to(cuda_device)
+        pos = torch.from_numpy(wl.context_lens.copy()).to(cuda_device)
+        lens1 = wl.context_lens + 1
+        out = torch.full((wl.batch, H, D), float("nan"), device=cuda_device)
+        B.pa_write_kv_and_decode(out, qd, h, layer, k[0].to(cuda_device), v[0].to(cuda_device),
+                                 pos, btn, wl.max_blocks, torch.from_numpy(lens1).to(cuda_device),
+                                 wl.batch, Bs, H, Hkv, D, wl.scale, pb, ws, need)
+        host = W.as_oracle_array(fused).copy()
+        oracle.write_kv(host, layer, W.as_oracle_array(k[0]), W.as_oracle_array(v[0]), tables,
+                        wl.context_lens)
+        ref1 = oracle.decode_attention(W.as_oracle_array(q), host, layer, tables, lens1, H,
+                                       wl.scale)
+        torch.cuda.synchronize()
+        assert max_abs_err(out, ref1) <= TOL[dtype], (i, "fused")
+        assert B.pa_get_status() == 0
+    finally:
+        B.pa_pool_destroy(h)
