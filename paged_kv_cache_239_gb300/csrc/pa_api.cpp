@@ -70,24 +70,27 @@ int num_sms_current(int* out) {
     return PA_OK;
 }
 
-// Partition size heuristic: 64 blocks (at most 1 MiB of K+V) per CTA, shrunk
-// by halves (not below 32 KiB) while the grid would hold fewer than two CTAs
-// per SM.  Sweeps on GB300: 64 blocks is the fastest or within 1% of it for the
-// large-batch (B 16), long-context (B 32) and MHA workloads; the 6.7 MB-per-layer
-// mini-infer shape is fastest at 8 blocks, where the shrinking stops.
+// Partition size heuristic.  The host does not see the lengths, so the batch's
+// K+V is estimated from the table capacity (half full on average) and split so
+// that about 12 partitions fall on each SM: enough CTAs of similar size that
+// ragged lengths even out.  Bounds: at most 64 blocks and 1 MiB per CTA (more
+// only adds partials and idle tail), at least 32 KiB (less is all ramp-up).
+// The pick is rounded down to a multiple of 8 blocks (two per warp of a CTA).
+// GB300 sweeps: large-batch 64 blocks (fastest; picks 64), long-context 32
+// (fastest; the unrounded 35 was 2.5% slower; picks 32), MHA batch 64 12-16
+// (picks 16), mini-infer shape 4-8 (picks 8).
 int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sms) {
     const long long blk_bytes = 2LL * g.B * g.D * g.elt;
-    long long pb = 64;
-    if (pb * blk_bytes > (1LL << 20)) pb = (1LL << 20) / blk_bytes;
-    if (pb < 1) pb = 1;
+    const long long est_total = (long long)batch * g.Hkv * maxb * blk_bytes / 2;
+    long long pb = est_total / ((long long)num_sms * 12 * blk_bytes);
+    long long hi = 64;
+    if (hi * blk_bytes > (1LL << 20)) hi = (1LL << 20) / blk_bytes;
+    const long long lo = (32 * 1024 + blk_bytes - 1) / blk_bytes;
+    if (pb > hi) pb = hi;
+    if (pb < lo) pb = lo;
+    if (pb > 8) pb -= pb % 8;
     if (pb > maxb) pb = maxb;
-    while (pb > 1) {
-        const long long parts = (maxb + pb - 1) / pb;
-        if ((long long)batch * g.Hkv * parts >= 2LL * num_sms) break;
-        const long long half = pb / 2;
-        if (half * blk_bytes < 32 * 1024) break;
-        pb = half;
-    }
+    if (pb < 1) pb = 1;
     return (int)pb;
 }
 
@@ -131,7 +134,7 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         !(pool->g.dtype == 1 && pa::decode_mma_supported(pool->g.D, pool->g.B, G)))
         return fail(PA_ERR_UNSUPPORTED,
                     "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
-                    "(built: head_dim 64/128, block_size 16/32; group 1-8 for bf16 pools, "
+                    "(built: head_dim 64/128, block_size 16/32; group 1-8 or 16 for bf16 pools, "
                     "1/2/4/8 for fp32 pools)",
                     pool->g.dtype, pool->g.D, pool->g.B, G);
     int pb = partition_blocks;

@@ -52,6 +52,7 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaSt
         case 6: return launch_inst<D, B, 6>(p, tm, s);
         case 7: return launch_inst<D, B, 7>(p, tm, s);
         case 8: return launch_inst<D, B, 8>(p, tm, s);
+        case 16: return launch_inst<D, B, 16>(p, tm, s);
         default: return cudaErrorNotSupported;
     }
 }
@@ -75,7 +76,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool decode_mma_supported(int D, int B, int G) {
     if (D != 64 && D != 128) return false;
     if (B != 16 && B != 32) return false;
-    return G >= 1 && G <= 8;  // heads past G in the 8-wide mma tile are masked
+    // heads past G in the 8-wide mma tiles are masked
+    return (G >= 1 && G <= 8) || G == 16;
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, int B, int G,

@@ -13,8 +13,9 @@
 // to cut the instruction count per token (the CUDA-core kernel is issue-bound):
 //  * a stage holds 16 rows of K and 16 rows of V, each as D/64 TMA boxes of
 //    16 x 64 bf16 with SWIZZLE_128B, so ldmatrix reads are bank-conflict free;
-//  * S = K Q^T on mma.sync: M = 16 tokens, N = 8 query heads of the group
-//    (heads >= G are zero), K = head_dim; the scale is applied to S in fp32;
+//  * S = K Q^T on mma.sync: M = 16 tokens, N = 8 query heads of the group per
+//    tile (one tile for G <= 8, two for G <= 16; heads >= G are zero),
+//    K = head_dim; the scale is applied to S in fp32;
 //  * online softmax on the S fragments (a lane holds 2 tokens x 2 heads);
 //  * P is split into bf16 hi + lo parts (|P - hi - lo| <= 2^-16 P), transposed
 //    in registers with movmatrix, and O^T = V^T P accumulates on mma.sync with
@@ -43,13 +44,14 @@ struct MmaCfg {
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile, then V tile
     static constexpr int KS = D / 16;              // k-steps of S = K Q^T
     static constexpr int MT = D / 16;              // m-tiles of O^T = V^T P
+    static constexpr int NT = (G + 7) / 8;         // 8-head mma tiles of the group
     static constexpr int WARP_STAGE_BYTES = S * STAGE_BYTES;
     static constexpr int META_BYTES = 64;          // per warp: nvalid[S], mbarriers[S]
     static constexpr int SMEM_BYTES = NW * WARP_STAGE_BYTES + NW * META_BYTES + 1024;
 
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
     static_assert(B % R == 0, "block size must be a multiple of 16");
-    static_assert(G >= 1 && G <= 8, "GQA group of at most 8 query heads");
+    static_assert(G >= 1 && G <= 16, "GQA group of at most 16 query heads");
     static_assert(S * 12 <= META_BYTES, "meta");
     static_assert((2 * G + G * D) * 4 <= WARP_STAGE_BYTES, "merge area must fit in the stages");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -192,32 +194,45 @@ __global__ void __launch_bounds__(NW * 32)
         }
     };
 
-    // q of the group as mma B fragments: b0 = q[g][16ks+2cq..+1], b1 = q[g][16ks+8+2cq..+1]
-    uint32_t qb[C::KS][2];
-    {
+    // q of the group as mma B fragments, one set per 8-head tile nt:
+    // b0 = q[8nt+g][16ks+2cq..+1], b1 = q[8nt+g][16ks+8+2cq..+1] (zero past the group)
+    uint32_t qb[C::NT][C::KS][2];
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) {
+        const int hq = 8 * nt + g;
         const unsigned short* qrow =
-            reinterpret_cast<const unsigned short*>(p.q) + ((long long)b * p.H + kvh * G + g) * D;
+            reinterpret_cast<const unsigned short*>(p.q) + ((long long)b * p.H + kvh * G + hq) * D;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
-            if (g < G) {
-                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * cq);
-                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * cq);
+            if (hq < G) {
+                qb[nt][ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * cq);
+                qb[nt][ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * cq);
             } else {
-                qb[ks][0] = 0u;
-                qb[ks][1] = 0u;
+                qb[nt][ks][0] = 0u;
+                qb[nt][ks][1] = 0u;
             }
         }
     }
 
-    float o[C::MT][4];
+    float o[C::NT][C::MT][4];
 #pragma unroll
-    for (int mt = 0; mt < C::MT; ++mt)
+    for (int nt = 0; nt < C::NT; ++nt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) o[mt][i] = 0.f;
-    // running max / sum of heads 2cq and 2cq+1 (the sum is this lane's share)
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const bool h0_ok = 2 * cq < G;
-    const bool h1_ok = 2 * cq + 1 < G;
+        for (int mt = 0; mt < C::MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[nt][mt][i] = 0.f;
+    // running max / sum of heads 8nt+2cq and 8nt+2cq+1 (the sum is this lane's share)
+    float m0[C::NT], m1[C::NT], l0[C::NT], l1[C::NT];
+    bool h0_ok[C::NT], h1_ok[C::NT];
+#pragma unroll
+    for (int nt = 0; nt < C::NT; ++nt) {
+        m0[nt] = -INFINITY;
+        m1[nt] = -INFINITY;
+        l0[nt] = 0.f;
+        l1[nt] = 0.f;
+        h0_ok[nt] = 8 * nt + 2 * cq < G;
+        h1_ok[nt] = 8 * nt + 2 * cq + 1 < G;
+    }
 
     int u_issue = 0;
     const int npro = U < S ? U : S;
@@ -247,8 +262,12 @@ __global__ void __launch_bounds__(NW * 32)
                 __syncwarp();
             }
 
-            // ---- S = K Q^T (16 tokens x 8 heads) ----
-            float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+            // ---- S = K Q^T (16 tokens x 8 heads per tile) ----
+            float sacc[C::NT][4];
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
             {
                 const int mtx = lane >> 3;
                 const int t = (lane & 7) + 8 * (mtx & 1);
@@ -256,54 +275,62 @@ __global__ void __launch_bounds__(NW * 32)
                 for (int ks = 0; ks < C::KS; ++ks) {
                     uint32_t a0, a1, a2, a3;
                     ldmatrix_x4(ktile + swz_offset(t, 2 * ks + (mtx >> 1)), a0, a1, a2, a3);
-                    mma_bf16_16816(sacc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+#pragma unroll
+                    for (int nt = 0; nt < C::NT; ++nt)
+                        mma_bf16_16816(sacc[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
                 }
             }
-            // ---- online softmax: lane has tokens g, g+8 x heads 2cq, 2cq+1 ----
+            // ---- online softmax: lane has tokens g, g+8 x heads 8nt+2cq, 8nt+2cq+1 ----
             const bool t0_ok = g < rows;
             const bool t1_ok = g + 8 < rows;
-            float s00 = (t0_ok && h0_ok) ? sacc[0] * p.qscale : -INFINITY;
-            float s01 = (t0_ok && h1_ok) ? sacc[1] * p.qscale : -INFINITY;
-            float s10 = (t1_ok && h0_ok) ? sacc[2] * p.qscale : -INFINITY;
-            float s11 = (t1_ok && h1_ok) ? sacc[3] * p.qscale : -INFINITY;
-            float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
+            uint32_t bh0[C::NT], bh1[C::NT], bl0[C::NT], bl1[C::NT];
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            // (heads past the group keep O = 0, so their factor is left at 1)
-            const float a0s = !h0_ok ? 1.f : (m0 == -INFINITY ? 0.f : exp2f(m0 - mn0));
-            const float a1s = !h1_ok ? 1.f : (m1 == -INFINITY ? 0.f : exp2f(m1 - mn1));
-            const float p00 = (s00 == -INFINITY) ? 0.f : exp2f(s00 - mn0);
-            const float p01 = (s01 == -INFINITY) ? 0.f : exp2f(s01 - mn1);
-            const float p10 = (s10 == -INFINITY) ? 0.f : exp2f(s10 - mn0);
-            const float p11 = (s11 == -INFINITY) ? 0.f : exp2f(s11 - mn1);
-            l0 = l0 * a0s + p00 + p10;
-            l1 = l1 * a1s + p01 + p11;
-            m0 = mn0;
-            m1 = mn1;
-            if (a0s != 1.f || a1s != 1.f) {
+            for (int nt = 0; nt < C::NT; ++nt) {
+                const float s00 = (t0_ok && h0_ok[nt]) ? sacc[nt][0] * p.qscale : -INFINITY;
+                const float s01 = (t0_ok && h1_ok[nt]) ? sacc[nt][1] * p.qscale : -INFINITY;
+                const float s10 = (t1_ok && h0_ok[nt]) ? sacc[nt][2] * p.qscale : -INFINITY;
+                const float s11 = (t1_ok && h1_ok[nt]) ? sacc[nt][3] * p.qscale : -INFINITY;
+                float mx0 = fmaxf(s00, s10), mx1 = fmaxf(s01, s11);
 #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                    o[mt][0] *= a0s;
-                    o[mt][1] *= a1s;
-                    o[mt][2] *= a0s;
-                    o[mt][3] *= a1s;
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
                 }
+                const float mn0 = fmaxf(m0[nt], mx0), mn1 = fmaxf(m1[nt], mx1);
+                // (heads past the group keep O = 0, so their factor is left at 1)
+                const float a0s =
+                    !h0_ok[nt] ? 1.f : (m0[nt] == -INFINITY ? 0.f : exp2f(m0[nt] - mn0));
+                const float a1s =
+                    !h1_ok[nt] ? 1.f : (m1[nt] == -INFINITY ? 0.f : exp2f(m1[nt] - mn1));
+                const float p00 = (s00 == -INFINITY) ? 0.f : exp2f(s00 - mn0);
+                const float p01 = (s01 == -INFINITY) ? 0.f : exp2f(s01 - mn1);
+                const float p10 = (s10 == -INFINITY) ? 0.f : exp2f(s10 - mn0);
+                const float p11 = (s11 == -INFINITY) ? 0.f : exp2f(s11 - mn1);
+                l0[nt] = l0[nt] * a0s + p00 + p10;
+                l1[nt] = l1[nt] * a1s + p01 + p11;
+                m0[nt] = mn0;
+                m1[nt] = mn1;
+                if (a0s != 1.f || a1s != 1.f) {
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt) {
+                        o[nt][mt][0] *= a0s;
+                        o[nt][mt][1] *= a1s;
+                        o[nt][mt][2] *= a0s;
+                        o[nt][mt][3] *= a1s;
+                    }
+                }
+                // ---- P -> bf16 hi + lo, transposed into mma B fragments ----
+                const __nv_bfloat162 hi_t = __floats2bfloat162_rn(p00, p01);
+                const __nv_bfloat162 hi_b = __floats2bfloat162_rn(p10, p11);
+                const __nv_bfloat162 lo_t = __floats2bfloat162_rn(p00 - __low2float(hi_t),
+                                                                  p01 - __high2float(hi_t));
+                const __nv_bfloat162 lo_b = __floats2bfloat162_rn(p10 - __low2float(hi_b),
+                                                                  p11 - __high2float(hi_b));
+                bh0[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&hi_t));
+                bh1[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&hi_b));
+                bl0[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&lo_t));
+                bl1[nt] = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&lo_b));
             }
-            // ---- P -> bf16 hi + lo, transposed into mma B fragments ----
-            const __nv_bfloat162 hi_t = __floats2bfloat162_rn(p00, p01);
-            const __nv_bfloat162 hi_b = __floats2bfloat162_rn(p10, p11);
-            const __nv_bfloat162 lo_t = __floats2bfloat162_rn(p00 - __low2float(hi_t),
-                                                              p01 - __high2float(hi_t));
-            const __nv_bfloat162 lo_b = __floats2bfloat162_rn(p10 - __low2float(hi_b),
-                                                              p11 - __high2float(hi_b));
-            const uint32_t bh0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&hi_t));
-            const uint32_t bh1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&hi_b));
-            const uint32_t bl0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&lo_t));
-            const uint32_t bl1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&lo_b));
             // ---- O^T += V^T P ----
             {
                 const int mtx = lane >> 3;
@@ -312,8 +339,11 @@ __global__ void __launch_bounds__(NW * 32)
                 for (int mt = 0; mt < C::MT; ++mt) {
                     uint32_t v0, v1, v2, v3;
                     ldmatrix_x4_trans(vtile + swz_offset(t, 2 * mt + (mtx & 1)), v0, v1, v2, v3);
-                    mma_bf16_16816(o[mt], v0, v1, v2, v3, bh0, bh1);
-                    mma_bf16_16816(o[mt], v0, v1, v2, v3, bl0, bl1);
+#pragma unroll
+                    for (int nt = 0; nt < C::NT; ++nt) {
+                        mma_bf16_16816(o[nt][mt], v0, v1, v2, v3, bh0[nt], bh1[nt]);
+                        mma_bf16_16816(o[nt][mt], v0, v1, v2, v3, bl0[nt], bl1[nt]);
+                    }
                 }
             }
         }
@@ -331,34 +361,40 @@ __global__ void __launch_bounds__(NW * 32)
 
     // ---- warp totals: l over the 8 lanes sharing cq ----
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(kFullMask, l0, off);
-        l1 += __shfl_xor_sync(kFullMask, l1, off);
-    }
+    for (int nt = 0; nt < C::NT; ++nt)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0[nt] += __shfl_xor_sync(kFullMask, l0[nt], off);
+            l1[nt] += __shfl_xor_sync(kFullMask, l1[nt], off);
+        }
     __syncwarp();
     float* w_m = reinterpret_cast<float*>(wbase);
     float* w_l = w_m + G;
     float* w_acc = w_l + G;  // [G][D]
-    if (g == 0) {
-        if (h0_ok) {
-            w_m[2 * cq] = m0;
-            w_l[2 * cq] = l0;
-        }
-        if (h1_ok) {
-            w_m[2 * cq + 1] = m1;
-            w_l[2 * cq + 1] = l1;
-        }
-    }
 #pragma unroll
-    for (int mt = 0; mt < C::MT; ++mt) {
-        const int d = 16 * mt + g;
-        if (h0_ok) {
-            w_acc[(2 * cq) * D + d] = o[mt][0];
-            w_acc[(2 * cq) * D + d + 8] = o[mt][2];
+    for (int nt = 0; nt < C::NT; ++nt) {
+        const int h0 = 8 * nt + 2 * cq;
+        if (g == 0) {
+            if (h0_ok[nt]) {
+                w_m[h0] = m0[nt];
+                w_l[h0] = l0[nt];
+            }
+            if (h1_ok[nt]) {
+                w_m[h0 + 1] = m1[nt];
+                w_l[h0 + 1] = l1[nt];
+            }
         }
-        if (h1_ok) {
-            w_acc[(2 * cq + 1) * D + d] = o[mt][1];
-            w_acc[(2 * cq + 1) * D + d + 8] = o[mt][3];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            const int d = 16 * mt + g;
+            if (h0_ok[nt]) {
+                w_acc[h0 * D + d] = o[nt][mt][0];
+                w_acc[h0 * D + d + 8] = o[nt][mt][2];
+            }
+            if (h1_ok[nt]) {
+                w_acc[(h0 + 1) * D + d] = o[nt][mt][1];
+                w_acc[(h0 + 1) * D + d + 8] = o[nt][mt][3];
+            }
         }
     }
     __syncthreads();

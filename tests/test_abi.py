@@ -133,7 +133,7 @@ def test_decode_host_checks(pa_lib):
 
         for bad, code in [(dict(layer=2), 1), (dict(B=32), 1), (dict(Hkv=1), 1), (dict(D=128), 1),
                           (dict(H=5), 1), (dict(maxb=0), 1), (dict(pb=-1), 1),
-                          (dict(scale=float("nan")), 1), (dict(H=18), 5), (dict(H=32), 5),
+                          (dict(scale=float("nan")), 1), (dict(H=18), 5), (dict(H=34), 5),
                           (dict(ws=None, wsb=0), 6), (dict(ws=F + 64, wsb=1 << 30), 6),
                           (dict(ws=F, wsb=16), 6)]:
             with pytest.raises(pa_lib.PagedAttnError) as e:

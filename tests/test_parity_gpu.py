@@ -407,3 +407,24 @@ def test_bounded_wait_times_out_into_status(cuda_device):
     out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
     assert max_abs_err(out, oracle_decode(wl, pool, q, 0)) <= 2e-3
     _check_status()
+
+
+@pytest.mark.parametrize("D,Bs", [(128, 16), (64, 32)])
+def test_group_of_16_on_tensor_cores(cuda_device, D, Bs):
+    """128 query heads over 8 KV heads style grouping (G = 16): two 8-head mma
+    tiles per KV head; the CUDA-core kernel refuses it."""
+    wl = W.custom("g16", "bf16", 2, 32, 2, D, Bs, [1, Bs, 5 * Bs + 3, 700, 0], seed=16,
+                  spare_blocks=3, interleave=True)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    ref = oracle_decode(wl, pool, q, 1)
+    for pb in (0, 1, 3, wl.max_blocks):
+        out = gpu_decode(gp, q.to(cuda_device), 1, bt, ln, partition_blocks=pb)
+        assert max_abs_err(out, ref) <= 2e-3, pb
+    B.pa_pool_set_decode_kernel(gp.h, B.PA_DECODE_CUDA_CORES)
+    with pytest.raises(B.PagedAttnError) as e:
+        gpu_decode(gp, q.to(cuda_device), 1, bt, ln)
+    assert e.value.code == B.PA_ERR_UNSUPPORTED
+    _check_status()
