@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -50,6 +51,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& tot
 __global__ void __launch_bounds__(kScanThreads)
 pa_device_alloc_kernel(int* stack, int* bt, int maxb, const int* positions, int batch, int B,
                        unsigned* status) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int s_warp[32];
     __shared__ int s_height;
     if (threadIdx.x == 0) s_height = stack[0];
@@ -86,6 +89,8 @@ pa_device_alloc_kernel(int* stack, int* bt, int maxb, const int* positions, int 
 __global__ void __launch_bounds__(kScanThreads)
 pa_device_free_kernel(int* stack, int* bt, int maxb, const int* lens, const uint8_t* finished,
                       int batch, int B, long long num_blocks, unsigned* status) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int s_warp[32];
     __shared__ int s_height;
     if (threadIdx.x == 0) s_height = stack[0];
@@ -139,18 +144,16 @@ pa_device_free_kernel(int* stack, int* bt, int maxb, const int* lens, const uint
 cudaError_t launch_device_alloc(int* stack, int* bt, int maxb, const int* positions, int batch,
                                 int B, unsigned* status, cudaStream_t s) {
     if (batch <= 0) return cudaSuccess;
-    pa_device_alloc_kernel<<<1, kScanThreads, 0, s>>>(stack, bt, maxb, positions, batch, B,
-                                                      status);
-    return cudaGetLastError();
+    return launch_pdl(pa_device_alloc_kernel, dim3(1), dim3(kScanThreads), 0, s, stack, bt, maxb,
+                      positions, batch, B, status);
 }
 
 cudaError_t launch_device_free(int* stack, int* bt, int maxb, const int* lens,
                                const uint8_t* finished, int batch, int B, long long num_blocks,
                                unsigned* status, cudaStream_t s) {
     if (batch <= 0) return cudaSuccess;
-    pa_device_free_kernel<<<1, kScanThreads, 0, s>>>(stack, bt, maxb, lens, finished, batch, B,
-                                                     num_blocks, status);
-    return cudaGetLastError();
+    return launch_pdl(pa_device_free_kernel, dim3(1), dim3(kScanThreads), 0, s, stack, bt, maxb,
+                      lens, finished, batch, B, num_blocks, status);
 }
 
 }  // namespace pa

@@ -75,13 +75,14 @@ static cudaError_t launch_combine_d(const DecodeParams& p, int B, long long head
     const long long hpc = 8 / W;
     const long long grid = (heads + hpc - 1) / hpc;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    cudaError_t e;
     switch (W) {
-        case 8: pa_combine_kernel<D, 8><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
-        case 4: pa_combine_kernel<D, 4><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
-        case 2: pa_combine_kernel<D, 2><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
-        default: pa_combine_kernel<D, 1><<<(unsigned)grid, 256, 0, s>>>(p, B); break;
+        case 8: e = launch_pdl(pa_combine_kernel<D, 8>, dim3((unsigned)grid), dim3(256), 0, s, p, B); break;
+        case 4: e = launch_pdl(pa_combine_kernel<D, 4>, dim3((unsigned)grid), dim3(256), 0, s, p, B); break;
+        case 2: e = launch_pdl(pa_combine_kernel<D, 2>, dim3((unsigned)grid), dim3(256), 0, s, p, B); break;
+        default: e = launch_pdl(pa_combine_kernel<D, 1>, dim3((unsigned)grid), dim3(256), 0, s, p, B); break;
     }
-    return cudaGetLastError();
+    return e;
 }
 
 cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) {
@@ -98,6 +99,8 @@ cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) 
 // k/v and the write into the pool row are coalesced.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pa_write_kv_kernel(const WriteParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int cpr = p.row_bytes / 16;
     const long long total = (long long)p.batch * 2 * p.Hkv * cpr;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -135,8 +138,7 @@ cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s) {
     long long blocks = (total + 255) / 256;
     const long long cap = (long long)num_sms * 8;
     if (blocks > cap) blocks = cap;
-    pa_write_kv_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(pa_write_kv_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -145,6 +147,8 @@ cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s) {
 // One thread per 16-byte chunk of every output row (K and V).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) pa_gather_kv_kernel(const GatherParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int cpr = p.row_bytes / 16;
     const long long total = (long long)p.batch * p.max_len * p.Hkv * 2 * cpr;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -192,6 +196,8 @@ __global__ void __launch_bounds__(256) pa_gather_kv_kernel(const GatherParams p)
 // are written as zeros; the mask rows of the block are written once.
 template <int CPR>
 __global__ void __launch_bounds__(256) pa_gather_kv_tiled(const GatherParams p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int RPP = 256 / CPR;  // rows per pass
     const int j = blockIdx.x;
     const int b = blockIdx.y;
@@ -251,19 +257,14 @@ cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s)
     const int cpr = p.row_bytes / 16;
     if (p.batch <= 65535 && nj <= 0x7fffffffLL && p.B <= 256 && (cpr == 8 || cpr == 16 || cpr == 32)) {
         const dim3 grid((unsigned)nj, (unsigned)p.batch);
-        if (cpr == 8)
-            pa_gather_kv_tiled<8><<<grid, 256, 0, s>>>(p);
-        else if (cpr == 16)
-            pa_gather_kv_tiled<16><<<grid, 256, 0, s>>>(p);
-        else
-            pa_gather_kv_tiled<32><<<grid, 256, 0, s>>>(p);
-        return cudaGetLastError();
+        if (cpr == 8) return launch_pdl(pa_gather_kv_tiled<8>, grid, dim3(256), 0, s, p);
+        if (cpr == 16) return launch_pdl(pa_gather_kv_tiled<16>, grid, dim3(256), 0, s, p);
+        return launch_pdl(pa_gather_kv_tiled<32>, grid, dim3(256), 0, s, p);
     }
     long long blocks = (total + 255) / 256;
     const long long cap = (long long)num_sms * 16;
     if (blocks > cap) blocks = cap;
-    pa_gather_kv_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(pa_gather_kv_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p);
 }
 
 }  // namespace pa

@@ -151,6 +151,8 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[P], int lane) {
 
 template <typename T, int D, int B, int G, int NW, int S>
 __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p) {
+    pdl_trigger();
+    pdl_wait();
     using C = DecodeCfg<T, D, B, G, NW, S>;
     constexpr int E2 = C::E / 2;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -486,6 +488,8 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
 // elements), then the W partial sums are merged through shared memory.
 template <int D, int W>
 __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, int B) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int PL = D / 32;
     constexpr int HPC = 8 / W;  // heads per CTA
     __shared__ float s_acc[8][D];

@@ -46,8 +46,8 @@ cudaError_t launch_decode_inst(const DecodeParams& p, cudaStream_t stream) {
     const long long grid = (long long)p.batch * p.Hkv * p.Cmax;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, kDecodeWarps * 32, C::SMEM_BYTES, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kDecodeWarps * 32), C::SMEM_BYTES, stream,
+                      p);
 }
 
 template <typename T, int D, int B>

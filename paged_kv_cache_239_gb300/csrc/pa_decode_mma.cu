@@ -37,8 +37,8 @@ cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream
     const long long grid = (long long)p.batch * p.Hkv * p.Cmax;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    kern<<<(unsigned)grid, kMmaWarps * 32, Cfg::SMEM_BYTES, stream>>>(p, tm[0], tm[1]);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kMmaWarps * 32), Cfg::SMEM_BYTES, stream, p,
+                      tm[0], tm[1]);
 }
 
 template <int D, int B>

@@ -68,6 +68,8 @@ template <int D, int B, int G, int NW, int S>
 __global__ void __launch_bounds__(NW * 32)
     pa_decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
+    pdl_trigger();
+    pdl_wait();
     using C = MmaCfg<D, B, G, NW, S>;
     extern __shared__ unsigned char smem_raw[];
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pa {
 
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -12,6 +14,36 @@ constexpr unsigned kFullMask = 0xffffffffu;
 // A bounded wait gives up after this many nanoseconds of %globaltimer.  A bulk
 // copy of a few KiB completes in microseconds; two seconds means it never will.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation: it lets the next kernel in the stream be
+// scheduled as soon as all of its own CTAs have started (pdl_trigger at the
+// top), and waits for the previous kernel to complete and flush its writes
+// (pdl_wait) before it reads anything that kernel may have produced.  A
+// dependent grid only launches once every CTA of its primary has been
+// scheduled, so waiting CTAs never starve the grids they wait for.  Both are
+// no-ops when there is no programmatic predecessor / successor.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Host: launch `kern` with the programmatic-serialisation attribute.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
