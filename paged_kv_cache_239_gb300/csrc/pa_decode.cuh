@@ -162,10 +162,11 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     const int rg = lane / C::LR;  // row group
     const int jl = lane % C::LR;  // position within the row
 
-    // ---- CTA coordinates: partition fastest, then KV head, then sequence ----
+    // ---- CTA coordinates: KV head fastest, then sequence, partition slowest ----
     int idx = blockIdx.x;
-    const int c = idx % p.Cmax;
-    idx /= p.Cmax;
+    const int nbh = p.batch * p.Hkv;
+    const int c = idx / nbh;
+    idx %= nbh;
     const int kvh = idx % p.Hkv;
     const int b = idx / p.Hkv;
 

@@ -78,9 +78,13 @@ __global__ void __launch_bounds__(NW * 32)
     const int g = lane >> 2;  // mma group id
     const int cq = lane & 3;  // thread within the group
 
+    // CTA order: partition index slowest, so the end of the grid holds only the
+    // last (partial) partitions of the longest sequences and empty slots --
+    // a lighter tail than ending on full partitions (1-1.5% on GB300).
     int idx = blockIdx.x;
-    const int c = idx % p.Cmax;
-    idx /= p.Cmax;
+    const int nbh = p.batch * p.Hkv;
+    const int c = idx / nbh;
+    idx %= nbh;
     const int kvh = idx % p.Hkv;
     const int b = idx / p.Hkv;
 
