@@ -64,8 +64,8 @@ def decode_flops(wl) -> int:
 # pa_decode_mma_kernel (ncu --set full) + pa_combine_kernel (ncu dram metrics),
 # see profiles/; valid only for the kernel sources they were taken from.
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2230982000 + 6236160 + 9851520,
-    "sources_sha256": "68f9745bdef703c277941acfe1662ff54a62bfdfff5500dea630c286be94dc00",
+    "bytes_per_launch": 2231161000 + 6421760 + 9851904,
+    "sources_sha256": "70686596f0b413de2000617cf15a12daca31341108ec92c37fa719edaf846ed2",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h"]
