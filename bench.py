@@ -278,6 +278,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     wl = W.named(args.workload)
+    if args.kv_heads > 0:      # same lengths, tables and query heads; another group size
+        if wl.num_heads % args.kv_heads:
+            raise SystemExit("--kv-heads must divide the workload's query heads")
+        wl.num_kv_heads = args.kv_heads
     if args.pool_layers > 0:   # smaller pool (same lengths/tables) for profiler captures
         wl.num_layers = min(args.pool_layers, wl.num_layers)
     L = wl.num_layers if args.layers <= 0 else min(args.layers, wl.num_layers)
@@ -803,6 +807,9 @@ def main():
                     help="with --row loop: free stack on the device, one CUDA graph per run")
     ap.add_argument("--fused", action="store_true",
                     help="step mode: pa_write_kv_and_decode instead of two calls per layer")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="override the workload's KV heads (query heads unchanged): group-size "
+                         "sweeps, e.g. --kv-heads 1 for one KV head per 32 query heads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--pool-layers", type=int, default=0,

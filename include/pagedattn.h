@@ -129,8 +129,9 @@ PA_API int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, i
 PA_API int pa_pool_destroy(pa_pool* pool);
 
 /* Built shapes: head_dim 64 or 128, block_size 16 or 32; GQA group
- * (num_heads / num_kv_heads) 1-8 or 16 on the tensor-core kernel (bf16 pools),
- * 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
+ * (num_heads / num_kv_heads) 1-8, 16 or any multiple of 8 on the tensor-core
+ * kernel (bf16 pools; groups above 16 run as 16- or 8-head chunks whose CTAs
+ * share each K/V tile through L2), 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
  *
  * Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
  * the tensor-core kernel for bf16 pools (mma.sync, K/V staged by tensor-map

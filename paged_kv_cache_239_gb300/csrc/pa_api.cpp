@@ -134,7 +134,8 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         !(pool->g.dtype == 1 && pa::decode_mma_supported(pool->g.D, pool->g.B, G)))
         return fail(PA_ERR_UNSUPPORTED,
                     "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
-                    "(built: head_dim 64/128, block_size 16/32; group 1-8 or 16 for bf16 pools, "
+                    "(built: head_dim 64/128, block_size 16/32; group 1-8, 16 or a multiple of 8 "
+                    "for bf16 pools, "
                     "1/2/4/8 for fp32 pools)",
                     pool->g.dtype, pool->g.D, pool->g.B, G);
     int pb = partition_blocks;
@@ -146,9 +147,11 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
     }
     if (pb > maxb) pb = maxb;
     const int Cmax = (maxb + pb - 1) / pb;
-    if ((long long)batch * pool->g.Hkv * Cmax > INT_MAX)
+    const int chunk = pa::decode_mma_chunk(G);
+    const long long nchunks = (pool->g.dtype == 1 && chunk > 0) ? G / chunk : 1;
+    if ((long long)batch * pool->g.Hkv * nchunks * Cmax > INT_MAX)
         return fail(PA_ERR_INVALID_ARG, "grid of %lld CTAs is too large",
-                    (long long)batch * pool->g.Hkv * Cmax);
+                    (long long)batch * pool->g.Hkv * nchunks * Cmax);
     out->G = G;
     out->PB = pb;
     out->Cmax = Cmax;

@@ -34,7 +34,7 @@ cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream
             done_mask |= bit;
         }
     }
-    const long long grid = (long long)p.batch * p.Hkv * p.Cmax;
+    const long long grid = (long long)p.batch * p.Hkv * p.nchunks * p.Cmax;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kMmaWarps * 32), Cfg::SMEM_BYTES, stream, p,
@@ -73,16 +73,29 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+int decode_mma_chunk(int G) {
+    if (G >= 1 && G <= 8) return G;
+    if (G == 16) return 16;
+    if (G > 16 && G % 16 == 0) return 16;
+    if (G > 16 && G % 8 == 0) return 8;
+    return 0;
+}
+
 bool decode_mma_supported(int D, int B, int G) {
     if (D != 64 && D != 128) return false;
     if (B != 16 && B != 32) return false;
-    // heads past G in the 8-wide mma tiles are masked
-    return (G >= 1 && G <= 8) || G == 16;
+    // heads past G in the 8-wide mma tiles are masked; larger groups in chunks
+    return decode_mma_chunk(G) > 0;
 }
 
-cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, int B, int G,
+cudaError_t launch_decode_mma(const DecodeParams& p_in, const void* tmaps, int D, int B, int Gtot,
                               cudaStream_t s) {
     const CUtensorMap* tm = static_cast<const CUtensorMap*>(tmaps);
+    const int G = decode_mma_chunk(Gtot);
+    if (G == 0) return cudaErrorNotSupported;
+    DecodeParams p = p_in;
+    p.gsize = Gtot;
+    p.nchunks = Gtot / G;
     if (D == 64) {
         if (B == 16) return launch_g<64, 16>(p, tm, G, s);
         if (B == 32) return launch_g<64, 32>(p, tm, G, s);

@@ -81,16 +81,22 @@ __global__ void __launch_bounds__(NW * 32)
     // CTA order: partition index slowest, so the end of the grid holds only the
     // last (partial) partitions of the longest sequences and empty slots --
     // a lighter tail than ending on full partitions (1-1.5% on GB300).
+    // A group larger than G is split into head chunks of G (fastest index):
+    // sibling chunks of one (sequence, KV head, partition) run side by side and
+    // share each K/V tile through L2.
     int idx = blockIdx.x;
+    const int hc = idx % p.nchunks;
+    idx /= p.nchunks;
     const int nbh = p.batch * p.Hkv;
     const int c = idx / nbh;
     idx %= nbh;
     const int kvh = idx % p.Hkv;
     const int b = idx / p.Hkv;
+    const int hbase = kvh * p.gsize + hc * G;  // first query head of this CTA in the sequence
 
     int n = __ldg(p.lens + b);
     if (n < 0 || n > p.maxb * B) {
-        if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+        if (c == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
         n = 0;
     }
     const int nblk = (n + B - 1) / B;
@@ -136,8 +142,11 @@ __global__ void __launch_bounds__(NW * 32)
     if (p.new_k != nullptr) {
         const int pos = __ldg(p.positions + b);
         if (pos < 0 || pos / B >= p.maxb) {
-            if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+            if (c == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0)
+                atomicOr(p.status, kStatusBadLength);
         } else if (c == (pos < n ? (pos / B) / p.PB : 0)) {
+            // every head chunk of the owning partition stores the (identical) row
+            // itself: its own store is then ordered before its own bulk copies
             constexpr int CPR = D * 2 / 16;
             const int blk = __ldg(bt_row + pos / B);
             if (blk < 0 || blk >= p.num_blocks) {
@@ -207,7 +216,7 @@ __global__ void __launch_bounds__(NW * 32)
     for (int nt = 0; nt < C::NT; ++nt) {
         const int hq = 8 * nt + g;
         const unsigned short* qrow =
-            reinterpret_cast<const unsigned short*>(p.q) + ((long long)b * p.H + kvh * G + hq) * D;
+            reinterpret_cast<const unsigned short*>(p.q) + ((long long)b * p.H + hbase + hq) * D;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
             if (hq < G) {
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(NW * 32)
     __syncthreads();
 
     // ---- merge the NW warps (log-sum-exp) and write ----
-    const long long head0 = (long long)b * p.H + kvh * G;
+    const long long head0 = (long long)b * p.H + hbase;
     for (int t = threadIdx.x; t < G * D; t += NW * 32) {
         const int h = t / D;
         const int d = t % D;

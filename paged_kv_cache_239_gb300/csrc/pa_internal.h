@@ -56,6 +56,9 @@ struct DecodeParams {
     // tensor-core kernel only: which of the tensor maps' outer dimensions
     // (2, 3, 4) index the physical block, the layer and the kv head
     int tma_slot_blk, tma_slot_layer, tma_slot_head;
+    // tensor-core kernel only: the group (num_heads / Hkv) is served in
+    // `nchunks` chunks of the kernel's compile-time G heads (1 unless G > 16)
+    int gsize, nchunks;
 };
 
 struct WriteParams {
@@ -96,7 +99,10 @@ cudaError_t launch_decode_f32(const DecodeParams& p, int D, int B, int G, cudaSt
 bool decode_supported(int dtype, int D, int B, int G);
 
 // Tensor-core kernel for bf16 pools; `tmaps` points to two CUtensorMap (K, V).
+// Groups of up to 8 or exactly 16 heads run in one CTA per KV head; larger
+// multiples of 8 in chunks (decode_mma_chunk gives the chunk size, 0 if none).
 bool decode_mma_supported(int D, int B, int G);
+int decode_mma_chunk(int G);
 cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, int B, int G,
                               cudaStream_t s);
 // Encodes the K and V tensor maps of a bf16 pool (5-D, box 64 x 16, 128-byte

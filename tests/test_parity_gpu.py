@@ -428,3 +428,44 @@ def test_group_of_16_on_tensor_cores(cuda_device, D, Bs):
         gpu_decode(gp, q.to(cuda_device), 1, bt, ln)
     assert e.value.code == B.PA_ERR_UNSUPPORTED
     _check_status()
+
+
+@pytest.mark.parametrize("Hkv,H,D,Bs", [(1, 24, 128, 16), (2, 64, 128, 32), (1, 32, 64, 16),
+                                         (1, 64, 128, 16)])
+def test_large_groups_in_head_chunks(cuda_device, Hkv, H, D, Bs):
+    """Groups above 16 (multiples of 8, e.g. MQA with one KV head) run as 8- or
+    16-head chunks of CTAs; every head matches the oracle, split or not, and
+    the fused append works per chunked group."""
+    wl = W.custom("bigg", "bf16", 2, H, Hkv, D, Bs, [1, Bs - 1, 3 * Bs, 9 * Bs + 5, 0, 400],
+                  seed=H + D, spare_blocks=2, interleave=True, steps=1)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    bt, ln = device_tables(wl, cuda_device)
+    ref = oracle_decode(wl, pool, q, 1)
+    for pb in (0, 1, 4, wl.max_blocks):
+        out = gpu_decode(gp, q.to(cuda_device), 1, bt, ln, partition_blocks=pb)
+        assert max_abs_err(out, ref) <= 2e-3, pb
+    k, v = W.make_new_tokens(wl, 1)
+    tables = wl.block_tables.copy()
+    for b, n in enumerate(wl.context_lens):
+        if n % Bs == 0:
+            tables[b, n // Bs] = wl.free_stack.pop()
+    btn = torch.from_numpy(tables).to(cuda_device)
+    pos = torch.from_numpy(wl.context_lens.copy()).to(cuda_device)
+    lens1 = wl.context_lens + 1
+    out = torch.full((wl.batch, H, D), float("nan"), device=cuda_device)
+    need = B.pa_decode_workspace_size(gp.h, wl.batch, H, wl.max_blocks, 2)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=cuda_device)
+    B.pa_write_kv_and_decode(out, q.to(cuda_device), gp.h, 0, k[0].to(cuda_device),
+                             v[0].to(cuda_device), pos, btn, wl.max_blocks,
+                             torch.from_numpy(lens1).to(cuda_device), wl.batch, Bs, H, Hkv, D,
+                             wl.scale, 2, ws, need)
+    host = W.as_oracle_array(pool).copy()
+    oracle.write_kv(host, 0, W.as_oracle_array(k[0]), W.as_oracle_array(v[0]), tables,
+                    wl.context_lens)
+    ref1 = oracle.decode_attention(W.as_oracle_array(q), host, 0, tables, lens1, H, wl.scale)
+    torch.cuda.synchronize()
+    assert max_abs_err(out, ref1) <= 2e-3
+    assert np.array_equal(W.as_oracle_array(gp.t), host)
+    _check_status()

@@ -1,5 +1,5 @@
 """Seeded randomized parity sweep on the GPU: random shapes (dtype, head_dim,
-block size, GQA group 1-8 or 16, KV heads, batch, ragged lengths with 0 / 1 / block
+block size, GQA group 1-8, 16, 24, 32, KV heads, batch, ragged lengths with 0 / 1 / block
 multiples), random layer, partition size, pool layout and decode kernel, plus
 the fused append path -- each case against the oracle on the same inputs."""
 import numpy as np
@@ -23,7 +23,7 @@ def _case(i):
     Bs = int(rng.choice([16, 32]))
     Hkv = int(rng.choice([1, 2, 4]))
     G = int(rng.choice([1, 2, 4, 8])) if dtype == "f32" else \
-        int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 16]))
+        int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 16, 24, 32]))
     L = int(rng.integers(1, 4))
     batch = int(rng.integers(1, 10))
     special = [0, 1, Bs - 1, Bs, Bs + 1, 2 * Bs]
