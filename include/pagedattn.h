@@ -129,17 +129,28 @@ PA_API int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, i
 PA_API int pa_pool_destroy(pa_pool* pool);
 
 /* Built shapes: head_dim 64 or 128, block_size 16 or 32; GQA group
- * (num_heads / num_kv_heads) 1-8, 16 or any multiple of 8 on the tensor-core
- * kernel (bf16 pools; groups above 16 run as 16- or 8-head chunks whose CTAs
- * share each K/V tile through L2), 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
+ * (num_heads / num_kv_heads) 1-8, 16 or any multiple of 8 on the mma.sync
+ * tensor-core kernel (bf16 pools; groups above 16 run as 16- or 8-head chunks
+ * whose CTAs share each K/V tile through L2), any multiple of 16 on the
+ * tcgen05 kernel (bf16 pools, head_dim 128; chunks of 64, 32 or 16 heads),
+ * 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
  *
  * Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
- * the tensor-core kernel for bf16 pools (mma.sync, K/V staged by tensor-map
- * TMA), the CUDA-core kernel for fp32 pools.  PA_DECODE_CUDA_CORES forces the
- * CUDA-core kernel (fp32 FMA on every dtype); PA_DECODE_TENSOR_CORES makes
- * calls that the tensor-core kernel cannot serve fail with PA_ERR_UNSUPPORTED.
- * Both compute the same result within the stated tolerances. */
-enum { PA_DECODE_AUTO = 0, PA_DECODE_CUDA_CORES = 1, PA_DECODE_TENSOR_CORES = 2 };
+ * for bf16 pools the tcgen05 kernel for groups that are multiples of 64 (S and
+ * O accumulate in tensor memory), else the mma.sync kernel (K/V staged by
+ * tensor-map TMA); the CUDA-core kernel for fp32 pools.
+ * PA_DECODE_CUDA_CORES forces the CUDA-core kernel (fp32 FMA on every dtype),
+ * PA_DECODE_TENSOR_CORES the mma.sync kernel, PA_DECODE_TCGEN05 the tcgen05
+ * kernel; a forced kernel that cannot serve a call makes it fail with
+ * PA_ERR_UNSUPPORTED.  All compute the same result within the stated
+ * tolerances.  The choice also fixes the automatic partition size (and so the
+ * workspace size): query pa_decode_workspace_size after setting it. */
+enum {
+    PA_DECODE_AUTO = 0,
+    PA_DECODE_CUDA_CORES = 1,
+    PA_DECODE_TENSOR_CORES = 2,
+    PA_DECODE_TCGEN05 = 3
+};
 PA_API int pa_pool_set_decode_kernel(pa_pool* pool, int kind);
 
 /* Bytes of one physical block: 2 * num_layers * num_kv_heads * block_size *

@@ -26,6 +26,7 @@ PA_ERR_WORKSPACE = 6
 PA_DECODE_AUTO = 0
 PA_DECODE_CUDA_CORES = 1
 PA_DECODE_TENSOR_CORES = 2
+PA_DECODE_TCGEN05 = 3
 
 PA_DTYPE_F32 = 0
 PA_DTYPE_BF16 = 1

@@ -79,18 +79,36 @@ int num_sms_current(int* out) {
 // GB300 sweeps: large-batch 64 blocks (fastest; picks 64), long-context 32
 // (fastest; the unrounded 35 was 2.5% slower; picks 32), MHA batch 64 12-16
 // (picks 16), mini-infer shape 4-8 (picks 8).
-int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sms) {
+int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sms, int G) {
     const long long blk_bytes = 2LL * g.B * g.D * g.elt;
     const long long est_total = (long long)batch * g.Hkv * maxb * blk_bytes / 2;
     long long pb = est_total / ((long long)num_sms * 12 * blk_bytes);
     long long hi = 64;
     if (hi * blk_bytes > (1LL << 20)) hi = (1LL << 20) / blk_bytes;
     const long long lo = (32 * 1024 + blk_bytes - 1) / blk_bytes;
+    // Groups of 16 and more carry G times the work per K/V byte: fewer, longer
+    // partitions win (GB300, large-batch lengths: 64 blocks beat the estimate's
+    // 16-32 by 10-54 % for G = 16, 32, 64).
+    if (G >= 16) pb = hi;
     if (pb > hi) pb = hi;
     if (pb < lo) pb = lo;
     if (pb > 8) pb -= pb % 8;
     if (pb > maxb) pb = maxb;
     if (pb < 1) pb = 1;
+    return (int)pb;
+}
+
+// tcgen05 kernel (persistent, one CTA per SM, 128-token tiles): the same
+// estimate, rounded up to whole tiles, and at least 1024 tokens per item so
+// that the per-item work (q load, first-tile max, epilogue) stays small against
+// the K/V stream (GB300: 1024 tokens fastest for G = 32 and 64).
+int auto_partition_blocks_tcgen05(const pa::PoolGeom& g, int batch, int maxb, int num_sms,
+                                  int G) {
+    const int tile_blocks = 128 / g.B;
+    long long pb = auto_partition_blocks(g, batch, maxb, num_sms, G);
+    if (pb < 1024 / g.B) pb = 1024 / g.B;
+    pb = (pb + tile_blocks - 1) / tile_blocks * tile_blocks;
+    if (pb > maxb) pb = maxb;
     return (int)pb;
 }
 
@@ -113,10 +131,58 @@ int check_layer(const pa_pool* pool, int layer) {
     return PA_OK;
 }
 
+// The kernels a decode call can run on.
+enum class Kernel { CudaCores, MmaSync, Tcgen05 };
+
 struct DecodeShape {
     int G, PB, Cmax;
+    Kernel kernel;
     size_t ws_bytes;
 };
+
+// The kernel the pool's choice selects for group G, or a PA_ERR_UNSUPPORTED
+// failure.  Automatic: tcgen05 for groups that are multiples of 64 (head_dim
+// 128), mma.sync for the other bf16 shapes, CUDA cores for fp32.  (GB300,
+// large-batch lengths: tcgen05 is 26 % faster than mma.sync at G = 64, level at
+// G = 32, slower at G = 16.)
+int pick_kernel(const pa_pool* pool, int G, Kernel* k) {
+    const pa::PoolGeom& g = pool->g;
+    const bool cuda_ok = pa::decode_supported(g.dtype, g.D, g.B, G);
+    const bool mma_ok = g.dtype == 1 && pa::decode_mma_supported(g.D, g.B, G);
+    const bool umma_ok = g.dtype == 1 && pa::decode_umma_supported(g.D, g.B, G);
+    if (!cuda_ok && !mma_ok && !umma_ok)
+        return fail(PA_ERR_UNSUPPORTED,
+                    "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
+                    "(built: head_dim 64/128, block_size 16/32; group 1-8, 16 or a multiple of 8 "
+                    "for bf16 pools, 1/2/4/8 for fp32 pools)",
+                    g.dtype, g.D, g.B, G);
+    switch (pool->decode_kernel) {
+        case PA_DECODE_CUDA_CORES:
+            if (!cuda_ok)
+                return fail(PA_ERR_UNSUPPORTED, "no CUDA-core decode kernel for group size %d", G);
+            *k = Kernel::CudaCores;
+            return PA_OK;
+        case PA_DECODE_TENSOR_CORES:
+            if (!mma_ok)
+                return fail(PA_ERR_UNSUPPORTED,
+                            "no mma.sync tensor-core decode kernel for this pool / group size");
+            *k = Kernel::MmaSync;
+            return PA_OK;
+        case PA_DECODE_TCGEN05:
+            if (!umma_ok)
+                return fail(PA_ERR_UNSUPPORTED,
+                            "no tcgen05 decode kernel for this pool / group size (bf16, head_dim "
+                            "128, group a multiple of 16)");
+            *k = Kernel::Tcgen05;
+            return PA_OK;
+        default:
+            *k = (umma_ok && G % 64 == 0) ? Kernel::Tcgen05
+                 : mma_ok                 ? Kernel::MmaSync
+                 : umma_ok                ? Kernel::Tcgen05
+                                          : Kernel::CudaCores;
+            return PA_OK;
+    }
+}
 
 int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb,
                          int partition_blocks, DecodeShape* out) {
@@ -130,29 +196,28 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
     if (partition_blocks < 0)
         return fail(PA_ERR_INVALID_ARG, "partition_blocks %d < 0", partition_blocks);
     const int G = num_heads / pool->g.Hkv;
-    if (!pa::decode_supported(pool->g.dtype, pool->g.D, pool->g.B, G) &&
-        !(pool->g.dtype == 1 && pa::decode_mma_supported(pool->g.D, pool->g.B, G)))
-        return fail(PA_ERR_UNSUPPORTED,
-                    "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
-                    "(built: head_dim 64/128, block_size 16/32; group 1-8, 16 or a multiple of 8 "
-                    "for bf16 pools, "
-                    "1/2/4/8 for fp32 pools)",
-                    pool->g.dtype, pool->g.D, pool->g.B, G);
+    Kernel kernel = Kernel::CudaCores;
+    if (int rc = pick_kernel(pool, G, &kernel)) return rc;
     int pb = partition_blocks;
     if (pb == 0) {
         int sms = 0;
         int rc = num_sms_current(&sms);
         if (rc != PA_OK) return rc;
-        pb = auto_partition_blocks(pool->g, batch, maxb, sms);
+        pb = kernel == Kernel::Tcgen05
+                 ? auto_partition_blocks_tcgen05(pool->g, batch, maxb, sms, G)
+                 : auto_partition_blocks(pool->g, batch, maxb, sms, G);
     }
     if (pb > maxb) pb = maxb;
     const int Cmax = (maxb + pb - 1) / pb;
-    const int chunk = pa::decode_mma_chunk(G);
-    const long long nchunks = (pool->g.dtype == 1 && chunk > 0) ? G / chunk : 1;
+    const int chunk = kernel == Kernel::Tcgen05 ? pa::decode_umma_chunk(G)
+                      : kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G)
+                                                  : G;
+    const long long nchunks = G / chunk;
     if ((long long)batch * pool->g.Hkv * nchunks * Cmax > INT_MAX)
         return fail(PA_ERR_INVALID_ARG, "grid of %lld CTAs is too large",
                     (long long)batch * pool->g.Hkv * nchunks * Cmax);
     out->G = G;
+    out->kernel = kernel;
     out->PB = pb;
     out->Cmax = Cmax;
     out->ws_bytes = workspace_bytes_for(batch, num_heads, Cmax, pool->g.D);
@@ -290,7 +355,8 @@ int pa_pool_destroy(pa_pool* pool) {
 
 int pa_pool_set_decode_kernel(pa_pool* pool, int kind) {
     if (int rc = check_pool(pool)) return rc;
-    if (kind != PA_DECODE_AUTO && kind != PA_DECODE_CUDA_CORES && kind != PA_DECODE_TENSOR_CORES)
+    if (kind != PA_DECODE_AUTO && kind != PA_DECODE_CUDA_CORES && kind != PA_DECODE_TENSOR_CORES &&
+        kind != PA_DECODE_TCGEN05)
         return fail(PA_ERR_INVALID_ARG, "unknown decode kernel kind %d", kind);
     std::lock_guard<std::mutex> lock(pool->mu);
     pool->decode_kernel = kind;
@@ -581,13 +647,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     p.new_v = new_v;
     p.positions = positions;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool mma_ok = g.dtype == 1 && pa::decode_mma_supported(g.D, g.B, sh.G);
-    if (pool->decode_kernel == PA_DECODE_TENSOR_CORES && !mma_ok)
-        return fail(PA_ERR_UNSUPPORTED, "no tensor-core decode kernel for this pool / group size");
-    if (!pa::decode_supported(g.dtype, g.D, g.B, sh.G) &&
-        (!mma_ok || pool->decode_kernel == PA_DECODE_CUDA_CORES))
-        return fail(PA_ERR_UNSUPPORTED, "no CUDA-core decode kernel for group size %d", sh.G);
-    if (mma_ok && pool->decode_kernel != PA_DECODE_CUDA_CORES) {
+    if (sh.kernel != Kernel::CudaCores) {
         {
             std::lock_guard<std::mutex> lock(pool->mu);
             if (!pool->tmaps_ready) {
@@ -600,7 +660,8 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
         p.tma_slot_blk = pool->tma_slots[0];
         p.tma_slot_layer = pool->tma_slots[1];
         p.tma_slot_head = pool->tma_slots[2];
-        e = pa::launch_decode_mma(p, pool->tmaps, g.D, g.B, sh.G, s);
+        e = sh.kernel == Kernel::Tcgen05 ? pa::launch_decode_umma(p, pool->tmaps, g.B, sh.G, s)
+                                         : pa::launch_decode_mma(p, pool->tmaps, g.D, g.B, sh.G, s);
     } else {
         e = g.dtype == 1 ? pa::launch_decode_bf16(p, g.D, g.B, sh.G, s)
                          : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);

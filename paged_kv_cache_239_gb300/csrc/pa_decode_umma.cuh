@@ -1,0 +1,807 @@
+// pa_decode_umma.cuh -- paged decode attention for bf16 pools with large GQA
+// groups (16, 32 or 64 query heads per CTA) on the 5th-generation tensor cores:
+// tcgen05.mma with the accumulators in tensor memory (TMEM).
+//
+// Computes the same thing as the other decode kernels: for sequence b and query
+// head h, out = softmax_t(scale * q . K_t) V_t over the tokens reached through
+// the block table ("vllmini", "PagedAttention Metaphor" / "The CUDA Block
+// Kernel"; mini-infer, "The Solution").
+//
+// Why a separate kernel: the work per K/V byte grows with the group (G flop per
+// byte for S = K Q^T, twice that for P V with the hi + lo split of P).  Up to
+// G = 8 mma.sync keeps pace with HBM; from G = 16 it does not, and a tile with
+// 128 tokens x G heads is a real contraction.
+//
+// Structure: persistent CTAs (one per SM, ~220 KB of shared memory), each
+// working through (sequence, KV head, head chunk, partition) items, with
+// warp-specialised roles connected by mbarriers:
+//  * warp 0 (producer): block-table walk, fused append store, q of the item
+//    into a swizzled K-major tile, and 5-D tensor-map TMA loads of 128-token
+//    K and V tiles (8 boxes of 16 rows per 64-column half, SWIZZLE_128B) into
+//    an ST-stage ring;
+//  * warp 1 (MMA): allocates TMEM; one thread issues
+//      S[128 tok x G]   = K[128 x 128] . Q^T          (A, B K-major in smem)
+//      O^T[128 d x 2G] += V^T[128 x 128 tok] . [P_hi | P_lo]  (A, B MN-major)
+//    and signals completion with tcgen05.commit.  S is double-buffered in
+//    TMEM, so S of tile i+1 is computed while tile i's softmax runs;
+//  * warps 2-5 (softmax, 128 threads, one TMEM lane each): read S (thread =
+//    token), online softmax in base 2 with a lazily raised running max (the
+//    max is raised, and O and the sums rescaled, only when a score exceeds it
+//    by more than 2^8 -- any reference point gives the same normalised
+//    result), write P as bf16 hi + lo (|P - hi - lo| <= 2^-16 P) into shared
+//    memory, and at the end of an item read O (thread = head-dim element),
+//    add the hi and lo halves and store the output or the split partial.
+// Every wait is bounded (PA_STATUS_TIMEOUT); the roles then stop together,
+// wait for their copies and MMAs in flight, and TMEM is freed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------- tcgen05 --
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (all >> 4), the fixed version field (bits 46-48 = 0b001) and the
+// 128-byte swizzle (layout type 2 in bits 61-63).  K-major operands: SBO is the
+// distance between 8-row groups, LBO unused.  MN-major operands: LBO is the
+// distance between 64-element column blocks, SBO between 8-row (K) groups.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B,
+// operand majors (0 = K-major, 1 = MN-major), N >> 3 and M >> 4.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) = A . B (+ D if accumulate), issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier receives one arrival once every tcgen05 operation this thread
+// issued before has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_addr, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     slot_addr),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane (32x32b shape: lane
+// 32 * (warp % 4) + laneid of the warp's quarter).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
+// N (8 or a multiple of 16) consecutive columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+    if constexpr (N == 8) {
+        tmem_ld8(taddr, r);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 16)
+            tmem_ld16(taddr + c, *reinterpret_cast<uint32_t(*)[16]>(r + c));
+    }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t* r) {
+    if constexpr (N == 8) {
+        tmem_st8(taddr, r);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; c += 16)
+            tmem_st16(taddr + c, *reinterpret_cast<const uint32_t(*)[16]>(r + c));
+    }
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Named barriers over the 128 softmax threads of one head part (four warps,
+// one per TMEM lane quarter): id 1 + 2 * part plain, 2 + 2 * part with an OR
+// reduction of `v` (separate ids, so the two forms never share one).
+__device__ __forceinline__ void part_bar(int part) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + 2 * part) : "memory");
+}
+__device__ __forceinline__ bool part_bar_or(int part, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(2 + 2 * part)
+        : "memory");
+    return r != 0;
+}
+
+// ------------------------------------------------------------------ config --
+
+template <int B_, int G_>
+struct UmmaCfg {
+    static constexpr int D = 128, B = B_, G = G_;
+    static constexpr int TT = 128;                  // tokens per tile (M of S = K Q^T)
+    static constexpr int NBOX = TT / 16;            // 16-row boxes per 64-column half
+    static constexpr int HALF = TT * 128;           // one 64-column half of a tile (bytes)
+    static constexpr int KV_TILE = 2 * HALF;        // K (or V) tile
+    static constexpr int STAGE = 2 * KV_TILE;       // K tile, then V tile
+    static constexpr int ST = 3;                    // pipeline stages
+    // P of a tile: [64-column block][token][128 B] rows of hi heads | lo heads |
+    // zeros, written into the K half of the tile's own stage once S = K Q^T has
+    // consumed it -- one P buffer per stage, so the softmax of tile i+1 never
+    // waits for P V of tile i.
+    static constexpr int PW = 2 * G < 64 ? 64 : 2 * G;
+    static constexpr int P_BYTES = (PW / 64) * HALF;
+    static constexpr int Q_BYTES = 2 * G * 128;     // q of the item, two 64-column halves
+    static constexpr int O_COL = 2 * G;             // TMEM: S0 [0, G), S1 [G, 2G), O^T after
+    static constexpr int TMEM_COLS = (2 * G + PW) <= 32 ? 32 : (2 * G + PW) <= 64 ? 64
+                                   : (2 * G + PW) <= 128 ? 128 : (2 * G + PW) <= 256 ? 256 : 512;
+    static constexpr int OFF_Q = ST * STAGE;
+    static constexpr int OFF_CTRL = OFF_Q + 2 * Q_BYTES;
+    // ctrl: mbarriers [0, 160) | stage meta | TMEM address | abort flag | m[G] | alpha[G] | red[4][G]
+    static constexpr int CTRL_BYTES = 256 + 6 * G * 4;
+    static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
+    // softmax: 4 lane quarters x (G / HG) head parts, one warp each (more
+    // than one warp per scheduler, so the dependent latencies of the
+    // per-token work overlap)
+    static constexpr int HG = G / 2;                // heads per softmax warp
+    static constexpr int NSW = 4 * (G / HG);        // softmax warps
+    static constexpr int NSM = NSW * 32;            // softmax threads
+    static constexpr int THREADS = 64 + NSM;
+    // barrier indices
+    static constexpr int KV_FULL = 0, KV_EMPTY = ST, Q_FULL = 2 * ST, Q_EMPTY = 2 * ST + 2,
+                         S_FULL = 2 * ST + 4, P_FULL = 2 * ST + 6, PV_DONE = 2 * ST + 8,
+                         FINAL = 2 * ST + 10, NBAR = 2 * ST + 11;
+    // S_FULL, P_FULL and PV_DONE are pairs used by tile parity.  The softmax of
+    // tile i + 1 may finish before the MMA thread has seen P of tile i, and a
+    // softmax thread waits on P V of tile i - 1 at most: with a pair, no
+    // barrier ever runs two phases ahead of a waiter (parity waits would alias).
+
+    static_assert(G == 16 || G == 32 || G == 64, "head chunk of 16, 32 or 64");
+    static_assert(B == 16 || B == 32, "block size 16 or 32");
+    static_assert(NBAR * 8 <= 160, "barriers");
+    static_assert(2 * G + PW <= TMEM_COLS, "TMEM columns");
+    static_assert(P_BYTES <= KV_TILE, "P fits in the K half of a stage");
+    static_assert(HG == 8 || HG % 16 == 0, "TMEM loads of 8 or 16k columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// One work item: (sequence b, KV head, head chunk, partition c).  Decoded the
+// same way by every role.  Head chunk fastest, then KV head, sequence, and
+// partition slowest (the grid-stride order of the items).
+struct UItem {
+    int b, kvh, hc, c, hbase, n, nparts, t0, t1, ntiles;
+    bool bad_len;
+};
+
+template <int B, int G>
+__device__ __forceinline__ bool umma_item(const DecodeParams& p, int idx, UItem& it) {
+    it.hc = idx % p.nchunks;
+    idx /= p.nchunks;
+    const int nbh = p.batch * p.Hkv;
+    it.c = idx / nbh;
+    idx %= nbh;
+    it.kvh = idx % p.Hkv;
+    it.b = idx / p.Hkv;
+    it.hbase = it.kvh * p.gsize + it.hc * G;
+    int n = __ldg(p.lens + it.b);
+    it.bad_len = n < 0 || n > p.maxb * B;
+    if (it.bad_len) n = 0;
+    it.n = n;
+    const int nblk = (n + B - 1) / B;
+    it.nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
+    const long long t0 = (long long)it.c * p.PB * B;
+    const long long t1 = min((long long)n, t0 + (long long)p.PB * B);
+    it.t0 = (int)min(t0, (long long)n);
+    it.t1 = (int)t1;
+    it.ntiles = t1 > t0 ? (int)((t1 - t0 + 127) / 128) : 0;
+    return it.c < it.nparts;
+}
+
+// Non-blocking test of an mbarrier phase (try_wait may suspend the thread for
+// a while; a thread that polls several barriers must not be parked on one).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, volatile int* abort_all,
+                                          unsigned* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_all) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+    }
+    *abort_all = 1;
+    atomicOr(status, kStatusTimeout);
+    return false;
+}
+
+// Byte offset of 16-byte chunk j of row r in a 1024-byte-aligned stack of
+// 128-byte rows with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128(int r, int j) {
+    return (uint32_t)(r * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+
+// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all
+// of this thread's outstanding ones.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int B, int G>
+__global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
+    pa_decode_umma_kernel(const DecodeParams p, const int total_items,
+                          const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv) {
+    pdl_trigger();
+    pdl_wait();
+    using C = UmmaCfg<B, G>;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+    unsigned char* smem = smem_raw + (sbase - raw_addr);
+    unsigned char* ctrl = smem + C::OFF_CTRL;
+    const uint32_t bar0 = sbase + C::OFF_CTRL;
+    int* meta = reinterpret_cast<int*>(ctrl + 160);                 // bad-box mask per stage
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 176);
+    volatile int* abort_all = reinterpret_cast<volatile int*>(ctrl + 180);
+    float* m_sh = reinterpret_cast<float*>(ctrl + 256);             // running max per head
+    float* a_sh = m_sh + G;                                         // rescale factor per head
+    float* red = a_sh + G;                                          // [4][G] cross-warp partials
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::NBAR; ++i)
+            mbar_init(bar0 + 8 * i, (i == C::P_FULL || i == C::P_FULL + 1) ? C::NSM : 1);
+        *abort_all = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================================================= producer (warp 0)
+        const uint64_t policy = l2_policy_evict_first();
+        int kt = 0, qi = 0;
+        bool aborted = false;
+        for (int idx = blockIdx.x; idx < total_items && !aborted; idx += gridDim.x) {
+            UItem it;
+            const bool live = umma_item<B, G>(p, idx, it);
+            if (it.bad_len && it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
+                atomicOr(p.status, kStatusBadLength);
+            if (!live) continue;
+            const int* bt_row = p.bt + (long long)it.b * p.maxb;
+            const long long tile0 = p.tile_off + (long long)it.kvh * p.s_head;
+            if (p.new_k != nullptr) {
+                // fused append: the partition that owns the new row stores it
+                // (every head chunk its own identical copy) before its copies
+                const int pos = __ldg(p.positions + it.b);
+                if (pos < 0 || pos / B >= p.maxb) {
+                    if (it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
+                        atomicOr(p.status, kStatusBadLength);
+                } else if (it.c == (pos < it.n ? (pos / B) / p.PB : 0)) {
+                    const int blk = __ldg(bt_row + pos / B);
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        if (lane == 0) atomicOr(p.status, kStatusBadBlock);
+                    } else {
+                        const int kv = lane >> 4;  // 16 chunks of 16 bytes per 128-element row
+                        const int ci = lane & 15;
+                        const long long src = ((long long)it.b * p.Hkv + it.kvh) * 256 + ci * 16;
+                        const long long off =
+                            (long long)blk * p.s_blk + tile0 + (long long)(pos % B) * 128;
+                        const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+                            static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src));
+                        unsigned short* dst = const_cast<unsigned short*>(
+                            reinterpret_cast<const unsigned short*>(kv ? p.v_base : p.k_base)) +
+                            off;
+                        reinterpret_cast<uint4*>(dst)[ci] = val;
+                        fence_proxy_async_global();
+                    }
+                }
+                __syncwarp();
+            }
+            if (it.ntiles == 0) continue;
+
+            // q of the item's G heads -> K-major swizzled tile [half][G][128 B]
+            if (qi >= 2 &&
+                !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + (qi & 1)),
+                                                 ((qi >> 1) - 1) & 1, abort_all, p.status))) {
+                aborted = true;
+                break;
+            }
+            {
+                const uint32_t qbuf = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
+                const uint4* qsrc = reinterpret_cast<const uint4*>(
+                    static_cast<const unsigned short*>(p.q) +
+                    ((long long)it.b * p.H + it.hbase) * 128);
+#pragma unroll
+                for (int i = lane; i < G * 16; i += 32) {
+                    const int g = i >> 4, c16 = i & 15;
+                    cp_async16(qbuf + (c16 >> 3) * (G * 128) + sw128(g, c16), qsrc + i);
+                }
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8 * (C::Q_FULL + (qi & 1)));
+            }
+
+            // 128-token K / V tiles: lane r < 8 walks box r (16 rows) of the tile
+            for (int i = 0; i < it.ntiles; ++i, ++kt) {
+                const int stage = kt % C::ST;
+                const int use = kt / C::ST;
+                const int tok = it.t0 + i * C::TT + 16 * lane;
+                bool valid = false;
+                int blk = 0;
+                if (lane < C::NBOX && tok < it.t1) {
+                    blk = __ldg(bt_row + tok / B);
+                    valid = true;
+                }
+                // (every lane waits and votes: the warp leaves the loop together)
+                if (use > 0 && !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::KV_EMPTY + stage),
+                                                                (use - 1) & 1, abort_all,
+                                                                p.status))) {
+                    aborted = true;
+                    break;
+                }
+                const bool bad = valid && (blk < 0 || blk >= p.num_blocks);
+                valid = valid && !bad;
+                const unsigned vmask = __ballot_sync(kFullMask, valid);
+                const unsigned bmask = __ballot_sync(kFullMask, bad);
+                const uint32_t fb = bar0 + 8 * (C::KV_FULL + stage);
+                if (lane == 0) {
+                    if (bmask) atomicOr(p.status, kStatusBadBlock);
+                    meta[stage] = (int)bmask;
+                    mbar_arrive_expect_tx(fb, (uint32_t)__popc(vmask) * 4u * 2048u);
+                }
+                __syncwarp();
+                if (valid) {
+                    const int row0 = tok % B;
+                    const int o2 = p.tma_slot_blk == 2 ? blk
+                                   : (p.tma_slot_layer == 2 ? p.layer : it.kvh);
+                    const int o3 = p.tma_slot_blk == 3 ? blk
+                                   : (p.tma_slot_layer == 3 ? p.layer : it.kvh);
+                    const int o4 = p.tma_slot_blk == 4 ? blk
+                                   : (p.tma_slot_layer == 4 ? p.layer : it.kvh);
+                    const uint32_t dst = sbase + stage * C::STAGE + lane * 2048;
+                    tma_load_5d(dst, &tmk, fb, 0, row0, o2, o3, o4, policy);
+                    tma_load_5d(dst + C::HALF, &tmk, fb, 64, row0, o2, o3, o4, policy);
+                    tma_load_5d(dst + C::KV_TILE, &tmv, fb, 0, row0, o2, o3, o4, policy);
+                    tma_load_5d(dst + C::KV_TILE + C::HALF, &tmv, fb, 64, row0, o2, o3, o4,
+                                policy);
+                }
+            }
+            if (!aborted) ++qi;
+        }
+        if (aborted) {
+            // copies still in flight land before the CTA can exit
+            for (int k = kt > C::ST ? kt - C::ST : 0; k < kt; ++k)
+                (void)mbar_wait_bounded(bar0 + 8 * (C::KV_FULL + k % C::ST), (k / C::ST) & 1);
+        }
+    } else if (warp == 1) {
+        // ============================================ MMA issuer (warp 1, lane 0)
+        if (lane == 0) {
+            // Two cursors: S = K Q^T of tile kt_q (as soon as its K / V and q are
+            // in and an S buffer is free: at most two tiles ahead of P V) and
+            // O^T += V^T [P_hi | P_lo] of tile kt_pv (as soon as its P is
+            // written).  Polled in one loop, so neither waits behind the other:
+            // the last P V of an item does not wait for the next item's data.
+            constexpr uint32_t IDQ = umma_idesc_bf16(128, G, 0, 0);
+            constexpr uint32_t IDP = umma_idesc_bf16(128, C::PW, 1, 1);
+            int idx_q = blockIdx.x;   // next item to look at
+            int tiles_left = 0;       // tiles of the current item still without S
+            int i_q = 0, qi = -1;     // tile within the item; q buffer use of the item
+            bool q_ready = false, done_q = false;
+            int kt_q = 0, kt_pv = 0;
+            unsigned first_bits = 0;  // bit (tile & 1): the tile is its item's first
+            unsigned long long idle_since = 0;
+            while (true) {
+                bool progressed = false;
+                if (kt_pv < kt_q &&
+                    mbar_test(bar0 + 8 * (C::P_FULL + (kt_pv & 1)), (kt_pv >> 1) & 1)) {
+                    tc_fence_after();
+                    const int stage = kt_pv % C::ST;
+                    const bool first = (first_bits >> (kt_pv & 1)) & 1u;
+                    const uint32_t pbuf = sbase + stage * C::STAGE;
+                    const uint32_t vt = pbuf + C::KV_TILE;
+#pragma unroll
+                    for (int k = 0; k < C::TT / 16; ++k)
+                        umma_bf16(tmem + C::O_COL, umma_desc_sw128(vt + k * 2048, C::HALF, 1024),
+                                  umma_desc_sw128(pbuf + k * 2048, C::HALF, 1024), IDP,
+                                  (k > 0 || !first) ? 1u : 0u);
+                    umma_commit(bar0 + 8 * (C::PV_DONE + (kt_pv & 1)));
+                    umma_commit(bar0 + 8 * (C::KV_EMPTY + stage));
+                    ++kt_pv;
+                    progressed = true;
+                }
+                if (!done_q && kt_q < kt_pv + 2) {
+                    while (tiles_left == 0 && idx_q < total_items) {
+                        UItem it;
+                        const bool live = umma_item<B, G>(p, idx_q, it);
+                        idx_q += gridDim.x;
+                        if (live && it.ntiles > 0) {
+                            tiles_left = it.ntiles;
+                            i_q = 0;
+                            ++qi;
+                            q_ready = false;
+                        }
+                    }
+                    if (tiles_left == 0) {
+                        done_q = true;
+                    } else {
+                        if (!q_ready)
+                            q_ready = mbar_test(bar0 + 8 * (C::Q_FULL + (qi & 1)), (qi >> 1) & 1);
+                        const int stage = kt_q % C::ST;
+                        if (q_ready &&
+                            mbar_test(bar0 + 8 * (C::KV_FULL + stage), (kt_q / C::ST) & 1)) {
+                            tc_fence_after();
+                            const uint32_t ktile = sbase + stage * C::STAGE;
+                            const uint32_t qb = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const int h = k >> 2, kk = k & 3;
+                                umma_bf16(tmem + (kt_q & 1) * G,
+                                          umma_desc_sw128(ktile + h * C::HALF + kk * 32, 0, 1024),
+                                          umma_desc_sw128(qb + h * (G * 128) + kk * 32, 0, 1024),
+                                          IDQ, k > 0 ? 1u : 0u);
+                            }
+                            umma_commit(bar0 + 8 * (C::S_FULL + (kt_q & 1)));
+                            first_bits = (first_bits & ~(1u << (kt_q & 1))) |
+                                         ((i_q == 0 ? 1u : 0u) << (kt_q & 1));
+                            ++i_q;
+                            if (--tiles_left == 0) umma_commit(bar0 + 8 * (C::Q_EMPTY + (qi & 1)));
+                            ++kt_q;
+                            progressed = true;
+                        }
+                    }
+                }
+                if (done_q && kt_pv == kt_q) break;
+                if (progressed) {
+                    idle_since = 0;
+                    continue;
+                }
+                if (*abort_all) break;
+                const unsigned long long now = globaltimer_ns();
+                if (idle_since == 0) {
+                    idle_since = now;
+                } else if (now - idle_since > kWaitLimitNs) {
+                    *abort_all = 1;
+                    atomicOr(p.status, kStatusTimeout);
+                    break;
+                }
+            }
+            // every MMA issued so far completes before TMEM is released
+            umma_commit(bar0 + 8 * C::FINAL);
+            (void)mbar_wait_bounded(bar0 + 8 * C::FINAL, 0);
+        }
+        __syncwarp();
+    } else {
+        // ============================== softmax (warps 2 .. 2 + NSW - 1)
+        // Warp w works on TMEM lane quarter w % 4 (token / head-dim rows
+        // 32 * (w % 4) + lane) and on heads [h0, h0 + HG).
+        // The head parts are independent (own barriers, heads, sums and
+        // maxima); they meet only at P_FULL.
+        constexpr int HG = C::HG;
+        const int part = (warp - 2) >> 2;
+        const int qd = warp & 3;
+        const int sp = ((warp - 2) & 3) * 32 + lane;  // thread within the part, 0 .. 127
+        const int h0 = part * HG;
+        const int r = qd * 32 + lane;            // token of the tile (S) / head-dim element (O)
+        const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+        int kt = 0;
+        bool stop = false;
+        // A failed wait only marks this thread; the softmax threads decide to
+        // stop together at the next barrier reduction, so none is left waiting
+        // at a named barrier the others have abandoned.
+        bool failed = false;
+        float lp[HG];  // this thread's share of the softmax denominators
+        for (int idx = blockIdx.x; idx < total_items && !stop; idx += gridDim.x) {
+            UItem it;
+            if (!umma_item<B, G>(p, idx, it)) continue;
+            const long long head0 = (long long)it.b * p.H + it.hbase + h0;
+            if (it.ntiles == 0) {  // empty context: output 0 (one partition)
+#pragma unroll
+                for (int g = 0; g < HG; ++g) p.out[(head0 + g) * 128 + r] = 0.f;
+                continue;
+            }
+#pragma unroll
+            for (int g = 0; g < HG; ++g) lp[g] = 0.f;
+            for (int i = 0; i < it.ntiles; ++i, ++kt) {
+                const int stage = kt % C::ST;
+                bool ok = umma_wait(bar0 + 8 * (C::S_FULL + (kt & 1)), (kt >> 1) & 1, abort_all,
+                                    p.status);
+                ok = ok && umma_wait(bar0 + 8 * (C::KV_FULL + stage), (kt / C::ST) & 1,
+                                     abort_all, p.status);
+                failed = failed || !ok;
+                __syncwarp();
+                tc_fence_after();
+                float x[HG];
+                {
+                    uint32_t v[HG];
+                    tmem_ld_cols<HG>(trow + (kt & 1) * G + h0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < HG; ++j) x[j] = __uint_as_float(v[j]);
+                }
+                const int tok = it.t0 + i * C::TT + r;
+                const bool valid = tok < it.t1 && !((meta[stage] >> (r >> 4)) & 1);
+                float mreg[HG];
+#pragma unroll
+                for (int g = 0; g < HG; g += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(m_sh + h0 + g);
+                    mreg[g] = m4.x;
+                    mreg[g + 1] = m4.y;
+                    mreg[g + 2] = m4.z;
+                    mreg[g + 3] = m4.w;
+                }
+                bool need = (i == 0);
+#pragma unroll
+                for (int g = 0; g < HG; ++g) {
+                    x[g] = valid ? x[g] * p.qscale : -INFINITY;
+                    need |= x[g] > mreg[g] + 8.f;
+                }
+                if (part_bar_or(part, need | failed)) {
+                    if (part_bar_or(part, failed)) {
+                        stop = true;
+                        break;
+                    }
+                    // raise the running max to this tile's max (per head)
+#pragma unroll
+                    for (int g = 0; g < HG; ++g) {
+                        float v = x[g];
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1)
+                            v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
+                        if (lane == 0) red[qd * G + h0 + g] = v;
+                    }
+                    part_bar(part);
+                    if (sp < HG) {
+                        const int h = h0 + sp;
+                        const float mt = fmaxf(fmaxf(red[h], red[G + h]),
+                                               fmaxf(red[2 * G + h], red[3 * G + h]));
+                        const float old = (i == 0) ? -INFINITY : m_sh[h];
+                        const float mn = fmaxf(old, mt);
+                        a_sh[h] = (old == -INFINITY) ? 0.f : exp2f(old - mn);
+                        m_sh[h] = mn;
+                    }
+                    part_bar(part);
+#pragma unroll
+                    for (int g = 0; g < HG; ++g) {
+                        lp[g] *= a_sh[h0 + g];
+                        mreg[g] = m_sh[h0 + g];
+                    }
+                    if (i > 0) {
+                        // O (this item's earlier tiles) scaled by the same factors
+                        if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)),
+                                       ((kt - 1) >> 1) & 1, abort_all, p.status))
+                            failed = true;
+                        __syncwarp();
+                        tc_fence_after();
+#pragma unroll
+                        for (int part = 0; part < 2; ++part) {   // hi heads, lo heads
+                            uint32_t v[HG];
+                            const uint32_t col = trow + C::O_COL + part * G + h0;
+                            tmem_ld_cols<HG>(col, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int j = 0; j < HG; ++j)
+                                v[j] = __float_as_uint(__uint_as_float(v[j]) * a_sh[h0 + j]);
+                            tmem_st_cols<HG>(col, v);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                // p = 2^(x - m) for this thread's token and heads (a head whose
+                // max is still -inf has only -inf scores here: p = 0)
+#pragma unroll
+                for (int g = 0; g < HG; ++g) {
+                    const float mm = mreg[g] == -INFINITY ? 0.f : mreg[g];
+                    const float pv = exp2f(x[g] - mm);
+                    lp[g] += pv;
+                    x[g] = pv;
+                }
+                if (!valid && h0 == 0) {
+                    // rows past the context (or of a bad block) hold stale or
+                    // foreign values: zero V so that 0 * V stays 0
+                    unsigned char* vrow = smem + stage * C::STAGE + C::KV_TILE + r * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        *reinterpret_cast<uint4*>(vrow + j * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vrow + C::HALF + j * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                }
+                // P row (MN-major, 64-column blocks) into the K half of this
+                // tile's stage, which S = K Q^T has finished reading: hi heads,
+                // then lo heads, then zeros up to 64 columns
+                unsigned char* pbuf = smem + stage * C::STAGE;
+                if (C::PW > 2 * G && h0 == 0) {
+#pragma unroll
+                    for (int j = (2 * G) / 8; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(pbuf + sw128(r, j)) = make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int g8 = 0; g8 < HG; g8 += 8) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float a = x[g8 + 2 * j], b = x[g8 + 2 * j + 1];
+                        hi[j] = pack_bf16x2(a, b);
+                        const float ha = __uint_as_float(hi[j] << 16);
+                        const float hb = __uint_as_float(hi[j] & 0xffff0000u);
+                        lo[j] = pack_bf16x2(a - ha, b - hb);
+                    }
+                    const int nh = h0 + g8, nl = G + h0 + g8;  // element index in the row
+                    *reinterpret_cast<uint4*>(pbuf + (nh >> 6) * C::HALF +
+                                              sw128(r, (nh & 63) >> 3)) =
+                        make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4*>(pbuf + (nl >> 6) * C::HALF +
+                                              sw128(r, (nl & 63) >> 3)) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar0 + 8 * (C::P_FULL + (kt & 1)));
+            }
+            if (stop) break;
+
+            // ---- item epilogue: denominators, O = O_hi + O_lo, output ----
+#pragma unroll
+            for (int g = 0; g < HG; ++g) {
+                float v = lp[g];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
+                if (lane == 0) red[qd * G + h0 + g] = v;
+            }
+            if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1,
+                           abort_all, p.status))
+                failed = true;
+            if (part_bar_or(part, failed)) {
+                stop = true;
+                break;
+            }
+            if (sp < HG) {
+                const int h = h0 + sp;
+                a_sh[h] = (red[h] + red[G + h]) + (red[2 * G + h] + red[3 * G + h]);
+            }
+            part_bar(part);
+            __syncwarp();
+            tc_fence_after();
+            {
+                uint32_t vh[HG], vl[HG];
+                tmem_ld_cols<HG>(trow + C::O_COL + h0, vh);
+                tmem_ld_cols<HG>(trow + C::O_COL + G + h0, vl);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < HG; ++g) {
+                    const float o = __uint_as_float(vh[g]) + __uint_as_float(vl[g]);
+                    const float L = a_sh[h0 + g];
+                    if (it.nparts == 1) {
+                        p.out[(head0 + g) * 128 + r] = L > 0.f ? o / L : 0.f;
+                    } else {
+                        const long long slot = (head0 + g) * p.Cmax + it.c;
+                        p.part_o[slot * 128 + r] = o;
+                        if (r == 0) {
+                            p.part_ml[slot * 2 + 0] = m_sh[h0 + g];
+                            p.part_ml[slot * 2 + 1] = L;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace pa

@@ -110,6 +110,14 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, i
 cudaError_t encode_pool_tmaps(const PoolGeom& g, void* tmaps, int* slot_blk, int* slot_layer,
                               int* slot_head);
 
+// tcgen05 kernel for bf16 pools, head_dim 128, groups that are multiples of
+// 16 (chunks of 64, 32 or 16 heads; decode_umma_chunk gives the chunk, 0 if
+// none); persistent, one CTA per SM.
+bool decode_umma_supported(int D, int B, int G);
+int decode_umma_chunk(int G);
+cudaError_t launch_decode_umma(const DecodeParams& p, const void* tmaps, int B, int G,
+                               cudaStream_t s);
+
 cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s);
 cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);

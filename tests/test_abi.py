@@ -212,10 +212,10 @@ def test_decode_kernel_choice_checks(pa_lib):
     h = _pool(pa_lib)
     try:
         for kind in (pa_lib.PA_DECODE_AUTO, pa_lib.PA_DECODE_CUDA_CORES,
-                     pa_lib.PA_DECODE_TENSOR_CORES):
+                     pa_lib.PA_DECODE_TENSOR_CORES, pa_lib.PA_DECODE_TCGEN05):
             pa_lib.pa_pool_set_decode_kernel(h, kind)
         with pytest.raises(pa_lib.PagedAttnError) as e:
-            pa_lib.pa_pool_set_decode_kernel(h, 3)
+            pa_lib.pa_pool_set_decode_kernel(h, 4)
         assert e.value.code == pa_lib.PA_ERR_INVALID_ARG
     finally:
         pa_lib.pa_pool_destroy(h)

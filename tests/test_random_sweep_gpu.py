@@ -1,7 +1,8 @@
 """Seeded randomized parity sweep on the GPU: random shapes (dtype, head_dim,
-block size, GQA group 1-8, 16, 24, 32, KV heads, batch, ragged lengths with 0 / 1 / block
-multiples), random layer, partition size, pool layout and decode kernel, plus
-the fused append path -- each case against the oracle on the same inputs."""
+block size, GQA group 1-8, 16, 24, 32, 48, 64, KV heads, batch, ragged lengths with 0 / 1 /
+block multiples), random layer, partition size, pool layout and decode kernel (CUDA cores,
+mma.sync, tcgen05), plus the fused append path -- each case against the oracle on the same
+inputs."""
 import numpy as np
 import pytest
 import torch
@@ -23,7 +24,7 @@ def _case(i):
     Bs = int(rng.choice([16, 32]))
     Hkv = int(rng.choice([1, 2, 4]))
     G = int(rng.choice([1, 2, 4, 8])) if dtype == "f32" else \
-        int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 16, 24, 32]))
+        int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 16, 24, 32, 48, 64]))
     L = int(rng.integers(1, 4))
     batch = int(rng.integers(1, 10))
     special = [0, 1, Bs - 1, Bs, Bs + 1, 2 * Bs]
@@ -68,6 +69,10 @@ def test_random_case_matches_oracle(cuda_device, i):
         kinds = [B.PA_DECODE_AUTO]
         if dtype == "bf16" and G in (1, 2, 4, 8):
             kinds.append(B.PA_DECODE_CUDA_CORES)
+        if dtype == "bf16":
+            kinds.append(B.PA_DECODE_TENSOR_CORES)
+        if dtype == "bf16" and D == 128 and G % 16 == 0:
+            kinds.append(B.PA_DECODE_TCGEN05)
         layer = int(rng.integers(0, L))
         pb = int(rng.choice([0, 1, 2, 3, wl.max_blocks]))
         bt = torch.from_numpy(wl.block_tables).to(cuda_device)
@@ -75,10 +80,10 @@ def test_random_case_matches_oracle(cuda_device, i):
         qd = q.to(cuda_device)
         ref = oracle.decode_attention(W.as_oracle_array(q), W.as_oracle_array(fused), layer,
                                       wl.block_tables, wl.context_lens, H, wl.scale)
-        need = B.pa_decode_workspace_size(h, wl.batch, H, wl.max_blocks, pb)
-        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=cuda_device)
         for kind in kinds:
             B.pa_pool_set_decode_kernel(h, kind)
+            need = B.pa_decode_workspace_size(h, wl.batch, H, wl.max_blocks, pb)
+            ws = torch.empty(max(need, 1), dtype=torch.uint8, device=cuda_device)
             out = torch.full((wl.batch, H, D), float("nan"), device=cuda_device)
             B.pa_decode_attention_partitioned(out, qd, h, layer, bt, wl.max_blocks, ln, wl.batch,
                                               Bs, H, Hkv, D, wl.scale, pb, ws, need)
@@ -92,6 +97,8 @@ def test_random_case_matches_oracle(cuda_device, i):
                                                   wl.batch, Bs, H, Hkv, D, wl.scale, pb, ws, need)
             assert e.value.code == B.PA_ERR_UNSUPPORTED
         B.pa_pool_set_decode_kernel(h, B.PA_DECODE_AUTO)
+        need = B.pa_decode_workspace_size(h, wl.batch, H, wl.max_blocks, pb)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=cuda_device)
 
         # fused append at position n (a new block where n % B == 0), decode over n + 1
         k, v = W.make_new_tokens(wl, 1)
