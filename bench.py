@@ -61,14 +61,16 @@ def decode_flops(wl) -> int:
 
 
 # DRAM bytes (read + write) of one pa_decode_attention call on this workload:
-# pa_decode_mma_kernel (ncu --set full) + pa_combine_kernel (ncu dram metrics),
-# see profiles/; valid only for the kernel sources they were taken from.
+# pa_decode_mma_kernel (ncu --set full: 2,231,171,072 read + 6,196,736 written)
+# + pa_combine_kernel (ncu dram metrics: 9,851,392 read, 0 written), see
+# profiles/; valid only for the sources they were taken from (the kernels, the
+# shared device code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231161000 + 6421760 + 9851904,
-    "sources_sha256": "70686596f0b413de2000617cf15a12daca31341108ec92c37fa719edaf846ed2",
+    "bytes_per_launch": 2231171072 + 6196736 + 9851392,
+    "sources_sha256": "2f90877281f8696e877e1a4a1fd9ca89fecce0663ec39d201ceba26bb1cf338a",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
-                  "pa_internal.h"]
+                  "pa_internal.h", "pa_api.cpp"]
 
 
 def decode_sources_sha256() -> str:
@@ -278,10 +280,12 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     wl = W.named(args.workload)
+    if args.num_heads > 0:     # same lengths and tables; another query-head count
+        wl.num_heads = args.num_heads
     if args.kv_heads > 0:      # same lengths, tables and query heads; another group size
-        if wl.num_heads % args.kv_heads:
-            raise SystemExit("--kv-heads must divide the workload's query heads")
         wl.num_kv_heads = args.kv_heads
+    if wl.num_heads % wl.num_kv_heads:
+        raise SystemExit("the KV heads must divide the query heads")
     if args.pool_layers > 0:   # smaller pool (same lengths/tables) for profiler captures
         wl.num_layers = min(args.pool_layers, wl.num_layers)
     L = wl.num_layers if args.layers <= 0 else min(args.layers, wl.num_layers)
@@ -545,7 +549,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "decode_tokens_per_s": wl.batch * steps * world / (total_ms / 1e3),
         "roofline": {"bound": "hbm", "kernel": "pa_decode_attention (decode + combine)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": decode_traffic(),
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     # the captured counters belong to the default workload only
+                     "traffic": (decode_traffic() if args.workload == WORKLOAD_CFG and
+                                 args.kv_heads <= 0 and args.num_heads <= 0 else None),
                      "traffic_kernel": "pa_decode_mma_kernel + pa_combine_kernel, ncu dram "
                                        "read+write per call",
                      "algorithmic_bytes_per_call": per_call,
@@ -810,6 +817,9 @@ def main():
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="override the workload's KV heads (query heads unchanged): group-size "
                          "sweeps, e.g. --kv-heads 1 for one KV head per 32 query heads")
+    ap.add_argument("--num-heads", type=int, default=0,
+                    help="override the workload's query heads (with --kv-heads: any group, e.g. "
+                         "--num-heads 64 --kv-heads 1 for the tcgen05 kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--pool-layers", type=int, default=0,
