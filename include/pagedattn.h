@@ -249,7 +249,8 @@ PA_API int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
  *   out           device fp32 [batch, num_heads, head_dim], 16-byte aligned.
  *   q             device [batch, num_heads, head_dim] of the pool dtype, 16-byte aligned.
  *   block_tables  device int32 [batch, max_blocks_per_seq]; entries past
- *                 ceil(n / B) are never read (pad with -1).
+ *                 ceil(n / B) do not affect the result (a kernel may load
+ *                 them with the rest of its row; pad with -1).
  *   context_lens  device int32 [batch], 0 <= n <= max_blocks_per_seq * B.
  *   block_size, num_kv_heads, head_dim must equal the pool's; num_heads must be
  *   a multiple of num_kv_heads.

@@ -170,6 +170,13 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     const int kvh = idx % p.Hkv;
     const int b = idx / p.Hkv;
 
+    // The first 32 block ids of this warp's share of the partition depend only
+    // on the partition index (the table row holds maxb entries): their load
+    // overlaps the length's instead of waiting for it.
+    const int* bt_row = p.bt + (long long)b * p.maxb;
+    const int k_first = c * p.PB + warp + lane * NW;
+    const int id_first = k_first < p.maxb ? __ldg(bt_row + k_first) : -1;
+
     int n = __ldg(p.lens + b);
     if (n < 0 || n > p.maxb * B) {
         if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
@@ -205,7 +212,6 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
         U = (nk - 1) * C::SPB + (rows_last + C::R - 1) / C::R;
     }
 
-    const int* bt_row = p.bt + (long long)b * p.maxb;
     // This CTA's tiles: element offset of (block 0, layer, kvh) from each base.
     const long long tile0 = p.tile_off + (long long)kvh * p.s_head;
     const T* kpool = reinterpret_cast<const T*>(p.k_base) + tile0;
@@ -243,7 +249,7 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
 
     // Block ids of this warp's blocks kbase..kbase+31, one per lane.
     int kbase = 0;
-    int myid = (lane < nk) ? __ldg(bt_row + pb0 + warp + lane * NW) : -1;
+    int myid = (lane < nk) ? id_first : -1;
 
     auto issue = [&](int u) {
         const int k = u / C::SPB;

@@ -94,6 +94,13 @@ __global__ void __launch_bounds__(NW * 32)
     const int b = idx / p.Hkv;
     const int hbase = kvh * p.gsize + hc * G;  // first query head of this CTA in the sequence
 
+    // The first 32 block ids of this warp's share of the partition depend only
+    // on the partition index (the table row holds maxb entries): their load
+    // overlaps the length's instead of waiting for it.
+    const int* bt_row = p.bt + (long long)b * p.maxb;
+    const int k_first = c * p.PB + warp + lane * NW;
+    const int id_first = k_first < p.maxb ? __ldg(bt_row + k_first) : -1;
+
     int n = __ldg(p.lens + b);
     if (n < 0 || n > p.maxb * B) {
         if (c == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
@@ -135,7 +142,6 @@ __global__ void __launch_bounds__(NW * 32)
         U = (nk - 1) * C::SPB + (rows_last + C::R - 1) / C::R;
     }
 
-    const int* bt_row = p.bt + (long long)b * p.maxb;
     const long long tile0 = p.tile_off + (long long)kvh * p.s_head;
 
     // fused append (see pa_decode_kernel): store the new row before any TMA read
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(NW * 32)
 
     const uint64_t policy = l2_policy_evict_first();
     int kbase = 0;
-    int myid = (lane < nk) ? __ldg(bt_row + pb0 + warp + lane * NW) : -1;
+    int myid = (lane < nk) ? id_first : -1;
 
     auto issue = [&](int u) {
         const int k = u / C::SPB;
