@@ -61,13 +61,13 @@ def decode_flops(wl) -> int:
 
 
 # DRAM bytes (read + write) of one pa_decode_attention call on this workload:
-# pa_decode_mma_kernel (ncu --set full: 2,231,171,072 read + 6,196,736 written)
+# pa_decode_mma_kernel (ncu --set full: 2,231,293,440 read + 6,367,488 written)
 # + pa_combine_kernel (ncu dram metrics: 9,851,392 read, 0 written), see
 # profiles/; valid only for the sources they were taken from (the kernels, the
 # shared device code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231171072 + 6196736 + 9851392,
-    "sources_sha256": "2f90877281f8696e877e1a4a1fd9ca89fecce0663ec39d201ceba26bb1cf338a",
+    "bytes_per_launch": 2231293440 + 6367488 + 9851392,
+    "sources_sha256": "dd165eb89f6ba313d48afdda5ab5288ff346d85ed7ed98221f305842650e8716",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h", "pa_api.cpp"]
