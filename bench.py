@@ -56,21 +56,28 @@ def decode_bytes(wl) -> int:
     return kv + qb + ob + tb + wl.batch * 4
 
 
+def append_bytes(wl) -> int:
+    """Algorithmic bytes of one layer's KV append: the new K and V rows read and
+    written, and the positions."""
+    return 2 * 2 * wl.batch * wl.num_kv_heads * wl.head_dim * wl.elem_bytes + wl.batch * 4
+
+
 def decode_flops(wl) -> int:
     return int(wl.context_lens.astype(np.int64).sum()) * 4 * wl.num_heads * wl.head_dim
 
 
-# DRAM bytes (read + write) of one pa_decode_attention call on this workload:
-# pa_decode_mma_kernel (ncu --set full: 2,231,293,440 read + 6,367,488 written)
-# + pa_combine_kernel (ncu dram metrics: 9,851,392 read, 0 written), see
+# DRAM bytes (read + write) of one layer's pa_write_kv_and_decode call on this
+# workload: pa_decode_mma_kernel with the fused append (ncu --set full:
+# 2,231,254,784 read + 6,523,904 written) + pa_combine_kernel (ncu dram
+# metrics: 9,852,160 read, 0 written), see
 # profiles/; valid only for the sources they were taken from (the kernels, the
 # shared device code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231293440 + 6367488 + 9851392,
-    "sources_sha256": "dd165eb89f6ba313d48afdda5ab5288ff346d85ed7ed98221f305842650e8716",
+    "bytes_per_launch": 2231254784 + 6523904 + 9852160,
+    "sources_sha256": "ca855aec1ee1e90be12bec108b19015d4cc2389cdd1eed336d00b53f44c27a0b",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
-                  "pa_internal.h", "pa_api.cpp"]
+                  "pa_internal.h", "pa_api.cpp", "pa_fused_append.cuh"]
 
 
 def decode_sources_sha256() -> str:
@@ -524,11 +531,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         B.pa_pool_destroy(h)
         return
     per_call = decode_bytes(wl)
+    # the timed launch of a layer: the fused call also moves the appended rows
+    launch_bytes = per_call + (append_bytes(wl) if args.fused else 0)
     steps = args.steps
     value = per_call * L * steps * world / (total_ms / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
     call_avg_ms = sum(call_ms) / len(call_ms)
-    achieved = per_call / (call_avg_ms / 1e3) / 1e9
+    achieved = launch_bytes / (call_avg_ms / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
@@ -541,21 +550,26 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             "context_lens": f"seed {wl.seed}, min {wl.context_lens.min()}, max "
                             f"{wl.context_lens.max()}, mean {wl.context_lens.mean():.0f}",
             "cuda_graph": use_graph,
+            "append": ("fused into the decode launch (pa_write_kv_and_decode)" if args.fused
+                       else "separate pa_write_kv launch before each decode"),
             "pool_gb": round(wl.pool_bytes() / 1e9, 1), "partition_blocks": pb,
             "l2": l2_note(wl, L),
             "parallelism": f"replicas x{world}",
         },
         "pct_hbm_peak": 100.0 * value / peak,
         "decode_tokens_per_s": wl.batch * steps * world / (total_ms / 1e3),
-        "roofline": {"bound": "hbm", "kernel": "pa_decode_attention (decode + combine)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("pa_write_kv_and_decode (append + decode + combine)" if args.fused
+                                else "pa_decode_attention (decode + combine)"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      # the captured counters belong to the default workload only
                      "traffic": (decode_traffic() if args.workload == WORKLOAD_CFG and
-                                 args.kv_heads <= 0 and args.num_heads <= 0 else None),
-                     "traffic_kernel": "pa_decode_mma_kernel + pa_combine_kernel, ncu dram "
-                                       "read+write per call",
-                     "algorithmic_bytes_per_call": per_call,
+                                 args.kv_heads <= 0 and args.num_heads <= 0 and args.fused
+                                 else None),
+                     "traffic_kernel": "pa_decode_mma_kernel (with the fused append) + "
+                                       "pa_combine_kernel, ncu dram read+write per call",
+                     "algorithmic_bytes_per_call": launch_bytes,
                      "avg_call_ms": call_avg_ms,
                      "timing": ("CUDA events around every decode call, recorded as event nodes "
                                 "of a graph replay of the same K steps"
@@ -812,8 +826,9 @@ def main():
     ap.add_argument("--ref-seqs", type=int, default=96, help="sequences per reference step")
     ap.add_argument("--device-alloc", action="store_true",
                     help="with --row loop: free stack on the device, one CUDA graph per run")
-    ap.add_argument("--fused", action="store_true",
-                    help="step mode: pa_write_kv_and_decode instead of two calls per layer")
+    ap.add_argument("--separate", action="store_true",
+                    help="step mode: pa_write_kv then pa_decode_attention per layer instead of "
+                         "the fused pa_write_kv_and_decode (the default)")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="override the workload's KV heads (query heads unchanged): group-size "
                          "sweeps, e.g. --kv-heads 1 for one KV head per 32 query heads")
@@ -826,6 +841,7 @@ def main():
                     help="build the pool with this many layers (0 = the workload's 32); "
                          "for small profiler captures, not for reported numbers")
     args = ap.parse_args()
+    args.fused = not args.separate
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
 

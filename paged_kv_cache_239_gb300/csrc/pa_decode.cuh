@@ -32,6 +32,7 @@
 #include <stdint.h>
 
 #include "pa_device.cuh"
+#include "pa_fused_append.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -217,33 +218,31 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     const T* kpool = reinterpret_cast<const T*>(p.k_base) + tile0;
     const T* vpool = reinterpret_cast<const T*>(p.v_base) + tile0;
 
-    // ---- fused append: the CTA whose partition holds the new token's block
+    // ---- fused append: the partition that holds the new token's block
     //      (partition 0 when the position lies past the context) stores this
-    //      KV head's new K and V rows before any bulk copy is issued. ----
+    //      KV head's new K and V rows; the warp that copies that block makes
+    //      the store, just before the copy (see pa_decode_mma_kernel). ----
+    int app_k = -1, app_blk = -1, app_pos = 0;
     if (p.new_k != nullptr) {
         const int pos = __ldg(p.positions + b);
         if (pos < 0 || pos / B >= p.maxb) {
             if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
         } else if (c == (pos < n ? (pos / B) / p.PB : 0)) {
-            constexpr int CPR = C::ROW_BYTES / 16;  // 16-byte chunks per row
-            const int blk = __ldg(bt_row + pos / B);
+            const int jb = pos / B;
+            const int blk = __ldg(bt_row + jb);
             if (blk < 0 || blk >= p.num_blocks) {
                 if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
-            } else if (threadIdx.x < 2 * CPR) {
-                const int kv = threadIdx.x / CPR;
-                const int ci = threadIdx.x % CPR;
-                const long long src = ((long long)b * p.Hkv + kvh) * C::ROW_BYTES + ci * 16;
-                const long long off = (long long)blk * p.s_blk + tile0 + (long long)(pos % B) * D;
-                const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                    static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src));
-                T* dst = const_cast<T*>(reinterpret_cast<const T*>(kv ? p.v_base : p.k_base)) +
-                         off;
-                reinterpret_cast<uint4*>(dst)[ci] = val;
-                // the stored row is read back below by the bulk-copy (async) proxy
-                fence_proxy_async_global();
+            } else if (pos < n) {
+                if (warp == (jb - pb0) % NW) {
+                    app_k = (jb - pb0) / NW;
+                    app_blk = blk;
+                    app_pos = pos;
+                }
+            } else if (warp == 0) {
+                // past the decoded context: no copy of this call needs the row
+                warp_store_new_row<C::ROW_BYTES, (int)sizeof(T)>(p, b, kvh, blk, pos, B, lane);
             }
         }
-        __syncthreads();
     }
     const uint64_t policy = l2_policy_evict_first();
 
@@ -264,6 +263,8 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
         const int row0 = sub * C::R;
         const int rows = min(C::R, n - (jb * B + row0));
         const int stage = u % S;
+        if (k == app_k && sub == 0)
+            warp_store_new_row<C::ROW_BYTES, (int)sizeof(T)>(p, b, kvh, app_blk, app_pos, B, lane);
         if (lane == 0) {
             const uint32_t bar = bars + 8 * stage;
             if (blk >= 0 && blk < p.num_blocks) {

@@ -29,6 +29,7 @@
 #include <stdint.h>
 
 #include "pa_device.cuh"
+#include "pa_fused_append.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -142,35 +143,34 @@ __global__ void __launch_bounds__(NW * 32)
         U = (nk - 1) * C::SPB + (rows_last + C::R - 1) / C::R;
     }
 
-    const long long tile0 = p.tile_off + (long long)kvh * p.s_head;
 
-    // fused append (see pa_decode_kernel): store the new row before any TMA read
+    // Fused append.  The partition that holds the new row's block (partition
+    // 0 when the position lies past the context) stores it; every head chunk
+    // of that partition stores the (identical) row itself.  The store is made
+    // by the warp that copies that block, just before the copy, so its latency
+    // hides behind the warp's earlier blocks and no other warp waits.
+    int app_k = -1, app_blk = -1, app_pos = 0;
     if (p.new_k != nullptr) {
         const int pos = __ldg(p.positions + b);
         if (pos < 0 || pos / B >= p.maxb) {
             if (c == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0)
                 atomicOr(p.status, kStatusBadLength);
         } else if (c == (pos < n ? (pos / B) / p.PB : 0)) {
-            // every head chunk of the owning partition stores the (identical) row
-            // itself: its own store is then ordered before its own bulk copies
-            constexpr int CPR = D * 2 / 16;
-            const int blk = __ldg(bt_row + pos / B);
+            const int jb = pos / B;
+            const int blk = __ldg(bt_row + jb);
             if (blk < 0 || blk >= p.num_blocks) {
                 if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
-            } else if (threadIdx.x < 2 * CPR) {
-                const int kv = threadIdx.x / CPR;
-                const int ci = threadIdx.x % CPR;
-                const long long src = ((long long)b * p.Hkv + kvh) * (D * 2) + ci * 16;
-                const long long off = (long long)blk * p.s_blk + tile0 + (long long)(pos % B) * D;
-                const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                    static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src));
-                unsigned short* dst = const_cast<unsigned short*>(
-                    reinterpret_cast<const unsigned short*>(kv ? p.v_base : p.k_base)) + off;
-                reinterpret_cast<uint4*>(dst)[ci] = val;
-                fence_proxy_async_global();
+            } else if (pos < n) {
+                if (warp == (jb - pb0) % NW) {
+                    app_k = (jb - pb0) / NW;
+                    app_blk = blk;
+                    app_pos = pos;
+                }
+            } else if (warp == 0) {
+                // past the decoded context: no copy of this call needs the row
+                warp_store_new_row<D * 2, 2>(p, b, kvh, blk, pos, B, lane);
             }
         }
-        __syncthreads();
     }
 
     const uint64_t policy = l2_policy_evict_first();
@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(NW * 32)
         const int row0 = sub * C::R;
         const int rows = min(C::R, n - (jb * B + row0));
         const int stage = u % S;
+        if (k == app_k && sub == 0) warp_store_new_row<D * 2, 2>(p, b, kvh, app_blk, app_pos, B, lane);
         if (lane == 0) {
             const uint32_t bar = bars + 8 * stage;
             if (blk >= 0 && blk < p.num_blocks) {
