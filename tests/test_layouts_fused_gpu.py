@@ -96,9 +96,12 @@ def test_strided_layouts_decode_append_gather(cuda_device, layout, dtype, L):
         B.pa_pool_destroy(h)
 
 
-@pytest.mark.parametrize("dtype,D,Bs,G,pb", [("bf16", 128, 16, 4, 0), ("bf16", 128, 32, 1, 2),
-                                             ("bf16", 64, 16, 8, 1), ("f32", 64, 16, 2, 3)])
-def test_fused_append_decode_matches_separate_calls(cuda_device, dtype, D, Bs, G, pb):
+@pytest.mark.parametrize("dtype,D,Bs,G,pb,kind", [("bf16", 128, 16, 4, 0, "AUTO"),
+                                                  ("bf16", 128, 32, 1, 2, "AUTO"),
+                                                  ("bf16", 64, 16, 8, 1, "AUTO"),
+                                                  ("bf16", 128, 32, 4, 3, "CUDA_CORES"),
+                                                  ("f32", 64, 16, 2, 3, "AUTO")])
+def test_fused_append_decode_matches_separate_calls(cuda_device, dtype, D, Bs, G, pb, kind):
     Hkv = 2
     lens = [0, 1, Bs - 1, Bs, 3 * Bs, 3 * Bs + 1, 7 * Bs + 3]   # positions of the new token
     wl = W.custom("fused", dtype, 2, Hkv * G, Hkv, D, Bs, lens, seed=D + G + Bs, steps=1,
@@ -111,6 +114,7 @@ def test_fused_append_decode_matches_separate_calls(cuda_device, dtype, D, Bs, G
         if n % wl.block_size == 0:
             tables[b, n // wl.block_size] = wl.free_stack.pop()
     gp = GpuPool(wl, pool.to(cuda_device))
+    B.pa_pool_set_decode_kernel(gp.h, getattr(B, "PA_DECODE_" + kind))
     bt = torch.from_numpy(tables).to(cuda_device)
     pos = torch.from_numpy(wl.context_lens.copy()).to(cuda_device)
     lens1 = wl.context_lens + 1
@@ -132,14 +136,16 @@ def test_fused_append_decode_matches_separate_calls(cuda_device, dtype, D, Bs, G
     assert B.pa_get_status() == 0
 
 
-def test_fused_append_position_past_context(cuda_device):
+@pytest.mark.parametrize("kind", ["AUTO", "CUDA_CORES"])
+def test_fused_append_position_past_context(cuda_device, kind):
     """A position outside the decoded context is still stored (by partition 0)
-    and does not change the decode."""
+    and does not change the decode -- on the tensor-core and CUDA-core kernels."""
     wl = W.custom("past", "bf16", 1, 8, 2, 128, 16, [40, 70], seed=3, spare_blocks=2)
     pool = W.make_pool(wl)
     q = W.make_queries(wl, 1)[0]
     k, v = W.make_new_tokens(wl, 1)
     gp = GpuPool(wl, pool.to(cuda_device))
+    B.pa_pool_set_decode_kernel(gp.h, getattr(B, "PA_DECODE_" + kind))
     bt, ln = device_tables(wl, cuda_device)
     pos_h = np.array([45, 75], np.int32)                      # beyond n, inside the last block
     out = torch.empty((2, 8, 128), device=cuda_device)
