@@ -13,12 +13,17 @@ namespace pa {
 namespace {
 
 constexpr int kMmaWarps = 4;
-constexpr int kMmaStages = 2;
+// Stages per warp: a head_dim-64 stage is half the size, so four of them keep
+// the CTA at the 64 KB (three CTAs per SM) of two head_dim-128 stages.  GB300,
+// mini-infer shape (head_dim 64): 8.6 -> 7.7 us per decode call with four; four
+// at head_dim 128 (one CTA per SM) halved the MHA batch-64 throughput.
+template <int D>
+constexpr int kMmaStages = D == 64 ? 4 : 2;
 
 template <int D, int B, int G>
 cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream_t stream) {
-    using Cfg = MmaCfg<D, B, G, kMmaWarps, kMmaStages>;
-    auto kern = pa_decode_mma_kernel<D, B, G, kMmaWarps, kMmaStages>;
+    using Cfg = MmaCfg<D, B, G, kMmaWarps, kMmaStages<D>>;
+    auto kern = pa_decode_mma_kernel<D, B, G, kMmaWarps, kMmaStages<D>>;
     static std::mutex mu;
     static unsigned long long done_mask = 0;
     int dev = 0;
