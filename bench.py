@@ -68,13 +68,13 @@ def decode_flops(wl) -> int:
 
 # DRAM bytes (read + write) of one layer's pa_write_kv_and_decode call on this
 # workload: pa_decode_mma_kernel with the fused append (ncu --set full:
-# 2,231,254,784 read + 6,523,904 written) + pa_combine_kernel (ncu dram
+# 2,231,476,224 read + 6,231,296 written) + pa_combine_kernel (ncu dram
 # metrics: 9,852,160 read, 0 written), see
 # profiles/; valid only for the sources they were taken from (the kernels, the
 # shared device code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231254784 + 6523904 + 9852160,
-    "sources_sha256": "ca855aec1ee1e90be12bec108b19015d4cc2389cdd1eed336d00b53f44c27a0b",
+    "bytes_per_launch": 2231476224 + 6231296 + 9852160,
+    "sources_sha256": "cefec597a1ea571eacdf310c8353efcd72156f9bac999b81bdb74bfd85b3ae68",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h", "pa_api.cpp", "pa_fused_append.cuh"]
