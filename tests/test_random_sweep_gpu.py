@@ -14,7 +14,7 @@ from gpu_helpers import TOL, max_abs_err
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 56
+N_CASES = 112
 
 
 def _case(i):
