@@ -15,6 +15,10 @@ import torch
 from . import binding as B
 
 
+_DECODE_KERNELS = {"auto": B.PA_DECODE_AUTO, "cuda_cores": B.PA_DECODE_CUDA_CORES,
+                   "tensor_cores": B.PA_DECODE_TENSOR_CORES, "tcgen05": B.PA_DECODE_TCGEN05}
+
+
 class BlockPool:
     def __init__(self, num_blocks: int, block_size: int = 16, num_layers: int = 24,
                  num_kv_heads: int = 2, head_dim: int = 64, dtype=torch.bfloat16,
@@ -47,6 +51,36 @@ class BlockPool:
     def block_bytes(self) -> int:
         return B.pa_pool_block_bytes(self.handle)
 
+    # -- the same free stack on the device (one launch per batch) -----------
+    def device_stack(self, stream=None) -> torch.Tensor:
+        """Moves the free stack into a new device tensor; the host allocator
+        refuses until download_device_stack brings it back."""
+        n = B.pa_device_stack_bytes(self.handle) // 4
+        stack = torch.empty(n, dtype=torch.int32, device=self.pool.device)
+        B.pa_device_stack_upload(self.handle, stack, stream)
+        return stack
+
+    def download_device_stack(self, stack: torch.Tensor, stream=None) -> None:
+        B.pa_device_stack_download(self.handle, stack, stream)
+
+    def device_allocate_blocks(self, stack: torch.Tensor, block_tables: torch.Tensor,
+                               positions: torch.Tensor, stream=None) -> None:
+        """Every sequence whose position starts a new block pops one from the
+        device stack into its table (the order repeated host calls give)."""
+        B.pa_device_alloc_blocks(self.handle, stack, block_tables, block_tables.shape[1],
+                                 positions, positions.shape[0], stream)
+
+    def device_free_blocks(self, stack: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, finished: torch.Tensor,
+                           stream=None) -> None:
+        """Finished sequences push their blocks back and their table rows become -1."""
+        B.pa_device_free_blocks(self.handle, stack, block_tables, block_tables.shape[1],
+                                context_lens, finished, context_lens.shape[0], stream)
+
+    def set_decode_kernel(self, kind: str) -> None:
+        """'auto' (default), 'cuda_cores', 'tensor_cores' (mma.sync) or 'tcgen05'."""
+        B.pa_pool_set_decode_kernel(self.handle, _DECODE_KERNELS[kind])
+
     # -- kernels -----------------------------------------------------------
     def write_kv(self, layer: int, k: torch.Tensor, v: torch.Tensor, block_tables: torch.Tensor,
                  positions: torch.Tensor, stream=None) -> None:
@@ -74,6 +108,27 @@ class BlockPool:
                                           context_lens, batch, self.block_size, num_heads,
                                           self.num_kv_heads, head_dim, scale, partition_blocks,
                                           workspace, wbytes, stream)
+        return out
+
+    def write_kv_and_decode(self, q: torch.Tensor, layer: int, k: torch.Tensor, v: torch.Tensor,
+                            positions: torch.Tensor, block_tables: torch.Tensor,
+                            context_lens: torch.Tensor, scale: float,
+                            out: Optional[torch.Tensor] = None, partition_blocks: int = 0,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """write_kv then decode_attention in one launch (context_lens normally
+        include the new token)."""
+        batch, num_heads, head_dim = q.shape
+        maxb = block_tables.shape[1]
+        if out is None:
+            out = torch.empty((batch, num_heads, head_dim), dtype=torch.float32, device=q.device)
+        need = self.workspace_size(batch, num_heads, maxb, partition_blocks)
+        if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        B.pa_write_kv_and_decode(out, q, self.handle, layer, k, v, positions, block_tables, maxb,
+                                 context_lens, batch, self.block_size, num_heads,
+                                 self.num_kv_heads, head_dim, scale, partition_blocks, workspace,
+                                 wbytes, stream)
         return out
 
     def gather_kv(self, layer: int, block_tables: torch.Tensor, context_lens: torch.Tensor,

@@ -62,3 +62,56 @@ def test_blockpool_grow_append_decode_gather(cuda_device):
     assert pool.allocate_block() == ref.allocate_block()
     assert np.array_equal(W.as_oracle_array(pool.pool), host)
     pool.close()
+
+
+@pytest.mark.parametrize("kind", ["auto", "cuda_cores", "tensor_cores"])
+def test_blockpool_device_loop_fused(cuda_device, kind):
+    """The device free stack and the fused append + decode through BlockPool:
+    every step allocates on the device, appends and decodes in one launch;
+    tables, pool and outputs match the host allocator + oracle."""
+    nb, Bs, Hkv, D, H, batch, steps = 48, 16, 2, 64, 16, 5, 37
+    pool = BlockPool(num_blocks=nb, block_size=Bs, num_layers=1, num_kv_heads=Hkv, head_dim=D,
+                     dtype=torch.bfloat16, device=cuda_device)
+    pool.set_decode_kernel(kind)
+    ref = FreeBlockStack(nb)
+    stack = pool.device_stack()
+    g = torch.Generator().manual_seed(11)
+    tables = np.full((batch, 8), -1, np.int32)
+    lens = np.zeros(batch, np.int32)
+    bt = torch.from_numpy(tables.copy()).to(cuda_device)
+    host = W.as_oracle_array(pool.pool.cpu()).copy()
+    for step in range(steps):
+        pos = torch.from_numpy(lens.copy()).to(cuda_device)
+        pool.device_allocate_blocks(stack, bt, pos)
+        for b in range(batch):
+            if lens[b] % Bs == 0:
+                tables[b, lens[b] // Bs] = ref.allocate_block()
+        k = torch.randn(batch, Hkv, D, generator=g).bfloat16()
+        v = torch.randn(batch, Hkv, D, generator=g).bfloat16()
+        q = torch.randn(batch, H, D, generator=g).bfloat16()
+        oracle.write_kv(host, 0, W.as_oracle_array(k), W.as_oracle_array(v), tables, lens)
+        lens = lens + 1
+        out = pool.write_kv_and_decode(q.to(cuda_device), 0, k.to(cuda_device), v.to(cuda_device),
+                                       pos, bt, torch.from_numpy(lens).to(cuda_device),
+                                       scale=D ** -0.5, partition_blocks=1)
+        if step in (0, 15, 16, steps - 1):
+            ref_out = oracle.decode_attention(W.as_oracle_array(q), host, 0, tables, lens, H,
+                                              D ** -0.5)
+            assert max_abs_err(out, ref_out) <= 2e-3, step
+    torch.cuda.synchronize()
+    assert np.array_equal(bt.cpu().numpy(), tables)
+    assert np.array_equal(W.as_oracle_array(pool.pool.cpu()), host)
+    # finish two sequences on the device; the stack comes back in the host's order
+    finished = torch.tensor([1, 0, 0, 1, 0], dtype=torch.uint8, device=cuda_device)
+    pool.device_free_blocks(stack, bt, torch.from_numpy(lens).to(cuda_device), finished)
+    for b in (0, 3):
+        for j in range(-(-int(lens[b]) // Bs)):
+            ref.free_block(int(tables[b, j]))
+            tables[b, j] = -1
+    torch.cuda.synchronize()
+    assert np.array_equal(bt.cpu().numpy(), tables)
+    pool.download_device_stack(stack)
+    assert pool.num_free() == ref.num_free()
+    assert [pool.allocate_block() for _ in range(ref.num_free())] == \
+        [ref.allocate_block() for _ in range(ref.num_free())]
+    pool.close()
