@@ -203,45 +203,54 @@ struct UmmaCfg {
     static constexpr int TT = 128;                  // tokens per tile (M of S = K Q^T)
     static constexpr int NBOX = TT / 16;            // 16-row boxes per 64-column half
     static constexpr int HALF = TT * 128;           // one 64-column half of a tile (bytes)
-    static constexpr int KV_TILE = 2 * HALF;        // K (or V) tile
-    static constexpr int STAGE = 2 * KV_TILE;       // K tile, then V tile
-    static constexpr int ST = 3;                    // pipeline stages
-    // P of a tile: [64-column block][token][128 B] rows of hi heads | lo heads |
-    // zeros, written into the K half of the tile's own stage once S = K Q^T has
-    // consumed it -- one P buffer per stage, so the softmax of tile i+1 never
-    // waits for P V of tile i.
+    static constexpr int TILE = 2 * HALF;           // a K or a V tile
+    // Separate K and V rings: a K stage is free once S = K Q^T has read it, a V
+    // stage only after P V; so K runs ahead and the V ring covers the long
+    // chain (copy, S, softmax, P V).
+    static constexpr int SK = G >= 64 ? 2 : 3;      // K stages
+    static constexpr int SV = 3;                    // V stages
+    // P of a tile: [64-column block][token][128 B] rows of hi heads | lo heads
+    // | zeros, in one buffer: the softmax of tile i + 1 overlaps P V of tile i
+    // and waits for it only before writing P.
     static constexpr int PW = 2 * G < 64 ? 64 : 2 * G;
     static constexpr int P_BYTES = (PW / 64) * HALF;
-    static constexpr int Q_BYTES = 2 * G * 128;     // q of the item, two 64-column halves
+    static constexpr int Q_BYTES = 2 * G * 128;     // q of one item, two 64-column halves
+                                                    // (two buffers: the next item's q
+                                                    // lands while this item's S runs)
     static constexpr int O_COL = 2 * G;             // TMEM: S0 [0, G), S1 [G, 2G), O^T after
     static constexpr int TMEM_COLS = (2 * G + PW) <= 32 ? 32 : (2 * G + PW) <= 64 ? 64
                                    : (2 * G + PW) <= 128 ? 128 : (2 * G + PW) <= 256 ? 256 : 512;
-    static constexpr int OFF_Q = ST * STAGE;
+    static constexpr int OFF_V = SK * TILE;
+    static constexpr int OFF_P = OFF_V + SV * TILE;
+    static constexpr int OFF_Q = OFF_P + P_BYTES;
     static constexpr int OFF_CTRL = OFF_Q + 2 * Q_BYTES;
-    // ctrl: mbarriers [0, 160) | stage meta | TMEM address | abort flag | m[G] | alpha[G] | red[4][G]
+    // ctrl: mbarriers [0, 192) | V stage meta | TMEM address | abort flag | m[G] | alpha[G] | red[4][G]
     static constexpr int CTRL_BYTES = 256 + 6 * G * 4;
+    static constexpr int META_OFF = 192, TMEM_SLOT_OFF = 224, ABORT_OFF = 228;
     static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
-    // softmax: 4 lane quarters x (G / HG) head parts, one warp each (more
-    // than one warp per scheduler, so the dependent latencies of the
-    // per-token work overlap)
+    // warps: 0 K producer (+ q), 1 MMA, 2 V producer, 3 .. 10 softmax (4 lane
+    // quarters x 2 head parts: more than one warp per scheduler, so the
+    // dependent latencies of the per-token work overlap)
     static constexpr int HG = G / 2;                // heads per softmax warp
-    static constexpr int NSW = 4 * (G / HG);        // softmax warps
+    static constexpr int SM_WARP0 = 3;
+    static constexpr int NSW = 8;                   // softmax warps
     static constexpr int NSM = NSW * 32;            // softmax threads
-    static constexpr int THREADS = 64 + NSM;
+    static constexpr int THREADS = (SM_WARP0 + NSW) * 32;
     // barrier indices
-    static constexpr int KV_FULL = 0, KV_EMPTY = ST, Q_FULL = 2 * ST, Q_EMPTY = 2 * ST + 2,
-                         S_FULL = 2 * ST + 4, P_FULL = 2 * ST + 6, PV_DONE = 2 * ST + 8,
-                         FINAL = 2 * ST + 10, NBAR = 2 * ST + 11;
-    // S_FULL, P_FULL and PV_DONE are pairs used by tile parity.  The softmax of
-    // tile i + 1 may finish before the MMA thread has seen P of tile i, and a
-    // softmax thread waits on P V of tile i - 1 at most: with a pair, no
-    // barrier ever runs two phases ahead of a waiter (parity waits would alias).
+    static constexpr int K_FULL = 0, K_EMPTY = SK, V_FULL = 2 * SK, V_EMPTY = 2 * SK + SV,
+                         Q_FULL = 2 * SK + 2 * SV, Q_EMPTY = Q_FULL + 2, S_FULL = Q_FULL + 4,
+                         P_FULL = Q_FULL + 6, PV_DONE = Q_FULL + 8, FINAL = Q_FULL + 10,
+                         NBAR = Q_FULL + 11;
+    // Q_FULL / Q_EMPTY pairs follow the two q buffers; S_FULL, P_FULL and
+    // PV_DONE are pairs used by tile parity, so that no barrier ever runs two
+    // phases ahead of a waiter (parity waits would alias); every other
+    // barrier's next phase needs the waiter's own progress.
 
     static_assert(G == 16 || G == 32 || G == 64, "head chunk of 16, 32 or 64");
     static_assert(B == 16 || B == 32, "block size 16 or 32");
-    static_assert(NBAR * 8 <= 160, "barriers");
+    static_assert(NBAR * 8 <= META_OFF, "barriers");
+    static_assert(META_OFF + 4 * SV <= TMEM_SLOT_OFF, "stage meta");
     static_assert(2 * G + PW <= TMEM_COLS, "TMEM columns");
-    static_assert(P_BYTES <= KV_TILE, "P fits in the K half of a stage");
     static_assert(HG == 8 || HG % 16 == 0, "TMEM loads of 8 or 16k columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -341,9 +350,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
     unsigned char* smem = smem_raw + (sbase - raw_addr);
     unsigned char* ctrl = smem + C::OFF_CTRL;
     const uint32_t bar0 = sbase + C::OFF_CTRL;
-    int* meta = reinterpret_cast<int*>(ctrl + 160);                 // bad-box mask per stage
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 176);
-    volatile int* abort_all = reinterpret_cast<volatile int*>(ctrl + 180);
+    int* meta = reinterpret_cast<int*>(ctrl + C::META_OFF);         // bad-box mask per V stage
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + C::TMEM_SLOT_OFF);
+    volatile int* abort_all = reinterpret_cast<volatile int*>(ctrl + C::ABORT_OFF);
     float* m_sh = reinterpret_cast<float*>(ctrl + 256);             // running max per head
     float* a_sh = m_sh + G;                                         // rescale factor per head
     float* red = a_sh + G;                                          // [4][G] cross-warp partials
@@ -367,42 +376,48 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ================================================= producer (warp 0)
+    if (warp == 0 || warp == 2) {
+        // ============================= producers: warp 0 K (and q), warp 2 V
+        // Both walk the same items and table entries.  The fused append's new
+        // row is stored by each producer for its own half (K or V) before that
+        // producer's copies of the item; warp 2 reports bad ids and lengths.
+        const bool is_v = (warp == 2);
+        const CUtensorMap* tm = is_v ? &tmv : &tmk;
+        const int NS = is_v ? C::SV : C::SK;
+        const uint32_t full0 = bar0 + 8 * (is_v ? C::V_FULL : C::K_FULL);
+        const uint32_t empty0 = bar0 + 8 * (is_v ? C::V_EMPTY : C::K_EMPTY);
+        const uint32_t ring = sbase + (is_v ? C::OFF_V : 0);
         const uint64_t policy = l2_policy_evict_first();
         int kt = 0, qi = 0;
         bool aborted = false;
         for (int idx = blockIdx.x; idx < total_items && !aborted; idx += gridDim.x) {
             UItem it;
             const bool live = umma_item<B, G>(p, idx, it);
-            if (it.bad_len && it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
+            if (is_v && it.bad_len && it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
                 atomicOr(p.status, kStatusBadLength);
             if (!live) continue;
             const int* bt_row = p.bt + (long long)it.b * p.maxb;
-            const long long tile0 = p.tile_off + (long long)it.kvh * p.s_head;
             if (p.new_k != nullptr) {
                 // fused append: the partition that owns the new row stores it
                 // (every head chunk its own identical copy) before its copies
                 const int pos = __ldg(p.positions + it.b);
                 if (pos < 0 || pos / B >= p.maxb) {
-                    if (it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
+                    if (is_v && it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
                         atomicOr(p.status, kStatusBadLength);
                 } else if (it.c == (pos < it.n ? (pos / B) / p.PB : 0)) {
                     const int blk = __ldg(bt_row + pos / B);
                     if (blk < 0 || blk >= p.num_blocks) {
-                        if (lane == 0) atomicOr(p.status, kStatusBadBlock);
-                    } else {
-                        const int kv = lane >> 4;  // 16 chunks of 16 bytes per 128-element row
-                        const int ci = lane & 15;
-                        const long long src = ((long long)it.b * p.Hkv + it.kvh) * 256 + ci * 16;
-                        const long long off =
-                            (long long)blk * p.s_blk + tile0 + (long long)(pos % B) * 128;
+                        if (is_v && lane == 0) atomicOr(p.status, kStatusBadBlock);
+                    } else if (lane < 16) {  // 16 chunks of 16 bytes per 128-element row
+                        const long long src = ((long long)it.b * p.Hkv + it.kvh) * 256 + lane * 16;
+                        const long long off = (long long)blk * p.s_blk + p.tile_off +
+                                              (long long)it.kvh * p.s_head + (long long)(pos % B) * 128;
                         const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                            static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src));
+                            static_cast<const unsigned char*>(is_v ? p.new_v : p.new_k) + src));
                         unsigned short* dst = const_cast<unsigned short*>(
-                            reinterpret_cast<const unsigned short*>(kv ? p.v_base : p.k_base)) +
+                            reinterpret_cast<const unsigned short*>(is_v ? p.v_base : p.k_base)) +
                             off;
-                        reinterpret_cast<uint4*>(dst)[ci] = val;
+                        reinterpret_cast<uint4*>(dst)[lane] = val;
                         fence_proxy_async_global();
                     }
                 }
@@ -410,14 +425,15 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             }
             if (it.ntiles == 0) continue;
 
-            // q of the item's G heads -> K-major swizzled tile [half][G][128 B]
-            if (qi >= 2 &&
-                !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + (qi & 1)),
-                                                 ((qi >> 1) - 1) & 1, abort_all, p.status))) {
-                aborted = true;
-                break;
-            }
-            {
+            if (!is_v) {
+                // q of the item's G heads -> K-major swizzled tile [half][G][128 B]
+                // (buffer qi & 1: free once the last S of item qi - 2 is done)
+                if (qi >= 2 &&
+                    !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + (qi & 1)),
+                                                     ((qi >> 1) - 1) & 1, abort_all, p.status))) {
+                    aborted = true;
+                    break;
+                }
                 const uint32_t qbuf = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
                 const uint4* qsrc = reinterpret_cast<const uint4*>(
                     static_cast<const unsigned short*>(p.q) +
@@ -433,10 +449,10 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 if (lane == 0) mbar_arrive(bar0 + 8 * (C::Q_FULL + (qi & 1)));
             }
 
-            // 128-token K / V tiles: lane r < 8 walks box r (16 rows) of the tile
+            // 128-token tiles: lane r < 8 walks box r (16 rows) of the tile
             for (int i = 0; i < it.ntiles; ++i, ++kt) {
-                const int stage = kt % C::ST;
-                const int use = kt / C::ST;
+                const int stage = kt % NS;
+                const int use = kt / NS;
                 const int tok = it.t0 + i * C::TT + 16 * lane;
                 bool valid = false;
                 int blk = 0;
@@ -445,9 +461,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     valid = true;
                 }
                 // (every lane waits and votes: the warp leaves the loop together)
-                if (use > 0 && !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::KV_EMPTY + stage),
-                                                                (use - 1) & 1, abort_all,
-                                                                p.status))) {
+                if (use > 0 && !__all_sync(kFullMask, umma_wait(empty0 + 8 * stage, (use - 1) & 1,
+                                                                abort_all, p.status))) {
                     aborted = true;
                     break;
                 }
@@ -455,11 +470,13 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 valid = valid && !bad;
                 const unsigned vmask = __ballot_sync(kFullMask, valid);
                 const unsigned bmask = __ballot_sync(kFullMask, bad);
-                const uint32_t fb = bar0 + 8 * (C::KV_FULL + stage);
+                const uint32_t fb = full0 + 8 * stage;
                 if (lane == 0) {
-                    if (bmask) atomicOr(p.status, kStatusBadBlock);
-                    meta[stage] = (int)bmask;
-                    mbar_arrive_expect_tx(fb, (uint32_t)__popc(vmask) * 4u * 2048u);
+                    if (is_v) {
+                        if (bmask) atomicOr(p.status, kStatusBadBlock);
+                        meta[stage] = (int)bmask;
+                    }
+                    mbar_arrive_expect_tx(fb, (uint32_t)__popc(vmask) * 2u * 2048u);
                 }
                 __syncwarp();
                 if (valid) {
@@ -470,34 +487,32 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                                    : (p.tma_slot_layer == 3 ? p.layer : it.kvh);
                     const int o4 = p.tma_slot_blk == 4 ? blk
                                    : (p.tma_slot_layer == 4 ? p.layer : it.kvh);
-                    const uint32_t dst = sbase + stage * C::STAGE + lane * 2048;
-                    tma_load_5d(dst, &tmk, fb, 0, row0, o2, o3, o4, policy);
-                    tma_load_5d(dst + C::HALF, &tmk, fb, 64, row0, o2, o3, o4, policy);
-                    tma_load_5d(dst + C::KV_TILE, &tmv, fb, 0, row0, o2, o3, o4, policy);
-                    tma_load_5d(dst + C::KV_TILE + C::HALF, &tmv, fb, 64, row0, o2, o3, o4,
-                                policy);
+                    const uint32_t dst = ring + stage * C::TILE + lane * 2048;
+                    tma_load_5d(dst, tm, fb, 0, row0, o2, o3, o4, policy);
+                    tma_load_5d(dst + C::HALF, tm, fb, 64, row0, o2, o3, o4, policy);
                 }
             }
             if (!aborted) ++qi;
         }
-        if (aborted) {
+        if (aborted || *abort_all) {
             // copies still in flight land before the CTA can exit
-            for (int k = kt > C::ST ? kt - C::ST : 0; k < kt; ++k)
-                (void)mbar_wait_bounded(bar0 + 8 * (C::KV_FULL + k % C::ST), (k / C::ST) & 1);
+            for (int k = kt > NS ? kt - NS : 0; k < kt; ++k)
+                (void)mbar_wait_bounded(full0 + 8 * (k % NS), (k / NS) & 1);
         }
     } else if (warp == 1) {
         // ============================================ MMA issuer (warp 1, lane 0)
         if (lane == 0) {
-            // Two cursors: S = K Q^T of tile kt_q (as soon as its K / V and q are
-            // in and an S buffer is free: at most two tiles ahead of P V) and
-            // O^T += V^T [P_hi | P_lo] of tile kt_pv (as soon as its P is
-            // written).  Polled in one loop, so neither waits behind the other:
-            // the last P V of an item does not wait for the next item's data.
+            // Two cursors: S = K Q^T of tile kt_q (once its K and q are in and an
+            // S buffer is free: at most two tiles ahead of P V; the K stage is
+            // released when S completes) and O^T += V^T [P_hi | P_lo] of tile
+            // kt_pv (once its P is written and its V is in; the V stage is
+            // released when P V completes).  Polled without blocking on either.
             constexpr uint32_t IDQ = umma_idesc_bf16(128, G, 0, 0);
             constexpr uint32_t IDP = umma_idesc_bf16(128, C::PW, 1, 1);
+            const uint32_t pbuf = sbase + C::OFF_P;
             int idx_q = blockIdx.x;   // next item to look at
             int tiles_left = 0;       // tiles of the current item still without S
-            int i_q = 0, qi = -1;     // tile within the item; q buffer use of the item
+            int i_q = 0, qi = -1;     // tile within the item; item (with tiles) count
             bool q_ready = false, done_q = false;
             int kt_q = 0, kt_pv = 0;
             unsigned first_bits = 0;  // bit (tile & 1): the tile is its item's first
@@ -505,19 +520,19 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             while (true) {
                 bool progressed = false;
                 if (kt_pv < kt_q &&
-                    mbar_test(bar0 + 8 * (C::P_FULL + (kt_pv & 1)), (kt_pv >> 1) & 1)) {
+                    mbar_test(bar0 + 8 * (C::P_FULL + (kt_pv & 1)), (kt_pv >> 1) & 1) &&
+                    mbar_test(bar0 + 8 * (C::V_FULL + kt_pv % C::SV), (kt_pv / C::SV) & 1)) {
                     tc_fence_after();
-                    const int stage = kt_pv % C::ST;
+                    const int vs = kt_pv % C::SV;
                     const bool first = (first_bits >> (kt_pv & 1)) & 1u;
-                    const uint32_t pbuf = sbase + stage * C::STAGE;
-                    const uint32_t vt = pbuf + C::KV_TILE;
+                    const uint32_t vt = sbase + C::OFF_V + vs * C::TILE;
 #pragma unroll
                     for (int k = 0; k < C::TT / 16; ++k)
                         umma_bf16(tmem + C::O_COL, umma_desc_sw128(vt + k * 2048, C::HALF, 1024),
                                   umma_desc_sw128(pbuf + k * 2048, C::HALF, 1024), IDP,
                                   (k > 0 || !first) ? 1u : 0u);
                     umma_commit(bar0 + 8 * (C::PV_DONE + (kt_pv & 1)));
-                    umma_commit(bar0 + 8 * (C::KV_EMPTY + stage));
+                    umma_commit(bar0 + 8 * (C::V_EMPTY + vs));
                     ++kt_pv;
                     progressed = true;
                 }
@@ -538,12 +553,12 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     } else {
                         if (!q_ready)
                             q_ready = mbar_test(bar0 + 8 * (C::Q_FULL + (qi & 1)), (qi >> 1) & 1);
-                        const int stage = kt_q % C::ST;
+                        const int ks = kt_q % C::SK;
+                        const uint32_t qb = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
                         if (q_ready &&
-                            mbar_test(bar0 + 8 * (C::KV_FULL + stage), (kt_q / C::ST) & 1)) {
+                            mbar_test(bar0 + 8 * (C::K_FULL + ks), (kt_q / C::SK) & 1)) {
                             tc_fence_after();
-                            const uint32_t ktile = sbase + stage * C::STAGE;
-                            const uint32_t qb = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
+                            const uint32_t ktile = sbase + ks * C::TILE;
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
                                 const int h = k >> 2, kk = k & 3;
@@ -553,6 +568,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                                           IDQ, k > 0 ? 1u : 0u);
                             }
                             umma_commit(bar0 + 8 * (C::S_FULL + (kt_q & 1)));
+                            umma_commit(bar0 + 8 * (C::K_EMPTY + ks));
                             first_bits = (first_bits & ~(1u << (kt_q & 1))) |
                                          ((i_q == 0 ? 1u : 0u) << (kt_q & 1));
                             ++i_q;
@@ -583,18 +599,25 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ============================== softmax (warps 2 .. 2 + NSW - 1)
+        // ====================== softmax (warps SM_WARP0 .. SM_WARP0 + NSW - 1)
         // Warp w works on TMEM lane quarter w % 4 (token / head-dim rows
         // 32 * (w % 4) + lane) and on heads [h0, h0 + HG).
         // The head parts are independent (own barriers, heads, sums and
         // maxima); they meet only at P_FULL.
         constexpr int HG = C::HG;
-        const int part = (warp - 2) >> 2;
+        const int part = (warp - C::SM_WARP0) >> 2;
         const int qd = warp & 3;
-        const int sp = ((warp - 2) & 3) * 32 + lane;  // thread within the part, 0 .. 127
+        const int sp = ((warp - C::SM_WARP0) & 3) * 32 + lane;  // thread within the part, 0 .. 127
         const int h0 = part * HG;
         const int r = qd * 32 + lane;            // token of the tile (S) / head-dim element (O)
         const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+        unsigned char* pbuf = smem + C::OFF_P;
+        if (C::PW > 2 * G && part == 0) {
+            // the P buffer's zero columns (heads past the group) are written once
+#pragma unroll
+            for (int j = (2 * G) / 8; j < 8; ++j)
+                *reinterpret_cast<uint4*>(pbuf + sw128(r, j)) = make_uint4(0, 0, 0, 0);
+        }
         int kt = 0;
         bool stop = false;
         // A failed wait only marks this thread; the softmax threads decide to
@@ -614,10 +637,10 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
 #pragma unroll
             for (int g = 0; g < HG; ++g) lp[g] = 0.f;
             for (int i = 0; i < it.ntiles; ++i, ++kt) {
-                const int stage = kt % C::ST;
+                const int stage = kt % C::SV;  // V stage (and its meta)
                 bool ok = umma_wait(bar0 + 8 * (C::S_FULL + (kt & 1)), (kt >> 1) & 1, abort_all,
                                     p.status);
-                ok = ok && umma_wait(bar0 + 8 * (C::KV_FULL + stage), (kt / C::ST) & 1,
+                ok = ok && umma_wait(bar0 + 8 * (C::V_FULL + stage), (kt / C::SV) & 1,
                                      abort_all, p.status);
                 failed = failed || !ok;
                 __syncwarp();
@@ -647,6 +670,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     x[g] = valid ? x[g] * p.qscale : -INFINITY;
                     need |= x[g] > mreg[g] + 8.f;
                 }
+                bool pv_waited = false;
                 if (part_bar_or(part, need | failed)) {
                     if (part_bar_or(part, failed)) {
                         stop = true;
@@ -682,6 +706,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                         if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)),
                                        ((kt - 1) >> 1) & 1, abort_all, p.status))
                             failed = true;
+                        pv_waited = true;
                         __syncwarp();
                         tc_fence_after();
 #pragma unroll
@@ -707,10 +732,15 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     lp[g] += pv;
                     x[g] = pv;
                 }
+                // the one P buffer is free once the previous tile's P V is done
+                if (!pv_waited && kt > 0 &&
+                    !umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1,
+                               abort_all, p.status))
+                    failed = true;
                 if (!valid && h0 == 0) {
                     // rows past the context (or of a bad block) hold stale or
                     // foreign values: zero V so that 0 * V stays 0
-                    unsigned char* vrow = smem + stage * C::STAGE + C::KV_TILE + r * 128;
+                    unsigned char* vrow = smem + C::OFF_V + stage * C::TILE + r * 128;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         *reinterpret_cast<uint4*>(vrow + j * 16) = make_uint4(0, 0, 0, 0);
@@ -718,15 +748,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                             make_uint4(0, 0, 0, 0);
                     }
                 }
-                // P row (MN-major, 64-column blocks) into the K half of this
-                // tile's stage, which S = K Q^T has finished reading: hi heads,
-                // then lo heads, then zeros up to 64 columns
-                unsigned char* pbuf = smem + stage * C::STAGE;
-                if (C::PW > 2 * G && h0 == 0) {
-#pragma unroll
-                    for (int j = (2 * G) / 8; j < 8; ++j)
-                        *reinterpret_cast<uint4*>(pbuf + sw128(r, j)) = make_uint4(0, 0, 0, 0);
-                }
+                // P row (MN-major, 64-column blocks): hi heads, then lo heads
 #pragma unroll
                 for (int g8 = 0; g8 < HG; g8 += 8) {
                     uint32_t hi[4], lo[4];
