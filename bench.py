@@ -311,8 +311,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     stream = torch.cuda.current_stream(dev)
     cur = {"sp": stream.cuda_stream, "stream": stream}
     lib = B.lib()
-    cmax = -(-wl.max_blocks // pb)
-    launches_per_step = L * ((1 if args.fused else 2) + (1 if cmax > 1 else 0))
+    # a second (combine) kernel runs exactly when the call needs a workspace
+    launches_per_step = L * ((1 if args.fused else 2) + (1 if ws_bytes > 0 else 0))
 
     sets = [dict(q=qs, k=ks, v=vs, bt=bt, lens=lens, pos=positions, out=outs)]
 

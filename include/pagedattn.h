@@ -144,7 +144,14 @@ PA_API int pa_pool_destroy(pa_pool* pool);
  * kernel; a forced kernel that cannot serve a call makes it fail with
  * PA_ERR_UNSUPPORTED.  All compute the same result within the stated
  * tolerances.  The choice also fixes the automatic partition size (and so the
- * workspace size): query pa_decode_workspace_size after setting it. */
+ * workspace size): query pa_decode_workspace_size after setting it.
+ * The tcgen05 kernel does not use partitions: it runs one persistent CTA per
+ * SM and gives each CTA an equal share of the call's 128-token tiles (in
+ * sequence, head-group, tile order), so contexts are split wherever the shares
+ * end and the combine kernel merges those.  partition_blocks does not apply to
+ * it (pa_decode_partition_blocks reports max_blocks_per_seq); its workspace,
+ * needed whenever more than one CTA runs, grows with the SM count (two slots
+ * of partials per CTA) and the number of (sequence, head group) pairs. */
 enum {
     PA_DECODE_AUTO = 0,
     PA_DECODE_CUDA_CORES = 1,
@@ -305,7 +312,8 @@ PA_API int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_he
 
 /* Workspace bytes needed by pa_decode_attention_partitioned with the same
  * arguments (partition_blocks = 0: the heuristic choice, which queries the
- * current device).  0 when a single partition covers the table. */
+ * current device; the tcgen05 kernel always queries it).  0 when a single
+ * partition covers the table (tcgen05 kernel: when a single CTA runs). */
 PA_API int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
                              int max_blocks_per_seq, int partition_blocks, size_t* bytes);
 

@@ -98,26 +98,22 @@ int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sm
     return (int)pb;
 }
 
-// tcgen05 kernel (persistent, one CTA per SM, 128-token tiles): the same
-// estimate, rounded up to whole tiles, and at least 1024 tokens per item so
-// that the per-item work (q load, first-tile max, epilogue) stays small against
-// the K/V stream (GB300: 1024 tokens fastest for G = 32 and 64).
-int auto_partition_blocks_tcgen05(const pa::PoolGeom& g, int batch, int maxb, int num_sms,
-                                  int G) {
-    const int tile_blocks = 128 / g.B;
-    long long pb = auto_partition_blocks(g, batch, maxb, num_sms, G);
-    if (pb < 1024 / g.B) pb = 1024 / g.B;
-    pb = (pb + tile_blocks - 1) / tile_blocks * tile_blocks;
-    if (pb > maxb) pb = maxb;
-    return (int)pb;
-}
-
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 size_t workspace_bytes_for(int batch, int H, int Cmax, int D) {
     if (Cmax <= 1) return 0;
     const size_t slots = (size_t)batch * H * Cmax;
     return align256(slots * D * sizeof(float)) + slots * 2 * sizeof(float);
+}
+
+// tcgen05 kernel: two partial slots of `chunk` heads per CTA (its first and
+// last piece), then one int4 descriptor per (sequence, head group).
+size_t tc_partial_slots(int grid, int chunk) { return (size_t)grid * 2 * chunk; }
+size_t tc_workspace_bytes(int grid, int chunk, int D, long long pairs) {
+    if (grid <= 1) return 0;
+    const size_t S = tc_partial_slots(grid, chunk);
+    return align256(S * D * sizeof(float)) + align256(S * 2 * sizeof(float)) +
+           (size_t)pairs * sizeof(int4);
 }
 
 int check_pool(const pa_pool* pool) {
@@ -137,7 +133,10 @@ enum class Kernel { CudaCores, MmaSync, Tcgen05 };
 struct DecodeShape {
     int G, PB, Cmax;
     Kernel kernel;
+    int chunk;    // heads per CTA chunk of the group
+    int tc_grid;  // tcgen05 kernel: persistent grid
     size_t ws_bytes;
+    bool combine;  // a second kernel merges split contexts
 };
 
 // The kernel the pool's choice selects for group G, or a PA_ERR_UNSUPPORTED
@@ -198,20 +197,38 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
     const int G = num_heads / pool->g.Hkv;
     Kernel kernel = Kernel::CudaCores;
     if (int rc = pick_kernel(pool, G, &kernel)) return rc;
+    if (kernel == Kernel::Tcgen05) {
+        // The tcgen05 kernel splits the tiles evenly over its persistent grid
+        // itself; partition_blocks does not apply to it.
+        int sms = 0;
+        if (int rc = num_sms_current(&sms)) return rc;
+        const int chunk = pa::decode_umma_chunk(G);
+        const long long pairs = (long long)batch * pool->g.Hkv * (G / chunk);
+        if (pairs > INT_MAX)
+            return fail(PA_ERR_INVALID_ARG, "%lld (sequence, head group) pairs is too many", pairs);
+        const long long tiles = ((long long)maxb * pool->g.B + 127) / 128;
+        const long long units = pairs * (tiles > 1 ? tiles : 1);  // upper bound
+        const int grid = (int)(units < sms ? units : sms);
+        out->G = G;
+        out->kernel = kernel;
+        out->PB = maxb;
+        out->Cmax = 2;
+        out->chunk = chunk;
+        out->tc_grid = grid;
+        out->ws_bytes = tc_workspace_bytes(grid, chunk, pool->g.D, pairs);
+        out->combine = grid > 1;
+        return PA_OK;
+    }
     int pb = partition_blocks;
     if (pb == 0) {
         int sms = 0;
         int rc = num_sms_current(&sms);
         if (rc != PA_OK) return rc;
-        pb = kernel == Kernel::Tcgen05
-                 ? auto_partition_blocks_tcgen05(pool->g, batch, maxb, sms, G)
-                 : auto_partition_blocks(pool->g, batch, maxb, sms, G);
+        pb = auto_partition_blocks(pool->g, batch, maxb, sms, G);
     }
     if (pb > maxb) pb = maxb;
     const int Cmax = (maxb + pb - 1) / pb;
-    const int chunk = kernel == Kernel::Tcgen05 ? pa::decode_umma_chunk(G)
-                      : kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G)
-                                                  : G;
+    const int chunk = kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G) : G;
     const long long nchunks = G / chunk;
     if ((long long)batch * pool->g.Hkv * nchunks * Cmax > INT_MAX)
         return fail(PA_ERR_INVALID_ARG, "grid of %lld CTAs is too large",
@@ -220,7 +237,10 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
     out->kernel = kernel;
     out->PB = pb;
     out->Cmax = Cmax;
+    out->chunk = chunk;
+    out->tc_grid = 0;
     out->ws_bytes = workspace_bytes_for(batch, num_heads, Cmax, pool->g.D);
+    out->combine = Cmax > 1;
     return PA_OK;
 }
 
@@ -608,15 +628,23 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
         return fail(PA_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
     float* part_o = nullptr;
     float* part_ml = nullptr;
+    int4* tc_desc = nullptr;
     if (sh.ws_bytes > 0) {
         if (!workspace || workspace_bytes < sh.ws_bytes || !aligned(workspace, 256))
             return fail(PA_ERR_WORKSPACE,
                         "workspace must be 256-byte aligned and hold %zu bytes (got %p, %zu)",
                         sh.ws_bytes, workspace, workspace_bytes);
-        part_o = static_cast<float*>(workspace);
-        part_ml = reinterpret_cast<float*>(
-            static_cast<char*>(workspace) +
-            align256((size_t)batch * num_heads * sh.Cmax * g.D * sizeof(float)));
+        char* ws = static_cast<char*>(workspace);
+        part_o = reinterpret_cast<float*>(ws);
+        if (sh.kernel == Kernel::Tcgen05) {
+            const size_t S = tc_partial_slots(sh.tc_grid, sh.chunk);
+            part_ml = reinterpret_cast<float*>(ws + align256(S * g.D * sizeof(float)));
+            tc_desc = reinterpret_cast<int4*>(ws + align256(S * g.D * sizeof(float)) +
+                                              align256(S * 2 * sizeof(float)));
+        } else {
+            part_ml = reinterpret_cast<float*>(
+                ws + align256((size_t)batch * num_heads * sh.Cmax * g.D * sizeof(float)));
+        }
     }
     unsigned* status = nullptr;
     cudaError_t e = pa::status_word(&status);
@@ -646,6 +674,10 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     p.new_k = new_k;
     p.new_v = new_v;
     p.positions = positions;
+    p.tc_grid = sh.tc_grid;
+    p.tc_desc = tc_desc;
+    p.gsize = sh.G;
+    p.nchunks = sh.G / sh.chunk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (sh.kernel != Kernel::CudaCores) {
         {
@@ -667,7 +699,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
                          : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-    if (sh.Cmax > 1) {
+    if (sh.combine) {
         e = pa::launch_combine(p, g.D, g.B, s);
         if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     }

@@ -491,7 +491,10 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
 // Merges the partitions of every (sequence, query head) with more than one:
 //   M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c .
 // W warps (1, 2, 4 or 8) serve one (sequence, head); a 256-thread CTA serves
-// 8 / W of them.  Warp w takes partitions w, w + W, ... four at a time (four
+// 8 / W of them.  Partial c of (sequence, head) gh sits at slot gh * Cmax + c
+// (fixed-size partitions), or, after the tcgen05 kernel (p.tc_desc set), at
+// slot ((first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + head in chunk: piece
+// c came from CTA first + c, and only the first piece can be a CTA's second.  Warp w takes partitions w, w + W, ... four at a time (four
 // independent loads in flight per lane; a lane owns D/32 consecutive
 // elements), then the W partial sums are merged through shared memory.
 template <int D, int W>
@@ -510,19 +513,40 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, i
     const long long gh = (long long)blockIdx.x * HPC + hl;  // b * H + h
     const bool live = gh < (long long)p.batch * p.H;
     int nparts = 0;
+    long long base = gh * p.Cmax;  // slot of partial c: base + c, or see below
+    int first = 0, slot0 = 0, chunk = 1;
     if (live) {
         const int b = (int)(gh / p.H);
-        int n = __ldg(p.lens + b);
-        if (n < 0 || n > p.maxb * B) n = 0;
-        const int nblk = (n + B - 1) / B;
-        nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
+        if (p.tc_desc != nullptr) {
+            const int h = (int)(gh % p.H);
+            const int kvh = h / p.gsize, hg = h % p.gsize;
+            chunk = p.gsize / p.nchunks;
+            const int4 d = p.tc_desc[(long long)b * p.Hkv * p.nchunks + kvh * p.nchunks +
+                                     hg / chunk];
+            first = d.x;
+            nparts = d.y;
+            slot0 = d.z;
+            base = hg % chunk;
+            // (a descriptor the decode never wrote -- it stopped on a timeout --
+            // must not send the loads outside the partial slots)
+            if (first < 0 || nparts < 0 || first > p.tc_grid - nparts || (slot0 & ~1)) nparts = 0;
+        } else {
+            int n = __ldg(p.lens + b);
+            if (n < 0 || n > p.maxb * B) n = 0;
+            const int nblk = (n + B - 1) / B;
+            nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
+        }
     }
-    const long long base = gh * p.Cmax;
-    const float* ml = p.part_ml + base * 2;
+    const bool by_cta = p.tc_desc != nullptr;
+    auto slot_of = [&](int c) -> long long {
+        return by_cta ? ((long long)(first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + base
+                      : base + c;
+    };
     // running max over this head's partitions, per warp then across the W warps
     float M = -INFINITY;
     if (nparts > 1)
-        for (int c = w * 32 + lane; c < nparts; c += W * 32) M = fmaxf(M, __ldg(ml + 2 * c));
+        for (int c = w * 32 + lane; c < nparts; c += W * 32)
+            M = fmaxf(M, __ldg(p.part_ml + 2 * slot_of(c)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
     if (lane == 0) s_m[warp] = M;
@@ -544,10 +568,11 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, i
 #pragma unroll
                 for (int i = 0; i < PL; ++i) ov[u][i] = 0.f;
                 if (c < nparts) {
-                    const float mc = __ldg(ml + 2 * c);
+                    const long long sl = slot_of(c);
+                    const float mc = __ldg(p.part_ml + 2 * sl);
                     wt[u] = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-                    L += wt[u] * __ldg(ml + 2 * c + 1);
-                    const float* oc = p.part_o + (base + c) * D + lane * PL;
+                    L += wt[u] * __ldg(p.part_ml + 2 * sl + 1);
+                    const float* oc = p.part_o + sl * D + lane * PL;
                     if constexpr (PL == 4) {
                         const float4 v = __ldg(reinterpret_cast<const float4*>(oc));
                         ov[u][0] = v.x;

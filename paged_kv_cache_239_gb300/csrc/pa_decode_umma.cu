@@ -16,7 +16,6 @@ cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream
     auto kern = pa_decode_umma_kernel<B, G>;
     static std::mutex mu;
     static unsigned long long done_mask = 0;
-    static int sms[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -27,18 +26,14 @@ cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      Cfg::SMEM_BYTES);
             if (e != cudaSuccess) return e;
-            e = cudaDeviceGetAttribute(&sms[dev & 63], cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess) return e;
             done_mask |= bit;
         }
     }
-    const long long items = (long long)p.batch * p.Hkv * p.nchunks * p.Cmax;
-    if (items <= 0) return cudaSuccess;
-    if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    // persistent: one CTA per SM (the shared memory admits no second one)
-    const int grid = (int)(items < sms[dev & 63] ? items : sms[dev & 63]);
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, p,
-                      (int)items, tm[0], tm[1]);
+    if (p.tc_grid <= 0) return cudaErrorInvalidConfiguration;
+    // persistent: one CTA per SM (the shared memory admits no second one),
+    // each taking an equal share of the tiles
+    return launch_pdl(kern, dim3((unsigned)p.tc_grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
+                      stream, p, tm[0], tm[1]);
 }
 
 template <int B>

@@ -224,16 +224,19 @@ struct UmmaCfg {
     static constexpr int OFF_P = OFF_V + SV * TILE;
     static constexpr int OFF_Q = OFF_P + P_BYTES;
     static constexpr int OFF_CTRL = OFF_Q + 2 * Q_BYTES;
-    // ctrl: mbarriers [0, 192) | V stage meta | TMEM address | abort flag | m[G] | alpha[G] | red[4][G]
-    static constexpr int CTRL_BYTES = 256 + 6 * G * 4;
+    // ctrl: mbarriers [0, 192) | V stage meta | TMEM address | abort flag | m[G] | alpha[G] |
+    // red[4][G] | this CTA's schedule (48 bytes)
+    static constexpr int SCHED_OFF = 256 + 6 * G * 4;
+    static constexpr int CTRL_BYTES = SCHED_OFF + 48;
     static constexpr int META_OFF = 192, TMEM_SLOT_OFF = 224, ABORT_OFF = 228;
     static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
     // warps: 0 K producer (+ q), 1 MMA, 2 V producer, 3 .. 10 softmax (4 lane
     // quarters x 2 head parts: more than one warp per scheduler, so the
     // dependent latencies of the per-token work overlap)
-    static constexpr int HG = G / 2;                // heads per softmax warp
+    static constexpr int NPART = G >= 64 ? 4 : 2;   // head parts
+    static constexpr int HG = G / NPART;            // heads per softmax warp
     static constexpr int SM_WARP0 = 3;
-    static constexpr int NSW = 8;                   // softmax warps
+    static constexpr int NSW = 4 * NPART;           // softmax warps
     static constexpr int NSM = NSW * 32;            // softmax threads
     static constexpr int THREADS = (SM_WARP0 + NSW) * 32;
     // barrier indices
@@ -255,36 +258,162 @@ struct UmmaCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// One work item: (sequence b, KV head, head chunk, partition c).  Decoded the
-// same way by every role.  Head chunk fastest, then KV head, sequence, and
-// partition slowest (the grid-stride order of the items).
+// Work schedule.  The unit of work is one 128-token tile of one (sequence b,
+// head group g) pair, g = kv head * nchunks + head chunk; a context of n
+// tokens has max(1, ceil(n / 128)) units (an empty one still owes its zero
+// output).  Units are ordered by b, then g, then tile, and CTA j of the
+// persistent grid takes the contiguous range [ceil(j T / grid), ceil((j + 1)
+// T / grid)) of the T units (grid <= T, so no range is empty): every CTA gets
+// the same number of tiles, whatever the mix of lengths.  A range covers whole
+// (b, g) pairs, except that its first and last piece may be parts of one that
+// neighbouring CTAs share; those write unnormalised partials into the CTA's
+// two slots (first piece slot 0, last slot 1) and the combine kernel merges
+// them, told where by the descriptor the first piece of each pair writes.
 struct UItem {
-    int b, kvh, hc, c, hbase, n, nparts, t0, t1, ntiles;
-    bool bad_len;
+    int b, g, kvh, hc, hbase, n, c, u, units, t0, t1, ntiles;
+    long long gpos;          // global index of the piece's first unit
+    bool bad_len, whole, first;
 };
 
+__device__ __forceinline__ int umma_units(int n, int maxtok) {
+    return (n <= 0 || n > maxtok) ? 1 : (int)(((long long)n + 127) / 128);
+}
+
+// Computes this CTA's range (warp-wide; lane 0 stores it in `sched`):
+// [0] T, [8] grid (min(gridDim, T)), [16] first unit, [24] unit count,
+// [32] first b, [36] its g, [40] its tile.
+template <int B>
+__device__ __forceinline__ void umma_schedule(const DecodeParams& p, unsigned char* sched,
+                                              int lane) {
+    const int maxtok = p.maxb * B;
+    const long long Gq = (long long)p.Hkv * p.nchunks;
+    long long T = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 256) {
+        int nv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int b = b0 + 32 * k + lane;
+            nv[k] = b < p.batch ? __ldg(p.lens + b) : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (b0 + 32 * k + lane < p.batch) T += umma_units(nv[k], maxtok);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(kFullMask, T, off);
+    T *= Gq;
+    const long long grid = min((long long)gridDim.x, T);
+    const long long j = blockIdx.x;
+    long long lo = 0, cnt = 0;
+    int b_sel = 0, g_sel = 0, u_sel = 0;
+    if (j < grid) {
+        lo = (j * T + grid - 1) / grid;
+        cnt = ((j + 1) * T + grid - 1) / grid - lo;
+        long long P = 0;  // units before sequence b0
+        for (int b0 = 0; b0 < p.batch; b0 += 32) {
+            const int b = b0 + lane;
+            const long long cu = b < p.batch ? umma_units(__ldg(p.lens + b), maxtok) * Gq : 0;
+            long long incl = cu;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long v = __shfl_up_sync(kFullMask, incl, off);
+                if (lane >= off) incl += v;
+            }
+            const unsigned hit = __ballot_sync(kFullMask, cu > 0 && P + incl - cu <= lo &&
+                                                              lo < P + incl);
+            if (hit) {
+                const int f = __ffs(hit) - 1;
+                const long long excl = __shfl_sync(kFullMask, incl - cu, f);
+                const long long cf = __shfl_sync(kFullMask, cu, f) / Gq;  // units per pair
+                const long long off = lo - P - excl;
+                b_sel = b0 + f;
+                g_sel = (int)(off / cf);
+                u_sel = (int)(off % cf);
+                break;
+            }
+            P += __shfl_sync(kFullMask, incl, 31);
+        }
+    }
+    if (lane == 0) {
+        long long* s64 = reinterpret_cast<long long*>(sched);
+        int* s32 = reinterpret_cast<int*>(sched + 32);
+        s64[0] = T;
+        s64[1] = grid;
+        s64[2] = lo;
+        s64[3] = cnt;
+        s32[0] = b_sel;
+        s32[1] = g_sel;
+        s32[2] = u_sel;
+    }
+}
+
+// Walks the pieces of this CTA's range.  Every role walks it the same way; the
+// length of the next sequence is loaded one sequence ahead (under a full HBM
+// stream a dependent global load costs microseconds).
+struct UWalk {
+    int b, g, u, n, c, n_next, gq;
+    bool bad;
+    long long T, grid, lo, gpos, left;
+};
+
+template <int B>
+__device__ __forceinline__ void umma_walk_seq(const DecodeParams& p, UWalk& w, int n_raw) {
+    const int maxtok = p.maxb * B;
+    w.bad = n_raw < 0 || n_raw > maxtok;
+    w.n = w.bad ? 0 : n_raw;
+    w.c = umma_units(w.n, maxtok);
+    w.n_next = w.b + 1 < p.batch ? __ldg(p.lens + w.b + 1) : 0;
+}
+
+template <int B>
+__device__ __forceinline__ void umma_walk_begin(const DecodeParams& p, const unsigned char* sched,
+                                                UWalk& w) {
+    const long long* s64 = reinterpret_cast<const long long*>(sched);
+    const int* s32 = reinterpret_cast<const int*>(sched + 32);
+    w.T = s64[0];
+    w.grid = s64[1];
+    w.lo = s64[2];
+    w.left = s64[3];
+    w.gpos = w.lo;
+    w.b = s32[0];
+    w.g = s32[1];
+    w.u = s32[2];
+    w.gq = p.Hkv * p.nchunks;
+    if (w.left > 0) umma_walk_seq<B>(p, w, __ldg(p.lens + w.b));
+}
+
 template <int B, int G>
-__device__ __forceinline__ bool umma_item(const DecodeParams& p, int idx, UItem& it) {
-    it.hc = idx % p.nchunks;
-    idx /= p.nchunks;
-    const int nbh = p.batch * p.Hkv;
-    it.c = idx / nbh;
-    idx %= nbh;
-    it.kvh = idx % p.Hkv;
-    it.b = idx / p.Hkv;
+__device__ __forceinline__ bool umma_walk_next(const DecodeParams& p, UWalk& w, UItem& it) {
+    if (w.left <= 0) return false;
+    const int units = (int)min((long long)(w.c - w.u), w.left);
+    it.b = w.b;
+    it.g = w.g;
+    it.kvh = w.g / p.nchunks;
+    it.hc = w.g % p.nchunks;
     it.hbase = it.kvh * p.gsize + it.hc * G;
-    int n = __ldg(p.lens + it.b);
-    it.bad_len = n < 0 || n > p.maxb * B;
-    if (it.bad_len) n = 0;
-    it.n = n;
-    const int nblk = (n + B - 1) / B;
-    it.nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
-    const long long t0 = (long long)it.c * p.PB * B;
-    const long long t1 = min((long long)n, t0 + (long long)p.PB * B);
-    it.t0 = (int)min(t0, (long long)n);
-    it.t1 = (int)t1;
-    it.ntiles = t1 > t0 ? (int)((t1 - t0 + 127) / 128) : 0;
-    return it.c < it.nparts;
+    it.n = w.n;
+    it.c = w.c;
+    it.u = w.u;
+    it.units = units;
+    it.gpos = w.gpos;
+    it.bad_len = w.bad;
+    it.whole = w.u == 0 && units == w.c;
+    it.first = w.gpos == w.lo;
+    it.t0 = (int)min((long long)w.u * 128, (long long)w.n);
+    it.t1 = (int)min((long long)(w.u + units) * 128, (long long)w.n);
+    it.ntiles = (it.t1 - it.t0 + 127) / 128;
+    w.left -= units;
+    w.gpos += units;
+    w.u += units;
+    if (w.u == w.c) {
+        w.u = 0;
+        if (++w.g == w.gq) {
+            w.g = 0;
+            ++w.b;
+            if (w.left > 0) umma_walk_seq<B>(p, w, w.n_next);
+        }
+    }
+    return true;
 }
 
 // Non-blocking test of an mbarrier phase (try_wait may suspend the thread for
@@ -338,8 +467,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 
 template <int B, int G>
 __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
-    pa_decode_umma_kernel(const DecodeParams p, const int total_items,
-                          const __grid_constant__ CUtensorMap tmk,
+    pa_decode_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv) {
     pdl_trigger();
     pdl_wait();
@@ -367,6 +495,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    if (warp == 2) umma_schedule<B>(p, ctrl + C::SCHED_OFF, lane);
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
@@ -390,21 +519,23 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         const uint64_t policy = l2_policy_evict_first();
         int kt = 0, qi = 0;
         bool aborted = false;
-        for (int idx = blockIdx.x; idx < total_items && !aborted; idx += gridDim.x) {
-            UItem it;
-            const bool live = umma_item<B, G>(p, idx, it);
-            if (is_v && it.bad_len && it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
-                atomicOr(p.status, kStatusBadLength);
-            if (!live) continue;
+        UWalk w;
+        umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
+        UItem it;
+        while (!aborted && umma_walk_next<B, G>(p, w, it)) {
+            // (the piece at tile 0 of head group 0 reports for the sequence)
+            const bool reporter = is_v && it.g == 0 && it.u == 0 && lane == 0;
+            if (reporter && it.bad_len) atomicOr(p.status, kStatusBadLength);
             const int* bt_row = p.bt + (long long)it.b * p.maxb;
             if (p.new_k != nullptr) {
-                // fused append: the partition that owns the new row stores it
-                // (every head chunk its own identical copy) before its copies
+                // fused append: the piece holding the new row's tile (the
+                // first piece if the row lies past the context) stores it --
+                // every head chunk its own identical copy -- before its copies
                 const int pos = __ldg(p.positions + it.b);
                 if (pos < 0 || pos / B >= p.maxb) {
-                    if (is_v && it.c == 0 && it.kvh == 0 && it.hc == 0 && lane == 0)
-                        atomicOr(p.status, kStatusBadLength);
-                } else if (it.c == (pos < it.n ? (pos / B) / p.PB : 0)) {
+                    if (reporter) atomicOr(p.status, kStatusBadLength);
+                } else if (pos < it.n ? (pos / 128 >= it.u && pos / 128 < it.u + it.units)
+                                      : it.u == 0) {
                     const int blk = __ldg(bt_row + pos / B);
                     if (blk < 0 || blk >= p.num_blocks) {
                         if (is_v && lane == 0) atomicOr(p.status, kStatusBadBlock);
@@ -449,17 +580,22 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 if (lane == 0) mbar_arrive(bar0 + 8 * (C::Q_FULL + (qi & 1)));
             }
 
-            // 128-token tiles: lane r < 8 walks box r (16 rows) of the tile
+            // 128-token tiles: lane r < 8 walks box r (16 rows) of the tile; the
+            // block-table entries of tile i + 1 are loaded while tile i waits
+            // for its stage
+            auto box_block = [&](int i) {
+                const int tok = it.t0 + i * C::TT + 16 * lane;
+                return (i < it.ntiles && lane < C::NBOX && tok < it.t1) ? __ldg(bt_row + tok / B)
+                                                                        : 0;
+            };
+            int blk_next = box_block(0);
             for (int i = 0; i < it.ntiles; ++i, ++kt) {
                 const int stage = kt % NS;
                 const int use = kt / NS;
                 const int tok = it.t0 + i * C::TT + 16 * lane;
-                bool valid = false;
-                int blk = 0;
-                if (lane < C::NBOX && tok < it.t1) {
-                    blk = __ldg(bt_row + tok / B);
-                    valid = true;
-                }
+                bool valid = lane < C::NBOX && tok < it.t1;
+                const int blk = blk_next;
+                blk_next = box_block(i + 1);
                 // (every lane waits and votes: the warp leaves the loop together)
                 if (use > 0 && !__all_sync(kFullMask, umma_wait(empty0 + 8 * stage, (use - 1) & 1,
                                                                 abort_all, p.status))) {
@@ -510,7 +646,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             constexpr uint32_t IDQ = umma_idesc_bf16(128, G, 0, 0);
             constexpr uint32_t IDP = umma_idesc_bf16(128, C::PW, 1, 1);
             const uint32_t pbuf = sbase + C::OFF_P;
-            int idx_q = blockIdx.x;   // next item to look at
+            UWalk wq;
+            umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, wq);
             int tiles_left = 0;       // tiles of the current item still without S
             int i_q = 0, qi = -1;     // tile within the item; item (with tiles) count
             bool q_ready = false, done_q = false;
@@ -537,11 +674,10 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     progressed = true;
                 }
                 if (!done_q && kt_q < kt_pv + 2) {
-                    while (tiles_left == 0 && idx_q < total_items) {
+                    while (tiles_left == 0) {
                         UItem it;
-                        const bool live = umma_item<B, G>(p, idx_q, it);
-                        idx_q += gridDim.x;
-                        if (live && it.ntiles > 0) {
+                        if (!umma_walk_next<B, G>(p, wq, it)) break;
+                        if (it.ntiles > 0) {
                             tiles_left = it.ntiles;
                             i_q = 0;
                             ++qi;
@@ -625,10 +761,20 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         // at a named barrier the others have abandoned.
         bool failed = false;
         float lp[HG];  // this thread's share of the softmax denominators
-        for (int idx = blockIdx.x; idx < total_items && !stop; idx += gridDim.x) {
-            UItem it;
-            if (!umma_item<B, G>(p, idx, it)) continue;
+        UWalk w;
+        umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
+        UItem it;
+        while (!stop && umma_walk_next<B, G>(p, w, it)) {
             const long long head0 = (long long)it.b * p.H + it.hbase + h0;
+            if (it.u == 0 && warp == C::SM_WARP0 && lane == 0 && p.tc_desc != nullptr) {
+                // where the combine finds this pair's pieces: CTAs first ..
+                // first + pieces - 1 (the owners of its first and last unit)
+                const int pieces =
+                    it.whole ? 1
+                             : (int)((it.gpos + it.c - 1) * w.grid / w.T - blockIdx.x + 1);
+                p.tc_desc[(long long)it.b * w.gq + it.g] =
+                    make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
+            }
             if (it.ntiles == 0) {  // empty context: output 0 (one partition)
 #pragma unroll
                 for (int g = 0; g < HG; ++g) p.out[(head0 + g) * 128 + r] = 0.f;
@@ -791,7 +937,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             }
             if (sp < HG) {
                 const int h = h0 + sp;
-                a_sh[h] = (red[h] + red[G + h]) + (red[2 * G + h] + red[3 * G + h]);
+                const float L = (red[h] + red[G + h]) + (red[2 * G + h] + red[3 * G + h]);
+                a_sh[h] = L;
+                red[h] = L > 0.f ? 1.f / L : 0.f;  // one division per head
             }
             part_bar(part);
             __syncwarp();
@@ -805,10 +953,11 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 for (int g = 0; g < HG; ++g) {
                     const float o = __uint_as_float(vh[g]) + __uint_as_float(vl[g]);
                     const float L = a_sh[h0 + g];
-                    if (it.nparts == 1) {
-                        p.out[(head0 + g) * 128 + r] = L > 0.f ? o / L : 0.f;
+                    if (it.whole) {
+                        p.out[(head0 + g) * 128 + r] = o * red[h0 + g];
                     } else {
-                        const long long slot = (head0 + g) * p.Cmax + it.c;
+                        const long long slot =
+                            ((long long)blockIdx.x * 2 + (it.first ? 0 : 1)) * G + h0 + g;
                         p.part_o[slot * 128 + r] = o;
                         if (r == 0) {
                             p.part_ml[slot * 2 + 0] = m_sh[h0 + g];

@@ -59,6 +59,12 @@ struct DecodeParams {
     // tensor-core kernel only: the group (num_heads / Hkv) is served in
     // `nchunks` chunks of the kernel's compile-time G heads (1 unless G > 16)
     int gsize, nchunks;
+    // tcgen05 kernel only: its persistent grid, and (with tc_grid > 1) one
+    // int4 per (sequence, head group) {first CTA, pieces, slot of the first
+    // piece} that tells the combine where the pieces of a split context are;
+    // the partials then sit in part_o / part_ml as [CTA][2 slots][chunk head]
+    int tc_grid;
+    int4* tc_desc;
 };
 
 struct WriteParams {
