@@ -136,9 +136,9 @@ PA_API int pa_pool_destroy(pa_pool* pool);
  * 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
  *
  * Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
- * for bf16 pools the tcgen05 kernel for groups that are multiples of 64 (S and
- * O accumulate in tensor memory), else the mma.sync kernel (K/V staged by
- * tensor-map TMA); the CUDA-core kernel for fp32 pools.
+ * for bf16 pools with head_dim 128 the tcgen05 kernel for groups that are
+ * multiples of 16 (S and O accumulate in tensor memory), else the mma.sync
+ * kernel (K/V staged by tensor-map TMA); the CUDA-core kernel for fp32 pools.
  * PA_DECODE_CUDA_CORES forces the CUDA-core kernel (fp32 FMA on every dtype),
  * PA_DECODE_TENSOR_CORES the mma.sync kernel, PA_DECODE_TCGEN05 the tcgen05
  * kernel; a forced kernel that cannot serve a call makes it fail with

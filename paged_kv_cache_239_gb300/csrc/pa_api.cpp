@@ -140,10 +140,10 @@ struct DecodeShape {
 };
 
 // The kernel the pool's choice selects for group G, or a PA_ERR_UNSUPPORTED
-// failure.  Automatic: tcgen05 for groups that are multiples of 64 (head_dim
+// failure.  Automatic: tcgen05 for groups that are multiples of 16 (head_dim
 // 128), mma.sync for the other bf16 shapes, CUDA cores for fp32.  (GB300,
-// large-batch lengths: tcgen05 is 26 % faster than mma.sync at G = 64, level at
-// G = 32, slower at G = 16.)
+// large-batch lengths, GB/s tcgen05 / mma.sync: G = 64 3562 / 1593, G = 32
+// 4854 / 2884, G = 16 5906 / 5152; long context G = 16 5159 / 5181.)
 int pick_kernel(const pa_pool* pool, int G, Kernel* k) {
     const pa::PoolGeom& g = pool->g;
     const bool cuda_ok = pa::decode_supported(g.dtype, g.D, g.B, G);
@@ -175,10 +175,7 @@ int pick_kernel(const pa_pool* pool, int G, Kernel* k) {
             *k = Kernel::Tcgen05;
             return PA_OK;
         default:
-            *k = (umma_ok && G % 64 == 0) ? Kernel::Tcgen05
-                 : mma_ok                 ? Kernel::MmaSync
-                 : umma_ok                ? Kernel::Tcgen05
-                                          : Kernel::CudaCores;
+            *k = umma_ok ? Kernel::Tcgen05 : mma_ok ? Kernel::MmaSync : Kernel::CudaCores;
             return PA_OK;
     }
 }

@@ -12,28 +12,34 @@
 // G = 8 mma.sync keeps pace with HBM; from G = 16 it does not, and a tile with
 // 128 tokens x G heads is a real contraction.
 //
-// Structure: persistent CTAs (one per SM, ~225 KB of shared memory), each
-// working through (sequence, KV head, head chunk, partition) items, with
-// warp-specialised roles connected by mbarriers:
-//  * warp 0 (producer): block-table walk, fused append store, q of the item
-//    into a swizzled K-major tile (cp.async), and 5-D tensor-map TMA loads of
-//    128-token K and V tiles (8 boxes of 16 rows per 64-column half,
-//    SWIZZLE_128B) into a 3-stage ring;
+// Structure: persistent CTAs (one per SM, ~225 KB of shared memory).  The
+// call's work is cut into 128-token tiles of (sequence, head group) pairs and
+// every CTA takes an equal contiguous share of them (see the schedule below),
+// so ragged lengths cost no tail.  Warp-specialised roles connected by
+// mbarriers:
+//  * warp 0 (K producer): block-table walk (entries loaded a tile ahead), the
+//    fused append's K row, q of each piece into a swizzled K-major tile
+//    (cp.async, two buffers), and 5-D tensor-map TMA loads of 128-token K
+//    tiles (8 boxes of 16 rows per 64-column half, SWIZZLE_128B) into the K
+//    ring;
+//  * warp 2 (V producer): computes the CTA's share at start; the same walk for
+//    V tiles into the V ring, the fused append's V row, bad ids / lengths.
+//    A K stage is free as soon as S = K Q^T is done, a V stage only after
+//    P V, so the two rings are sized and released separately;
 //  * warp 1 (MMA): allocates TMEM; one thread issues
 //      S[128 tok x G]   = K[128 x 128] . Q^T          (A, B K-major in smem)
 //      O^T[128 d x 2G] += V^T[128 x 128 tok] . [P_hi | P_lo]  (A, B MN-major)
 //    polling the barriers of both without blocking on either, and signals
 //    completion with tcgen05.commit.  S is double-buffered in TMEM, so S of
 //    tile i+1 is computed while tile i's softmax runs;
-//  * warps 2-9 (softmax, 256 threads): two warps per TMEM lane quarter, each
-//    with half of the heads.  They read S (thread = token), run the online
-//    softmax in base 2 with a lazily raised running max (the max is raised,
-//    and O and the sums rescaled, only when a score exceeds it by more than
-//    2^8 -- any reference point gives the same normalised result), write P as
-//    bf16 hi + lo (|P - hi - lo| <= 2^-16 P) into the K half of the tile's own
-//    stage (dead once S is computed: one P buffer per stage), and at the end of
-//    an item read O^T (thread = head-dim element), add the hi and lo halves
-//    and store the output or the split partial.
+//  * warps 3 .. (softmax, 8 or 16 warps): 2 or 4 head parts per TMEM lane
+//    quarter.  They read S (thread = token), run the online softmax in base 2
+//    with a lazily raised running max (the max is raised, and O and the sums
+//    rescaled, only when a score exceeds it by more than 2^8 -- any reference
+//    point gives the same normalised result), write P as bf16 hi + lo
+//    (|P - hi - lo| <= 2^-16 P) into the one P buffer once the previous P V
+//    has read it, and at the end of a piece read O^T (thread = head-dim
+//    element), add the hi and lo halves and store the output or the partial.
 // Every wait is bounded (PA_STATUS_TIMEOUT); the roles then stop together,
 // wait for their copies and MMAs in flight, and TMEM is freed.
 #pragma once

@@ -1,5 +1,5 @@
 """The tcgen05 decode kernel (GQA groups that are multiples of 16 on bf16 pools
-with head_dim 128; the automatic choice for multiples of 64) against the
+with head_dim 128; the automatic choice for them) against the
 oracle: ragged lengths around the 128-token tile, every partition size, chunked
 groups, the fused append, many more work items than SMs (persistent CTAs),
 stale values past the context, bad ids / lengths, and replays of a captured
@@ -221,6 +221,37 @@ def test_graph_replays_match(cuda_device):
             g.replay()
             torch.cuda.synchronize()
             assert max_abs_err(out, oracle_decode(wl, pool, qs[t], 0)) <= TOL, t
+        assert B.pa_get_status() == 0
+    finally:
+        gp.close()
+
+
+@pytest.mark.parametrize("lens,H,Hkv", [
+    ([20000], 64, 1),                 # one context cut into a piece per CTA
+    ([1], 64, 1),                     # one unit: a single CTA has work
+    ([5000, 0, 3, 9000, 0], 128, 1),  # two 64-head chunks, empty contexts
+    ([700, 1500, 0, 129, 2047], 48, 1),   # three 16-head chunks
+    ([33000, 17, 128], 32, 2),        # long + short, two KV heads
+])
+def test_equal_tile_shares_split_anywhere(cuda_device, lens, H, Hkv):
+    """Every CTA takes an equal run of 128-token tiles in (sequence, head
+    group, tile) order, so contexts are cut at arbitrary tiles and merged by
+    the combine; the result must not depend on where the cuts fall."""
+    wl = W.custom("tcshare", "bf16", 1, H, Hkv, 128, 16, lens, seed=sum(lens) % 997 + H,
+                  spare_blocks=2, interleave=True)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    try:
+        B.pa_pool_set_decode_kernel(gp.h, B.PA_DECODE_TCGEN05)
+        sizes = {B.pa_decode_workspace_size(gp.h, wl.batch, H, wl.max_blocks, pb)
+                 for pb in (0, 1, wl.max_blocks)}
+        assert len(sizes) == 1, sizes   # partition_blocks does not apply to it
+        bt, ln = device_tables(wl, cuda_device)
+        ref = oracle_decode(wl, pool, q, 0)
+        _status_clear()
+        out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
+        assert max_abs_err(out, ref) <= TOL
         assert B.pa_get_status() == 0
     finally:
         gp.close()
