@@ -266,18 +266,23 @@ struct UmmaCfg {
 
 // Work schedule.  The unit of work is one 128-token tile of one (sequence b,
 // head group g) pair, g = kv head * nchunks + head chunk; a context of n
-// tokens has max(1, ceil(n / 128)) units (an empty one still owes its zero
-// output).  Units are ordered by b, then g, then tile, and CTA j of the
-// persistent grid takes the contiguous range [ceil(j T / grid), ceil((j + 1)
-// T / grid)) of the T units (grid <= T, so no range is empty): every CTA gets
-// the same number of tiles, whatever the mix of lengths.  A range covers whole
-// (b, g) pairs, except that its first and last piece may be parts of one that
-// neighbouring CTAs share; those write unnormalised partials into the CTA's
-// two slots (first piece slot 0, last slot 1) and the combine kernel merges
-// them, told where by the descriptor the first piece of each pair writes.
+// tokens has max(1, ceil(n / 128)) tiles (an empty one still owes its zero
+// output).  Every pair is charged kUmmaPieceUnits more units for the fixed
+// cost of starting and finishing a piece of it (q load, first-tile maximum,
+// output), placed before its tiles and doing no work.  Units are ordered by
+// b, then g, then position, and CTA j of the persistent grid takes the
+// contiguous range [ceil(j T / grid), ceil((j + 1) T / grid)) of the T units
+// (grid <= T): every CTA gets the same share of the work, whatever the mix of
+// lengths.  A range covers whole pairs, except that its first and last piece
+// may be parts of one that neighbouring CTAs share; those write unnormalised
+// partials into the CTA's two slots (first piece slot 0, last slot 1) and the
+// combine kernel merges them, told where by the descriptor the piece holding
+// tile 0 writes.
+constexpr int kUmmaPieceUnits = 3;
+
 struct UItem {
     int b, g, kvh, hc, hbase, n, c, u, units, t0, t1, ntiles;
-    long long gpos;          // global index of the piece's first unit
+    long long gpos;          // global index of the piece's first tile
     bool bad_len, whole, first;
 };
 
@@ -285,25 +290,35 @@ __device__ __forceinline__ int umma_units(int n, int maxtok) {
     return (n <= 0 || n > maxtok) ? 1 : (int)(((long long)n + 127) / 128);
 }
 
+// Units of the pairs of sequences b0 + 8 lane + k, k < 8 (0 past the batch).
+template <int B>
+__device__ __forceinline__ void umma_pair_units(const DecodeParams& p, int b0, int lane,
+                                                int (&cu)[8]) {
+    int nv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int b = b0 + 8 * lane + k;
+        nv[k] = b < p.batch ? __ldg(p.lens + b) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        cu[k] = b0 + 8 * lane + k < p.batch ? kUmmaPieceUnits + umma_units(nv[k], p.maxb * B) : 0;
+}
+
 // Computes this CTA's range (warp-wide; lane 0 stores it in `sched`):
 // [0] T, [8] grid (min(gridDim, T)), [16] first unit, [24] unit count,
-// [32] first b, [36] its g, [40] its tile.
+// [32] its b, [36] its g, [40] its offset within the pair.  A batch of up to
+// 256 sequences takes one round of loads (8 per lane).
 template <int B>
 __device__ __forceinline__ void umma_schedule(const DecodeParams& p, unsigned char* sched,
                                               int lane) {
-    const int maxtok = p.maxb * B;
     const long long Gq = (long long)p.Hkv * p.nchunks;
+    int cu[8];
     long long T = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 256) {
-        int nv[8];
+        umma_pair_units<B>(p, b0, lane, cu);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int b = b0 + 32 * k + lane;
-            nv[k] = b < p.batch ? __ldg(p.lens + b) : 0;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (b0 + 32 * k + lane < p.batch) T += umma_units(nv[k], maxtok);
+        for (int k = 0; k < 8; ++k) T += cu[k];
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(kFullMask, T, off);
@@ -311,30 +326,45 @@ __device__ __forceinline__ void umma_schedule(const DecodeParams& p, unsigned ch
     const long long grid = min((long long)gridDim.x, T);
     const long long j = blockIdx.x;
     long long lo = 0, cnt = 0;
-    int b_sel = 0, g_sel = 0, u_sel = 0;
+    int b_sel = 0, g_sel = 0, o_sel = 0;
     if (j < grid) {
         lo = (j * T + grid - 1) / grid;
         cnt = ((j + 1) * T + grid - 1) / grid - lo;
         long long P = 0;  // units before sequence b0
-        for (int b0 = 0; b0 < p.batch; b0 += 32) {
-            const int b = b0 + lane;
-            const long long cu = b < p.batch ? umma_units(__ldg(p.lens + b), maxtok) * Gq : 0;
-            long long incl = cu;
+        for (int b0 = 0; b0 < p.batch; b0 += 256) {
+            if (p.batch > 256) umma_pair_units<B>(p, b0, lane, cu);
+            long long mine = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mine += cu[k];
+            mine *= Gq;
+            long long incl = mine;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const long long v = __shfl_up_sync(kFullMask, incl, off);
                 if (lane >= off) incl += v;
             }
-            const unsigned hit = __ballot_sync(kFullMask, cu > 0 && P + incl - cu <= lo &&
-                                                              lo < P + incl);
+            const unsigned hit =
+                __ballot_sync(kFullMask, mine > 0 && P + incl - mine <= lo && lo < P + incl);
             if (hit) {
                 const int f = __ffs(hit) - 1;
-                const long long excl = __shfl_sync(kFullMask, incl - cu, f);
-                const long long cf = __shfl_sync(kFullMask, cu, f) / Gq;  // units per pair
-                const long long off = lo - P - excl;
-                b_sel = b0 + f;
-                g_sel = (int)(off / cf);
-                u_sel = (int)(off % cf);
+                if (lane == f) {
+                    long long pos = P + incl - mine;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const long long pc = (long long)cu[k] * Gq;
+                        if (cu[k] > 0 && lo < pos + pc) {
+                            const long long off = lo - pos;
+                            b_sel = b0 + 8 * lane + k;
+                            g_sel = (int)(off / cu[k]);
+                            o_sel = (int)(off % cu[k]);
+                            break;
+                        }
+                        pos += pc;
+                    }
+                }
+                b_sel = __shfl_sync(kFullMask, b_sel, f);
+                g_sel = __shfl_sync(kFullMask, g_sel, f);
+                o_sel = __shfl_sync(kFullMask, o_sel, f);
                 break;
             }
             P += __shfl_sync(kFullMask, incl, 31);
@@ -349,7 +379,7 @@ __device__ __forceinline__ void umma_schedule(const DecodeParams& p, unsigned ch
         s64[3] = cnt;
         s32[0] = b_sel;
         s32[1] = g_sel;
-        s32[2] = u_sel;
+        s32[2] = o_sel;
     }
 }
 
@@ -357,9 +387,10 @@ __device__ __forceinline__ void umma_schedule(const DecodeParams& p, unsigned ch
 // length of the next sequence is loaded one sequence ahead (under a full HBM
 // stream a dependent global load costs microseconds).
 struct UWalk {
-    int b, g, u, n, c, n_next, gq;
-    bool bad;
-    long long T, grid, lo, gpos, left;
+    int b, g, o, n, c, n_next;  // o: offset within the pair, overhead units first
+    bool bad, emitted;
+    long long gpos, left;
+    const long long* sched;  // T, grid, first unit (read where needed: registers are short)
 };
 
 template <int B>
@@ -376,22 +407,28 @@ __device__ __forceinline__ void umma_walk_begin(const DecodeParams& p, const uns
                                                 UWalk& w) {
     const long long* s64 = reinterpret_cast<const long long*>(sched);
     const int* s32 = reinterpret_cast<const int*>(sched + 32);
-    w.T = s64[0];
-    w.grid = s64[1];
-    w.lo = s64[2];
+    w.sched = s64;
     w.left = s64[3];
-    w.gpos = w.lo;
+    w.gpos = s64[2];
     w.b = s32[0];
     w.g = s32[1];
-    w.u = s32[2];
-    w.gq = p.Hkv * p.nchunks;
+    w.o = s32[2];
+    w.emitted = false;
     if (w.left > 0) umma_walk_seq<B>(p, w, __ldg(p.lens + w.b));
 }
 
 template <int B, int G>
 __device__ __forceinline__ bool umma_walk_next(const DecodeParams& p, UWalk& w, UItem& it) {
     if (w.left <= 0) return false;
-    const int units = (int)min((long long)(w.c - w.u), w.left);
+    if (w.o < kUmmaPieceUnits) {  // the pair's overhead units: nothing to do
+        const long long skip = min((long long)(kUmmaPieceUnits - w.o), w.left);
+        w.o += (int)skip;
+        w.gpos += skip;
+        w.left -= skip;
+        if (w.left <= 0) return false;
+    }
+    const int u = w.o - kUmmaPieceUnits;
+    const int units = (int)min((long long)(w.c - u), w.left);
     it.b = w.b;
     it.g = w.g;
     it.kvh = w.g / p.nchunks;
@@ -399,21 +436,22 @@ __device__ __forceinline__ bool umma_walk_next(const DecodeParams& p, UWalk& w, 
     it.hbase = it.kvh * p.gsize + it.hc * G;
     it.n = w.n;
     it.c = w.c;
-    it.u = w.u;
+    it.u = u;
     it.units = units;
     it.gpos = w.gpos;
     it.bad_len = w.bad;
-    it.whole = w.u == 0 && units == w.c;
-    it.first = w.gpos == w.lo;
-    it.t0 = (int)min((long long)w.u * 128, (long long)w.n);
-    it.t1 = (int)min((long long)(w.u + units) * 128, (long long)w.n);
+    it.whole = u == 0 && units == w.c;
+    it.first = !w.emitted;
+    w.emitted = true;
+    it.t0 = (int)min((long long)u * 128, (long long)w.n);
+    it.t1 = (int)min((long long)(u + units) * 128, (long long)w.n);
     it.ntiles = (it.t1 - it.t0 + 127) / 128;
     w.left -= units;
     w.gpos += units;
-    w.u += units;
-    if (w.u == w.c) {
-        w.u = 0;
-        if (++w.g == w.gq) {
+    w.o += units;
+    if (w.o == kUmmaPieceUnits + w.c) {
+        w.o = 0;
+        if (++w.g == p.Hkv * p.nchunks) {
             w.g = 0;
             ++w.b;
             if (w.left > 0) umma_walk_seq<B>(p, w, w.n_next);
@@ -777,8 +815,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 // first + pieces - 1 (the owners of its first and last unit)
                 const int pieces =
                     it.whole ? 1
-                             : (int)((it.gpos + it.c - 1) * w.grid / w.T - blockIdx.x + 1);
-                p.tc_desc[(long long)it.b * w.gq + it.g] =
+                             : (int)((it.gpos + it.c - 1) * w.sched[1] / w.sched[0] -
+                                     blockIdx.x + 1);
+                p.tc_desc[(long long)it.b * p.Hkv * p.nchunks + it.g] =
                     make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
             }
             if (it.ntiles == 0) {  // empty context: output 0 (one partition)
@@ -807,20 +846,19 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 }
                 const int tok = it.t0 + i * C::TT + r;
                 const bool valid = tok < it.t1 && !((meta[stage] >> (r >> 4)) & 1);
-                float mreg[HG];
+                // (the running maxima are read from shared memory where they
+                // are used: no thread of the part changes them before every
+                // thread has passed this tile's vote, and registers are short)
+                bool need = (i == 0);
 #pragma unroll
                 for (int g = 0; g < HG; g += 4) {
                     const float4 m4 = *reinterpret_cast<const float4*>(m_sh + h0 + g);
-                    mreg[g] = m4.x;
-                    mreg[g + 1] = m4.y;
-                    mreg[g + 2] = m4.z;
-                    mreg[g + 3] = m4.w;
-                }
-                bool need = (i == 0);
+                    const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-                for (int g = 0; g < HG; ++g) {
-                    x[g] = valid ? x[g] * p.qscale : -INFINITY;
-                    need |= x[g] > mreg[g] + 8.f;
+                    for (int e = 0; e < 4; ++e) {
+                        x[g + e] = valid ? x[g + e] * p.qscale : -INFINITY;
+                        need |= x[g + e] > mv[e] + 8.f;
+                    }
                 }
                 bool pv_waited = false;
                 if (part_bar_or(part, need | failed)) {
@@ -849,10 +887,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     }
                     part_bar(part);
 #pragma unroll
-                    for (int g = 0; g < HG; ++g) {
-                        lp[g] *= a_sh[h0 + g];
-                        mreg[g] = m_sh[h0 + g];
-                    }
+                    for (int g = 0; g < HG; ++g) lp[g] *= a_sh[h0 + g];
                     if (i > 0) {
                         // O (this item's earlier tiles) scaled by the same factors
                         if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)),
@@ -878,11 +913,16 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 // p = 2^(x - m) for this thread's token and heads (a head whose
                 // max is still -inf has only -inf scores here: p = 0)
 #pragma unroll
-                for (int g = 0; g < HG; ++g) {
-                    const float mm = mreg[g] == -INFINITY ? 0.f : mreg[g];
-                    const float pv = exp2f(x[g] - mm);
-                    lp[g] += pv;
-                    x[g] = pv;
+                for (int g = 0; g < HG; g += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4*>(m_sh + h0 + g);
+                    const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float mm = mv[e] == -INFINITY ? 0.f : mv[e];
+                        const float pv = exp2f(x[g + e] - mm);
+                        lp[g + e] += pv;
+                        x[g + e] = pv;
+                    }
                 }
                 // the one P buffer is free once the previous tile's P V is done
                 if (!pv_waited && kt > 0 &&
