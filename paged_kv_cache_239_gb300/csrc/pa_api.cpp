@@ -209,7 +209,9 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         out->G = G;
         out->kernel = kernel;
         out->PB = maxb;
-        out->Cmax = 2;
+        // (Cmax only sizes the combine: pieces per pair when all contexts are
+        // equally long -- fewer pairs than CTAs means long ones cut in many)
+        out->Cmax = pairs < grid ? (int)((grid + pairs - 1) / pairs) + 1 : 2;
         out->chunk = chunk;
         out->tc_grid = grid;
         out->ws_bytes = tc_workspace_bytes(grid, chunk, pool->g.D, pairs);
