@@ -230,11 +230,11 @@ struct UmmaCfg {
     static constexpr int OFF_P = OFF_V + SV * TILE;
     static constexpr int OFF_Q = OFF_P + P_BYTES;
     static constexpr int OFF_CTRL = OFF_Q + 2 * Q_BYTES;
-    // ctrl: mbarriers [0, 192) | V stage meta | TMEM address | abort flag | m[G] | alpha[G] |
+    // ctrl: mbarriers [0, 224) | TMEM address | abort flag | m[G] | alpha[G] |
     // red[4][G] | this CTA's schedule (48 bytes)
     static constexpr int SCHED_OFF = 256 + 6 * G * 4;
     static constexpr int CTRL_BYTES = SCHED_OFF + 48;
-    static constexpr int META_OFF = 192, TMEM_SLOT_OFF = 224, ABORT_OFF = 228;
+    static constexpr int TMEM_SLOT_OFF = 224, ABORT_OFF = 228;
     static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
     // warps: 0 K producer (+ q), 1 MMA, 2 V producer, 3 .. 10 softmax (4 lane
     // quarters x 2 head parts: more than one warp per scheduler, so the
@@ -257,8 +257,7 @@ struct UmmaCfg {
 
     static_assert(G == 16 || G == 32 || G == 64, "head chunk of 16, 32 or 64");
     static_assert(B == 16 || B == 32, "block size 16 or 32");
-    static_assert(NBAR * 8 <= META_OFF, "barriers");
-    static_assert(META_OFF + 4 * SV <= TMEM_SLOT_OFF, "stage meta");
+    static_assert(NBAR * 8 <= TMEM_SLOT_OFF, "barriers");
     static_assert(2 * G + PW <= TMEM_COLS, "TMEM columns");
     static_assert(HG == 8 || HG % 16 == 0, "TMEM loads of 8 or 16k columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -522,7 +521,6 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
     unsigned char* smem = smem_raw + (sbase - raw_addr);
     unsigned char* ctrl = smem + C::OFF_CTRL;
     const uint32_t bar0 = sbase + C::OFF_CTRL;
-    int* meta = reinterpret_cast<int*>(ctrl + C::META_OFF);         // bad-box mask per V stage
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + C::TMEM_SLOT_OFF);
     volatile int* abort_all = reinterpret_cast<volatile int*>(ctrl + C::ABORT_OFF);
     float* m_sh = reinterpret_cast<float*>(ctrl + 256);             // running max per head
@@ -563,10 +561,23 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         const uint64_t policy = l2_policy_evict_first();
         int kt = 0, qi = 0;
         bool aborted = false;
+        // block-table entry of box `lane` of tile i of a piece (0 if none)
+        auto box_block = [&](const UItem& pc, int i) {
+            const int tok = pc.t0 + i * C::TT + 16 * lane;
+            return (i < pc.ntiles && lane < C::NBOX && tok < pc.t1)
+                       ? __ldg(p.bt + (long long)pc.b * p.maxb + tok / B)
+                       : 0;
+        };
         UWalk w;
         umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
-        UItem it;
-        while (!aborted && umma_walk_next<B, G>(p, w, it)) {
+        UItem it, nx;
+        bool have = umma_walk_next<B, G>(p, w, it);
+        int blk_first = have ? box_block(it, 0) : 0;
+        while (have && !aborted) {
+            // one piece ahead: the next piece's first table entries are loaded
+            // now, so its first copies need not wait for them
+            const bool have_nx = umma_walk_next<B, G>(p, w, nx);
+            const int blk_first_nx = have_nx ? box_block(nx, 0) : 0;
             // (the piece at tile 0 of head group 0 reports for the sequence)
             const bool reporter = is_v && it.g == 0 && it.u == 0 && lane == 0;
             if (reporter && it.bad_len) atomicOr(p.status, kStatusBadLength);
@@ -598,48 +609,18 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 }
                 __syncwarp();
             }
-            if (it.ntiles == 0) continue;
-
-            if (!is_v) {
-                // q of the item's G heads -> K-major swizzled tile [half][G][128 B]
-                // (buffer qi & 1: free once the last S of item qi - 2 is done)
-                if (qi >= 2 &&
-                    !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + (qi & 1)),
-                                                     ((qi >> 1) - 1) & 1, abort_all, p.status))) {
-                    aborted = true;
-                    break;
-                }
-                const uint32_t qbuf = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
-                const uint4* qsrc = reinterpret_cast<const uint4*>(
-                    static_cast<const unsigned short*>(p.q) +
-                    ((long long)it.b * p.H + it.hbase) * 128);
-#pragma unroll
-                for (int i = lane; i < G * 16; i += 32) {
-                    const int g = i >> 4, c16 = i & 15;
-                    cp_async16(qbuf + (c16 >> 3) * (G * 128) + sw128(g, c16), qsrc + i);
-                }
-                cp_async_wait_all();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar0 + 8 * (C::Q_FULL + (qi & 1)));
-            }
 
             // 128-token tiles: lane r < 8 walks box r (16 rows) of the tile; the
             // block-table entries of tile i + 1 are loaded while tile i waits
             // for its stage
-            auto box_block = [&](int i) {
-                const int tok = it.t0 + i * C::TT + 16 * lane;
-                return (i < it.ntiles && lane < C::NBOX && tok < it.t1) ? __ldg(bt_row + tok / B)
-                                                                        : 0;
-            };
-            int blk_next = box_block(0);
+            int blk_next = blk_first;
             for (int i = 0; i < it.ntiles; ++i, ++kt) {
                 const int stage = kt % NS;
                 const int use = kt / NS;
                 const int tok = it.t0 + i * C::TT + 16 * lane;
                 bool valid = lane < C::NBOX && tok < it.t1;
                 const int blk = blk_next;
-                blk_next = box_block(i + 1);
+                blk_next = box_block(it, i + 1);
                 // (every lane waits and votes: the warp leaves the loop together)
                 if (use > 0 && !__all_sync(kFullMask, umma_wait(empty0 + 8 * stage, (use - 1) & 1,
                                                                 abort_all, p.status))) {
@@ -652,10 +633,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 const unsigned bmask = __ballot_sync(kFullMask, bad);
                 const uint32_t fb = full0 + 8 * stage;
                 if (lane == 0) {
-                    if (is_v) {
-                        if (bmask) atomicOr(p.status, kStatusBadBlock);
-                        meta[stage] = (int)bmask;
-                    }
+                    if (is_v && bmask) atomicOr(p.status, kStatusBadBlock);
                     mbar_arrive_expect_tx(fb, (uint32_t)__popc(vmask) * 2u * 2048u);
                 }
                 __syncwarp();
@@ -671,8 +649,37 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     tma_load_5d(dst, tm, fb, 0, row0, o2, o3, o4, policy);
                     tma_load_5d(dst + C::HALF, tm, fb, 64, row0, o2, o3, o4, policy);
                 }
+                if (!is_v && i == 0) {
+                    // q of the piece's G heads -> K-major swizzled tile
+                    // [half][G][128 B], once its first K copy is on its way
+                    // (buffer qi & 1: free once the last S of piece qi - 2 is done)
+                    if (qi >= 2 &&
+                        !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + (qi & 1)),
+                                                         ((qi >> 1) - 1) & 1, abort_all,
+                                                         p.status))) {
+                        aborted = true;
+                        ++kt;  // (tile 0's copy is in flight: the exit path waits for it)
+                        break;
+                    }
+                    const uint32_t qbuf = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
+                    const uint4* qsrc = reinterpret_cast<const uint4*>(
+                        static_cast<const unsigned short*>(p.q) +
+                        ((long long)it.b * p.H + it.hbase) * 128);
+#pragma unroll
+                    for (int j = lane; j < G * 16; j += 32) {
+                        const int g = j >> 4, c16 = j & 15;
+                        cp_async16(qbuf + (c16 >> 3) * (G * 128) + sw128(g, c16), qsrc + j);
+                    }
+                    cp_async_wait_all();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar0 + 8 * (C::Q_FULL + (qi & 1)));
+                }
             }
-            if (!aborted) ++qi;
+            if (!aborted && it.ntiles > 0) ++qi;
+            it = nx;
+            have = have_nx;
+            blk_first = blk_first_nx;
         }
         if (aborted || *abort_all) {
             // copies still in flight land before the CTA can exit
@@ -827,12 +834,21 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             }
 #pragma unroll
             for (int g = 0; g < HG; ++g) lp[g] = 0.f;
+            // this thread's token's block id, a tile ahead: a token past the
+            // context or in a bad block gets no weight (the producers skip the
+            // same boxes)
+            const int* bt_row = p.bt + (long long)it.b * p.maxb;
+            auto tok_block = [&](int i) {
+                const int tok = it.t0 + i * C::TT + r;
+                return (i < it.ntiles && tok < it.t1) ? __ldg(bt_row + tok / B) : -1;
+            };
+            int blk_next = tok_block(0);
             for (int i = 0; i < it.ntiles; ++i, ++kt) {
-                const int stage = kt % C::SV;  // V stage (and its meta)
-                bool ok = umma_wait(bar0 + 8 * (C::S_FULL + (kt & 1)), (kt >> 1) & 1, abort_all,
-                                    p.status);
-                ok = ok && umma_wait(bar0 + 8 * (C::V_FULL + stage), (kt / C::SV) & 1,
-                                     abort_all, p.status);
+                const int stage = kt % C::SV;  // V stage
+                const int blk = blk_next;
+                blk_next = tok_block(i + 1);
+                const bool ok = umma_wait(bar0 + 8 * (C::S_FULL + (kt & 1)), (kt >> 1) & 1,
+                                          abort_all, p.status);
                 failed = failed || !ok;
                 __syncwarp();
                 tc_fence_after();
@@ -845,7 +861,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     for (int j = 0; j < HG; ++j) x[j] = __uint_as_float(v[j]);
                 }
                 const int tok = it.t0 + i * C::TT + r;
-                const bool valid = tok < it.t1 && !((meta[stage] >> (r >> 4)) & 1);
+                const bool valid = tok < it.t1 && blk >= 0 && blk < p.num_blocks;
                 // (the running maxima are read from shared memory where they
                 // are used: no thread of the part changes them before every
                 // thread has passed this tile's vote, and registers are short)
@@ -928,6 +944,12 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 if (!pv_waited && kt > 0 &&
                     !umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1,
                                abort_all, p.status))
+                    failed = true;
+                // V of this tile must have landed before its invalid rows are
+                // zeroed (only the rows' own threads need it, but all wait so
+                // that the tile's stage is in place before P is published)
+                if (!umma_wait(bar0 + 8 * (C::V_FULL + stage), (kt / C::SV) & 1, abort_all,
+                               p.status))
                     failed = true;
                 if (!valid && h0 == 0) {
                     // rows past the context (or of a bad block) hold stale or
