@@ -68,13 +68,13 @@ def decode_flops(wl) -> int:
 
 # DRAM bytes (read + write) of one layer's pa_write_kv_and_decode call on this
 # workload: pa_decode_mma_kernel with the fused append (ncu --set full:
-# 2,231,476,224 read + 6,231,296 written) + pa_combine_kernel (ncu dram
-# metrics: 9,852,160 read, 0 written), see
+# 2,231,387,904 read + 6,593,792 written) + pa_combine_kernel (ncu dram
+# metrics: 9,857,024 read, 0 written), see
 # profiles/; valid only for the sources they were taken from (the kernels, the
 # shared device code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231476224 + 6231296 + 9852160,
-    "sources_sha256": "cefec597a1ea571eacdf310c8353efcd72156f9bac999b81bdb74bfd85b3ae68",
+    "bytes_per_launch": 2231387904 + 6593792 + 9857024,
+    "sources_sha256": "5ad7564c56ca78af29784c89f69335393e5d0248ec3e0df37bae2a1d1ffbf53d",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h", "pa_api.cpp", "pa_fused_append.cuh"]
