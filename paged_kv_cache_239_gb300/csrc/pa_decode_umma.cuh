@@ -220,9 +220,9 @@ struct UmmaCfg {
     // and waits for it only before writing P.
     static constexpr int PW = 2 * G < 64 ? 64 : 2 * G;
     static constexpr int P_BYTES = (PW / 64) * HALF;
-    static constexpr int Q_BYTES = 2 * G * 128;     // q of one item, two 64-column halves
-                                                    // (two buffers: the next item's q
-                                                    // lands while this item's S runs)
+    static constexpr int Q_BYTES = 2 * G * 128;     // q of one piece, two 64-column halves
+                                                    // (two buffers: the next piece's q
+                                                    // lands while this piece's S runs)
     static constexpr int O_COL = 2 * G;             // TMEM: S0 [0, G), S1 [G, 2G), O^T after
     static constexpr int TMEM_COLS = (2 * G + PW) <= 32 ? 32 : (2 * G + PW) <= 64 ? 64
                                    : (2 * G + PW) <= 128 ? 128 : (2 * G + PW) <= 256 ? 256 : 512;
@@ -549,9 +549,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
 
     if (warp == 0 || warp == 2) {
         // ============================= producers: warp 0 K (and q), warp 2 V
-        // Both walk the same items and table entries.  The fused append's new
+        // Both walk the same pieces and table entries.  The fused append's new
         // row is stored by each producer for its own half (K or V) before that
-        // producer's copies of the item; warp 2 reports bad ids and lengths.
+        // producer's copies of the piece; warp 2 reports bad ids and lengths.
         const bool is_v = (warp == 2);
         const CUtensorMap* tm = is_v ? &tmv : &tmk;
         const int NS = is_v ? C::SV : C::SK;
@@ -699,11 +699,11 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             const uint32_t pbuf = sbase + C::OFF_P;
             UWalk wq;
             umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, wq);
-            int tiles_left = 0;       // tiles of the current item still without S
-            int i_q = 0, qi = -1;     // tile within the item; item (with tiles) count
+            int tiles_left = 0;       // tiles of the current piece still without S
+            int i_q = 0, qi = -1;     // tile within the piece; piece (with tiles) count
             bool q_ready = false, done_q = false;
             int kt_q = 0, kt_pv = 0;
-            unsigned first_bits = 0;  // bit (tile & 1): the tile is its item's first
+            unsigned first_bits = 0;  // bit (tile & 1): the tile is its piece's first
             unsigned long long idle_since = 0;
             while (true) {
                 bool progressed = false;
@@ -827,7 +827,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 p.tc_desc[(long long)it.b * p.Hkv * p.nchunks + it.g] =
                     make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
             }
-            if (it.ntiles == 0) {  // empty context: output 0 (one partition)
+            if (it.ntiles == 0) {  // empty context: output 0 (always a whole piece)
 #pragma unroll
                 for (int g = 0; g < HG; ++g) p.out[(head0 + g) * 128 + r] = 0.f;
                 continue;
@@ -905,7 +905,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
 #pragma unroll
                     for (int g = 0; g < HG; ++g) lp[g] *= a_sh[h0 + g];
                     if (i > 0) {
-                        // O (this item's earlier tiles) scaled by the same factors
+                        // O (this piece's earlier tiles) scaled by the same factors
                         if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)),
                                        ((kt - 1) >> 1) & 1, abort_all, p.status))
                             failed = true;
@@ -988,7 +988,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             }
             if (stop) break;
 
-            // ---- item epilogue: denominators, O = O_hi + O_lo, output ----
+            // ---- piece epilogue: denominators, O = O_hi + O_lo, output ----
 #pragma unroll
             for (int g = 0; g < HG; ++g) {
                 float v = lp[g];

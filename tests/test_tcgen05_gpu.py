@@ -255,3 +255,46 @@ def test_equal_tile_shares_split_anywhere(cuda_device, lens, H, Hkv):
         assert B.pa_get_status() == 0
     finally:
         gp.close()
+
+
+def test_workspace_reused_across_calls_and_checked(cuda_device):
+    """The per-CTA partial slots and the pair descriptors need no clearing: a
+    workspace left by a call with other lengths (more pieces, other cuts) gives
+    the same results; a workspace one byte short is refused before launch."""
+    lens_a = [20000, 3, 0, 5000]
+    lens_b = [129, 7000, 1, 0, 16000, 640]
+    H = 64
+    wl = W.custom("tcreuse", "bf16", 1, H, 1, 128, 16, lens_a + lens_b, seed=404,
+                  spare_blocks=2, interleave=True)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    try:
+        B.pa_pool_set_decode_kernel(gp.h, B.PA_DECODE_TCGEN05)
+        need = B.pa_decode_workspace_size(gp.h, wl.batch, H, wl.max_blocks, 0)
+        assert need > 0
+        ws = torch.full((need,), 0xA5, dtype=torch.uint8, device=cuda_device)
+        ref = oracle_decode(wl, pool, q, 0)
+        na = len(lens_a)
+        # first call: the first sequences only (same tables), then all of them
+        tables = torch.from_numpy(wl.block_tables).to(cuda_device)
+        lens = torch.from_numpy(wl.context_lens).to(cuda_device)
+        qd = q.to(cuda_device)
+        _status_clear()
+        for rows in (slice(0, na), slice(0, wl.batch)):
+            nb = rows.stop
+            out = torch.full((nb, H, 128), float("nan"), device=cuda_device)
+            B.pa_decode_attention_partitioned(out, qd[rows].contiguous(), gp.h, 0,
+                                              tables[rows].contiguous(), wl.max_blocks,
+                                              lens[rows].contiguous(), nb, 16, H, 1, 128,
+                                              wl.scale, 0, ws, need)
+            torch.cuda.synchronize()
+            assert max_abs_err(out, ref[:nb]) <= TOL, nb
+        assert B.pa_get_status() == 0
+        out = torch.zeros((wl.batch, H, 128), device=cuda_device)
+        with pytest.raises(B.PagedAttnError) as e:
+            B.pa_decode_attention_partitioned(out, qd, gp.h, 0, tables, wl.max_blocks, lens,
+                                              wl.batch, 16, H, 1, 128, wl.scale, 0, ws, need - 1)
+        assert e.value.code == B.PA_ERR_WORKSPACE
+    finally:
+        gp.close()

@@ -30,9 +30,10 @@ def _noalloc(gp, q, layer, bt, ln, partition_blocks):
     return out
 
 
-@pytest.mark.parametrize("partition_blocks", [3, 0])
-def test_noalloc_matches_workspace_entry_point(cuda_device, partition_blocks):
-    wl = W.custom("noalloc", "bf16", 2, 32, 8, 128, 32, [4000, 9000, 1, 700, 0, 2048, 33],
+@pytest.mark.parametrize("partition_blocks,H,Hkv", [(3, 32, 8), (0, 32, 8),
+                                                    (0, 64, 1), (0, 32, 2)])  # last two: tcgen05
+def test_noalloc_matches_workspace_entry_point(cuda_device, partition_blocks, H, Hkv):
+    wl = W.custom("noalloc", "bf16", 2, H, Hkv, 128, 32, [4000, 9000, 1, 700, 0, 2048, 33],
                   seed=77, spare_blocks=9)
     pool = W.make_pool(wl)
     qs = W.make_queries(wl, 2)
