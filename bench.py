@@ -62,6 +62,13 @@ def append_bytes(wl) -> int:
     return 2 * 2 * wl.batch * wl.num_kv_heads * wl.head_dim * wl.elem_bytes + wl.batch * 4
 
 
+def kernel_name(B, kind: int) -> str:
+    """The decode kernel's name for a PA_DECODE_* kind."""
+    return {B.PA_DECODE_CUDA_CORES: "pa_decode_kernel",
+            B.PA_DECODE_TENSOR_CORES: "pa_decode_mma_kernel",
+            B.PA_DECODE_TCGEN05: "pa_decode_umma_kernel"}[kind]
+
+
 def decode_flops(wl) -> int:
     return int(wl.context_lens.astype(np.int64).sum()) * 4 * wl.num_heads * wl.head_dim
 
@@ -306,6 +313,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                          wl.head_dim, pool.dtype)
     pb = B.pa_decode_partition_blocks(h, wl.batch, wl.num_heads, wl.max_blocks)
     ws_bytes = B.pa_decode_workspace_size(h, wl.batch, wl.num_heads, wl.max_blocks, 0)
+    kernel_kind = B.pa_decode_kernel_choice(h, wl.num_heads)
+    decode_kernel = kernel_name(B, kernel_kind)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     outs = torch.empty((L, wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -552,7 +561,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             "cuda_graph": use_graph,
             "append": ("fused into the decode launch (pa_write_kv_and_decode)" if args.fused
                        else "separate pa_write_kv launch before each decode"),
-            "pool_gb": round(wl.pool_bytes() / 1e9, 1), "partition_blocks": pb,
+            "pool_gb": round(wl.pool_bytes() / 1e9, 1),
+            "decode_kernel": decode_kernel,
+            "partition_blocks": (pb if kernel_kind != B.PA_DECODE_TCGEN05 else
+                                 "none: equal 128-token tile shares per persistent CTA"),
             "l2": l2_note(wl, L),
             "parallelism": f"replicas x{world}",
         },
@@ -567,8 +579,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                      "traffic": (decode_traffic() if args.workload == WORKLOAD_CFG and
                                  args.kv_heads <= 0 and args.num_heads <= 0 and args.fused
                                  else None),
-                     "traffic_kernel": "pa_decode_mma_kernel (with the fused append) + "
-                                       "pa_combine_kernel, ncu dram read+write per call",
+                     "traffic_kernel": (decode_kernel + (" (with the fused append)" if args.fused
+                                                       else "") +
+                                        " + pa_combine_kernel, ncu dram read+write per call"),
                      "algorithmic_bytes_per_call": launch_bytes,
                      "avg_call_ms": call_avg_ms,
                      "timing": ("CUDA events around every decode call, recorded as event nodes "

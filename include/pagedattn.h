@@ -160,6 +160,14 @@ enum {
 };
 PA_API int pa_pool_set_decode_kernel(pa_pool* pool, int kind);
 
+/* The decode kernel that a decode call with `num_heads` query heads runs on
+ * this pool under its current choice: PA_DECODE_CUDA_CORES,
+ * PA_DECODE_TENSOR_CORES or PA_DECODE_TCGEN05 in *kind.  PA_ERR_UNSUPPORTED
+ * (with the reason) when no kernel serves the shape or the forced one cannot;
+ * PA_ERR_INVALID_ARG when num_heads is not a positive multiple of the pool's
+ * KV heads.  Host only: touches no device. */
+PA_API int pa_decode_kernel_choice(const pa_pool* pool, int num_heads, int* kind);
+
 /* Bytes of one physical block: 2 * num_layers * num_kv_heads * block_size *
  * head_dim * element size (K and V of every layer and KV head). */
 PA_API int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes);

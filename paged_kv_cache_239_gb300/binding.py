@@ -81,6 +81,7 @@ _SIGNATURES = {
     "pa_pool_destroy": ([_P], _I),
     "pa_pool_block_bytes": ([_P, _PSZ], _I),
     "pa_pool_set_decode_kernel": ([_P, _I], _I),
+    "pa_decode_kernel_choice": ([_P, _I, _PI], _I),
     "pa_pool_seed_free_stack": ([_P, _P, _I], _I),
     "pa_alloc_block": ([_P, _PI], _I),
     "pa_free_block": ([_P, _I], _I),
@@ -210,6 +211,13 @@ def pa_pool_destroy(pool: int) -> None:
 
 def pa_pool_set_decode_kernel(pool: int, kind: int) -> None:
     _check(lib().pa_pool_set_decode_kernel(pool, kind), "pa_pool_set_decode_kernel")
+
+
+def pa_decode_kernel_choice(pool: int, num_heads: int) -> int:
+    v = ctypes.c_int()
+    _check(lib().pa_decode_kernel_choice(pool, num_heads, ctypes.byref(v)),
+           "pa_decode_kernel_choice")
+    return v.value
 
 
 def pa_pool_block_bytes(pool: int) -> int:

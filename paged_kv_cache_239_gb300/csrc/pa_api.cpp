@@ -382,6 +382,20 @@ int pa_pool_set_decode_kernel(pa_pool* pool, int kind) {
     return PA_OK;
 }
 
+int pa_decode_kernel_choice(const pa_pool* pool, int num_heads, int* kind) {
+    if (int rc = check_pool(pool)) return rc;
+    if (!kind) return fail(PA_ERR_INVALID_ARG, "kind is NULL");
+    if (num_heads <= 0 || num_heads % pool->g.Hkv != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_heads %d is not a positive multiple of num_kv_heads %d",
+                    num_heads, pool->g.Hkv);
+    Kernel k = Kernel::CudaCores;
+    if (int rc = pick_kernel(pool, num_heads / pool->g.Hkv, &k)) return rc;
+    *kind = k == Kernel::Tcgen05   ? PA_DECODE_TCGEN05
+            : k == Kernel::MmaSync ? PA_DECODE_TENSOR_CORES
+                                   : PA_DECODE_CUDA_CORES;
+    return PA_OK;
+}
+
 int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes) {
     if (int rc = check_pool(pool)) return rc;
     if (!bytes) return fail(PA_ERR_INVALID_ARG, "bytes is NULL");

@@ -208,6 +208,44 @@ def test_strided_pool_checks(pa_lib):
         assert e.value.code == pa_lib.PA_ERR_INVALID_ARG, args
 
 
+def test_decode_kernel_choice_query(pa_lib):
+    """Which kernel a call runs (host only): automatic choice by dtype, head_dim
+    and group; forced kinds that cannot serve the shape are refused."""
+    L = pa_lib
+    cases = [  # (Hkv, D, dtype, num_heads, automatic kernel)
+        (2, 64, 1, 16, L.PA_DECODE_TENSOR_CORES),    # bf16, group 8
+        (2, 128, 1, 8, L.PA_DECODE_TENSOR_CORES),    # bf16, group 4
+        (1, 128, 1, 16, L.PA_DECODE_TCGEN05),        # bf16, head_dim 128, group 16
+        (2, 128, 1, 128, L.PA_DECODE_TCGEN05),       # group 64
+        (1, 128, 1, 24, L.PA_DECODE_TENSOR_CORES),   # group 24: not a multiple of 16
+        (1, 64, 1, 32, L.PA_DECODE_TENSOR_CORES),    # head_dim 64: no tcgen05
+        (2, 64, 0, 8, L.PA_DECODE_CUDA_CORES),       # fp32
+    ]
+    for Hkv, D, dtype, H, want in cases:
+        h = _pool(pa_lib, Hkv=Hkv, D=D, dtype=dtype)
+        try:
+            assert L.pa_decode_kernel_choice(h, H) == want, (Hkv, D, dtype, H)
+            L.pa_pool_set_decode_kernel(h, L.PA_DECODE_CUDA_CORES)
+            if H // Hkv in (1, 2, 4, 8):
+                assert L.pa_decode_kernel_choice(h, H) == L.PA_DECODE_CUDA_CORES
+            else:
+                with pytest.raises(L.PagedAttnError) as e:
+                    L.pa_decode_kernel_choice(h, H)
+                assert e.value.code == L.PA_ERR_UNSUPPORTED
+            L.pa_pool_set_decode_kernel(h, L.PA_DECODE_TCGEN05)
+            if want == L.PA_DECODE_TCGEN05:
+                assert L.pa_decode_kernel_choice(h, H) == L.PA_DECODE_TCGEN05
+            else:
+                with pytest.raises(L.PagedAttnError) as e:
+                    L.pa_decode_kernel_choice(h, H)
+                assert e.value.code == L.PA_ERR_UNSUPPORTED
+            with pytest.raises(L.PagedAttnError) as e:
+                L.pa_decode_kernel_choice(h, H + 1 if Hkv > 1 else 0)
+            assert e.value.code == L.PA_ERR_INVALID_ARG
+        finally:
+            L.pa_pool_destroy(h)
+
+
 def test_decode_kernel_choice_checks(pa_lib):
     h = _pool(pa_lib)
     try:
