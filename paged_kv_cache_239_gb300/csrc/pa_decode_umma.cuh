@@ -513,7 +513,6 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
     pa_decode_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv) {
     pdl_trigger();
-    pdl_wait();
     using C = UmmaCfg<B, G>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_addr(smem_raw);
@@ -537,11 +536,14 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
-    if (warp == 2) umma_schedule<B>(p, ctrl + C::SCHED_OFF, lane);
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
     }
+    // (nothing above reads what the previous kernel may have written: the
+    // set-up overlaps its tail)
+    pdl_wait();
+    if (warp == 2) umma_schedule<B>(p, ctrl + C::SCHED_OFF, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -878,11 +880,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 }
                 bool pv_waited = false;
                 if (part_bar_or(part, need | failed)) {
-                    if (part_bar_or(part, failed)) {
-                        stop = true;
-                        break;
-                    }
-                    // raise the running max to this tile's max (per head)
+                    // raise the running max to this tile's max (per head); the
+                    // barrier that publishes the warps' maxima also decides
+                    // whether the part stops
 #pragma unroll
                     for (int g = 0; g < HG; ++g) {
                         float v = x[g];
@@ -891,7 +891,10 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                             v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
                         if (lane == 0) red[qd * G + h0 + g] = v;
                     }
-                    part_bar(part);
+                    if (part_bar_or(part, failed)) {
+                        stop = true;
+                        break;
+                    }
                     if (sp < HG) {
                         const int h = h0 + sp;
                         const float mt = fmaxf(fmaxf(red[h], red[G + h]),
