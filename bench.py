@@ -74,14 +74,15 @@ def decode_flops(wl) -> int:
 
 
 # DRAM bytes (read + write) of one layer's pa_write_kv_and_decode call on this
-# workload: pa_decode_mma_kernel with the fused append (ncu --set full:
-# 2,231,387,904 read + 6,593,792 written) + pa_combine_kernel (ncu dram
-# metrics: 9,857,024 read, 0 written), see
-# profiles/; valid only for the sources they were taken from (the kernels, the
-# shared device code, and the dispatch / partition choice in pa_api.cpp).
+# workload, one ncu capture of both kernels of the call (--metrics
+# dram__bytes_read.sum,dram__bytes_write.sum): pa_decode_mma_kernel with the
+# fused append 2,231,260,160 read + 6,223,104 written, pa_combine_kernel
+# 9,856,000 read + 0 written; see profiles/.  Valid only for the sources they
+# were taken from (the kernels, the shared device code, and the dispatch /
+# partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231387904 + 6593792 + 9857024,
-    "sources_sha256": "5ad7564c56ca78af29784c89f69335393e5d0248ec3e0df37bae2a1d1ffbf53d",
+    "bytes_per_launch": 2231260160 + 6223104 + 9856000,
+    "sources_sha256": "de4596a6aef044b0a42b301d7ceb33bd5f7d1e6bbd0763a2e6386a2749048f9e",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h", "pa_api.cpp", "pa_fused_append.cuh"]
