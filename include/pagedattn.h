@@ -274,7 +274,9 @@ PA_API int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
  *                 need no initialisation; concurrent calls need separate workspaces.
  * The context of each (sequence, KV head) is split into partitions of a
  * heuristically chosen number of blocks; with more than one partition a second
- * kernel merges the per-partition results (log-sum-exp combine).
+ * kernel merges the per-partition results (log-sum-exp combine).  The tcgen05
+ * kernel instead cuts the batch's 128-token tiles into equal shares per SM
+ * (see PA_DECODE_TCGEN05) and the same combine merges the cut contexts.
  */
 PA_API int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int layer,
                         const int* block_tables, int max_blocks_per_seq,
@@ -286,7 +288,8 @@ PA_API int pa_decode_attention(float* out, const void* q, const pa_pool* pool, i
  * pa_decode_attention with an explicit partition size: `partition_blocks`
  * physical blocks per partition (>= 1), or 0 for the heuristic choice.
  * A partition covering the whole table (partition_blocks >= max_blocks_per_seq)
- * runs a single kernel and needs no workspace.
+ * runs a single kernel and needs no workspace.  The tcgen05 kernel ignores
+ * partition_blocks (its split depends on the lengths only).
  */
 PA_API int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
                                     const int* block_tables, int max_blocks_per_seq,
