@@ -503,6 +503,38 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Max (or sum) of v[j] over the warp's 32 lanes for each of N = 2^k values,
+// as a reduce-scatter butterfly: at each step a lane sends the half of its
+// values it does not keep, so N + N/2 + ... shuffles become N - 1 + 5 - log2 N
+// (16 values: 16 shuffles instead of 80).  Lane l ends with value
+// l / (32 / N)'s result (lanes that differ in their low 5 - log2 N bits hold
+// the same one).
+template <int N, bool MAX>
+__device__ __forceinline__ float warp_scatter_reduce(const float (&in)[N], int lane) {
+    static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "a power of two up to 32");
+    float v[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) v[j] = in[j];
+#pragma unroll
+    for (int k = N, o = 16; k > 1; k >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < k / 2; ++j) {
+            const float send = up ? v[j] : v[j + k / 2];
+            const float keep = up ? v[j + k / 2] : v[j];
+            const float got = __shfl_xor_sync(kFullMask, send, o);
+            v[j] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 / N; o > 0; o >>= 1) {
+        const float got = __shfl_xor_sync(kFullMask, r, o);
+        r = MAX ? fmaxf(r, got) : r + got;
+    }
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -883,13 +915,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     // raise the running max to this tile's max (per head); the
                     // barrier that publishes the warps' maxima also decides
                     // whether the part stops
-#pragma unroll
-                    for (int g = 0; g < HG; ++g) {
-                        float v = x[g];
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1)
-                            v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
-                        if (lane == 0) red[qd * G + h0 + g] = v;
+                    {
+                        const float v = warp_scatter_reduce<HG, true>(x, lane);
+                        if ((lane & (32 / HG - 1)) == 0) red[qd * G + h0 + lane / (32 / HG)] = v;
                     }
                     if (part_bar_or(part, failed)) {
                         stop = true;
@@ -992,12 +1020,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             if (stop) break;
 
             // ---- piece epilogue: denominators, O = O_hi + O_lo, output ----
-#pragma unroll
-            for (int g = 0; g < HG; ++g) {
-                float v = lp[g];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFullMask, v, off);
-                if (lane == 0) red[qd * G + h0 + g] = v;
+            {
+                const float v = warp_scatter_reduce<HG, false>(lp, lane);
+                if ((lane & (32 / HG - 1)) == 0) red[qd * G + h0 + lane / (32 / HG)] = v;
             }
             if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1,
                            abort_all, p.status))
