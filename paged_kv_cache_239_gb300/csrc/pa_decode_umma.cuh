@@ -52,6 +52,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_schedule.cuh"
 
 namespace pa {
 
@@ -263,200 +264,27 @@ struct UmmaCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// Work schedule.  The unit of work is one 128-token tile of one (sequence b,
-// head group g) pair, g = kv head * nchunks + head chunk; a context of n
-// tokens has max(1, ceil(n / 128)) tiles (an empty one still owes its zero
-// output).  Every pair is charged kUmmaPieceUnits more units for the fixed
-// cost of starting and finishing a piece of it (q load, first-tile maximum,
-// output), placed before its tiles and doing no work.  Units are ordered by
-// b, then g, then position, and CTA j of the persistent grid takes the
-// contiguous range [ceil(j T / grid), ceil((j + 1) T / grid)) of the T units
-// (grid <= T): every CTA gets the same share of the work, whatever the mix of
-// lengths.  A range covers whole pairs, except that its first and last piece
-// may be parts of one that neighbouring CTAs share; those write unnormalised
-// partials into the CTA's two slots (first piece slot 0, last slot 1) and the
-// combine kernel merges them, told where by the descriptor the piece holding
-// tile 0 writes.
+// Work schedule: equal shares of 128-token tiles per persistent CTA (see
+// pa_schedule.cuh), each (sequence, head group) pair charged three extra units
+// for a piece's fixed cost (q, the first tile's maximum, the output, the next
+// copies' latency).
 constexpr int kUmmaPieceUnits = 3;
+using UItem = SPiece;
+using UWalk = SWalk;
 
-struct UItem {
-    int b, g, kvh, hc, hbase, n, c, u, units, t0, t1, ntiles;
-    long long gpos;          // global index of the piece's first tile
-    bool bad_len, whole, first;
-};
-
-__device__ __forceinline__ int umma_units(int n, int maxtok) {
-    return (n <= 0 || n > maxtok) ? 1 : (int)(((long long)n + 127) / 128);
-}
-
-// Units of the pairs of sequences b0 + 8 lane + k, k < 8 (0 past the batch).
-template <int B>
-__device__ __forceinline__ void umma_pair_units(const DecodeParams& p, int b0, int lane,
-                                                int (&cu)[8]) {
-    int nv[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int b = b0 + 8 * lane + k;
-        nv[k] = b < p.batch ? __ldg(p.lens + b) : 0;
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        cu[k] = b0 + 8 * lane + k < p.batch ? kUmmaPieceUnits + umma_units(nv[k], p.maxb * B) : 0;
-}
-
-// Computes this CTA's range (warp-wide; lane 0 stores it in `sched`):
-// [0] T, [8] grid (min(gridDim, T)), [16] first unit, [24] unit count,
-// [32] its b, [36] its g, [40] its offset within the pair.  A batch of up to
-// 256 sequences takes one round of loads (8 per lane).
 template <int B>
 __device__ __forceinline__ void umma_schedule(const DecodeParams& p, unsigned char* sched,
                                               int lane) {
-    const long long Gq = (long long)p.Hkv * p.nchunks;
-    int cu[8];
-    long long T = 0;
-    for (int b0 = 0; b0 < p.batch; b0 += 256) {
-        umma_pair_units<B>(p, b0, lane, cu);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) T += cu[k];
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(kFullMask, T, off);
-    T *= Gq;
-    const long long grid = min((long long)gridDim.x, T);
-    const long long j = blockIdx.x;
-    long long lo = 0, cnt = 0;
-    int b_sel = 0, g_sel = 0, o_sel = 0;
-    if (j < grid) {
-        lo = (j * T + grid - 1) / grid;
-        cnt = ((j + 1) * T + grid - 1) / grid - lo;
-        long long P = 0;  // units before sequence b0
-        for (int b0 = 0; b0 < p.batch; b0 += 256) {
-            if (p.batch > 256) umma_pair_units<B>(p, b0, lane, cu);
-            long long mine = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mine += cu[k];
-            mine *= Gq;
-            long long incl = mine;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const long long v = __shfl_up_sync(kFullMask, incl, off);
-                if (lane >= off) incl += v;
-            }
-            const unsigned hit =
-                __ballot_sync(kFullMask, mine > 0 && P + incl - mine <= lo && lo < P + incl);
-            if (hit) {
-                const int f = __ffs(hit) - 1;
-                if (lane == f) {
-                    long long pos = P + incl - mine;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const long long pc = (long long)cu[k] * Gq;
-                        if (cu[k] > 0 && lo < pos + pc) {
-                            const long long off = lo - pos;
-                            b_sel = b0 + 8 * lane + k;
-                            g_sel = (int)(off / cu[k]);
-                            o_sel = (int)(off % cu[k]);
-                            break;
-                        }
-                        pos += pc;
-                    }
-                }
-                b_sel = __shfl_sync(kFullMask, b_sel, f);
-                g_sel = __shfl_sync(kFullMask, g_sel, f);
-                o_sel = __shfl_sync(kFullMask, o_sel, f);
-                break;
-            }
-            P += __shfl_sync(kFullMask, incl, 31);
-        }
-    }
-    if (lane == 0) {
-        long long* s64 = reinterpret_cast<long long*>(sched);
-        int* s32 = reinterpret_cast<int*>(sched + 32);
-        s64[0] = T;
-        s64[1] = grid;
-        s64[2] = lo;
-        s64[3] = cnt;
-        s32[0] = b_sel;
-        s32[1] = g_sel;
-        s32[2] = o_sel;
-    }
+    sched_compute<B, 128, kUmmaPieceUnits>(p, sched, lane);
 }
-
-// Walks the pieces of this CTA's range.  Every role walks it the same way; the
-// length of the next sequence is loaded one sequence ahead (under a full HBM
-// stream a dependent global load costs microseconds).
-struct UWalk {
-    int b, g, o, n, c, n_next;  // o: offset within the pair, overhead units first
-    bool bad, emitted;
-    long long gpos, left;
-    const long long* sched;  // T, grid, first unit (read where needed: registers are short)
-};
-
-template <int B>
-__device__ __forceinline__ void umma_walk_seq(const DecodeParams& p, UWalk& w, int n_raw) {
-    const int maxtok = p.maxb * B;
-    w.bad = n_raw < 0 || n_raw > maxtok;
-    w.n = w.bad ? 0 : n_raw;
-    w.c = umma_units(w.n, maxtok);
-    w.n_next = w.b + 1 < p.batch ? __ldg(p.lens + w.b + 1) : 0;
-}
-
 template <int B>
 __device__ __forceinline__ void umma_walk_begin(const DecodeParams& p, const unsigned char* sched,
                                                 UWalk& w) {
-    const long long* s64 = reinterpret_cast<const long long*>(sched);
-    const int* s32 = reinterpret_cast<const int*>(sched + 32);
-    w.sched = s64;
-    w.left = s64[3];
-    w.gpos = s64[2];
-    w.b = s32[0];
-    w.g = s32[1];
-    w.o = s32[2];
-    w.emitted = false;
-    if (w.left > 0) umma_walk_seq<B>(p, w, __ldg(p.lens + w.b));
+    sched_walk_begin<B, 128>(p, sched, w);
 }
-
 template <int B, int G>
 __device__ __forceinline__ bool umma_walk_next(const DecodeParams& p, UWalk& w, UItem& it) {
-    if (w.left <= 0) return false;
-    if (w.o < kUmmaPieceUnits) {  // the pair's overhead units: nothing to do
-        const long long skip = min((long long)(kUmmaPieceUnits - w.o), w.left);
-        w.o += (int)skip;
-        w.gpos += skip;
-        w.left -= skip;
-        if (w.left <= 0) return false;
-    }
-    const int u = w.o - kUmmaPieceUnits;
-    const int units = (int)min((long long)(w.c - u), w.left);
-    it.b = w.b;
-    it.g = w.g;
-    it.kvh = w.g / p.nchunks;
-    it.hc = w.g % p.nchunks;
-    it.hbase = it.kvh * p.gsize + it.hc * G;
-    it.n = w.n;
-    it.c = w.c;
-    it.u = u;
-    it.units = units;
-    it.gpos = w.gpos;
-    it.bad_len = w.bad;
-    it.whole = u == 0 && units == w.c;
-    it.first = !w.emitted;
-    w.emitted = true;
-    it.t0 = (int)min((long long)u * 128, (long long)w.n);
-    it.t1 = (int)min((long long)(u + units) * 128, (long long)w.n);
-    it.ntiles = (it.t1 - it.t0 + 127) / 128;
-    w.left -= units;
-    w.gpos += units;
-    w.o += units;
-    if (w.o == kUmmaPieceUnits + w.c) {
-        w.o = 0;
-        if (++w.g == p.Hkv * p.nchunks) {
-            w.g = 0;
-            ++w.b;
-            if (w.left > 0) umma_walk_seq<B>(p, w, w.n_next);
-        }
-    }
-    return true;
+    return sched_walk_next<B, 128, kUmmaPieceUnits, G>(p, w, it);
 }
 
 // Non-blocking test of an mbarrier phase (try_wait may suspend the thread for
@@ -854,10 +682,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             if (it.u == 0 && warp == C::SM_WARP0 && lane == 0 && p.tc_desc != nullptr) {
                 // where the combine finds this pair's pieces: CTAs first ..
                 // first + pieces - 1 (the owners of its first and last unit)
-                const int pieces =
-                    it.whole ? 1
-                             : (int)((it.gpos + it.c - 1) * w.sched[1] / w.sched[0] -
-                                     blockIdx.x + 1);
+                const int pieces = sched_pieces(it, w);
                 p.tc_desc[(long long)it.b * p.Hkv * p.nchunks + it.g] =
                     make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
             }
