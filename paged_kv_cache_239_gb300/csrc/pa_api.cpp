@@ -107,13 +107,19 @@ size_t workspace_bytes_for(int batch, int H, int Cmax, int D) {
 }
 
 // tcgen05 kernel: two partial slots of `chunk` heads per CTA (its first and
-// last piece), then one int4 descriptor per (sequence, head group).
+// last piece), one int4 descriptor per (sequence, head group), then one int
+// per CTA naming the cut pair whose first piece it holds.
 size_t tc_partial_slots(int grid, int chunk) { return (size_t)grid * 2 * chunk; }
+size_t tc_desc_offset(int grid, int chunk, int D) {
+    const size_t S = tc_partial_slots(grid, chunk);
+    return align256(S * D * sizeof(float)) + align256(S * 2 * sizeof(float));
+}
+size_t tc_cut_offset(int grid, int chunk, int D, long long pairs) {
+    return tc_desc_offset(grid, chunk, D) + align256((size_t)pairs * sizeof(int4));
+}
 size_t tc_workspace_bytes(int grid, int chunk, int D, long long pairs) {
     if (grid <= 1) return 0;
-    const size_t S = tc_partial_slots(grid, chunk);
-    return align256(S * D * sizeof(float)) + align256(S * 2 * sizeof(float)) +
-           (size_t)pairs * sizeof(int4);
+    return tc_cut_offset(grid, chunk, D, pairs) + (size_t)grid * sizeof(int);
 }
 
 int check_pool(const pa_pool* pool) {
@@ -642,6 +648,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     float* part_o = nullptr;
     float* part_ml = nullptr;
     int4* tc_desc = nullptr;
+    int* tc_cut = nullptr;
     if (sh.ws_bytes > 0) {
         if (!workspace || workspace_bytes < sh.ws_bytes || !aligned(workspace, 256))
             return fail(PA_ERR_WORKSPACE,
@@ -651,9 +658,10 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
         part_o = reinterpret_cast<float*>(ws);
         if (sh.kernel == Kernel::Tcgen05) {
             const size_t S = tc_partial_slots(sh.tc_grid, sh.chunk);
+            const long long pairs = (long long)batch * g.Hkv * (sh.G / sh.chunk);
             part_ml = reinterpret_cast<float*>(ws + align256(S * g.D * sizeof(float)));
-            tc_desc = reinterpret_cast<int4*>(ws + align256(S * g.D * sizeof(float)) +
-                                              align256(S * 2 * sizeof(float)));
+            tc_desc = reinterpret_cast<int4*>(ws + tc_desc_offset(sh.tc_grid, sh.chunk, g.D));
+            tc_cut = reinterpret_cast<int*>(ws + tc_cut_offset(sh.tc_grid, sh.chunk, g.D, pairs));
         } else {
             part_ml = reinterpret_cast<float*>(
                 ws + align256((size_t)batch * num_heads * sh.Cmax * g.D * sizeof(float)));
@@ -689,6 +697,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     p.positions = positions;
     p.tc_grid = sh.tc_grid;
     p.tc_desc = tc_desc;
+    p.tc_cut = tc_cut;
     p.gsize = sh.G;
     p.nchunks = sh.G / sh.chunk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -712,7 +721,12 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
                          : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-    if (sh.combine) {
+    if (sh.combine && sh.kernel == Kernel::Tcgen05) {
+        // (fewer pairs than CTAs: most are cut, so every pair gets a CTA group)
+        const long long pairs = (long long)batch * g.Hkv * (sh.G / sh.chunk);
+        e = pa::launch_combine_tc(p, g.D, pairs <= sh.tc_grid, sh.Cmax, s);
+        if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    } else if (sh.combine) {
         e = pa::launch_combine(p, g.D, g.B, s);
         if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     }

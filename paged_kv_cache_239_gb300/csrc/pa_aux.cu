@@ -93,6 +93,31 @@ cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) 
     return cudaErrorNotSupported;
 }
 
+template <int W>
+static cudaError_t launch_combine_tc_w(const DecodeParams& p, long long groups, int direct,
+                                       cudaStream_t s) {
+    const int chunk = p.gsize / p.nchunks;
+    const long long grid = groups * (chunk / (8 / W));
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    return launch_pdl(pa_combine_tc_kernel<128, W>, dim3((unsigned)grid), dim3(256), 0, s, p,
+                      direct);
+}
+
+cudaError_t launch_combine_tc(const DecodeParams& p, int D, bool direct, int pieces_hint,
+                              cudaStream_t s) {
+    if (D != 128) return cudaErrorNotSupported;
+    const long long groups = direct ? (long long)p.batch * p.Hkv * p.nchunks : p.tc_grid;
+    // warps per head from the expected pieces per cut pair (as for partitions)
+    const int W = pieces_hint > 32 ? 8 : (pieces_hint > 8 ? 4 : (pieces_hint > 4 ? 2 : 1));
+    switch (W) {
+        case 8: return launch_combine_tc_w<8>(p, groups, direct ? 1 : 0, s);
+        case 4: return launch_combine_tc_w<4>(p, groups, direct ? 1 : 0, s);
+        case 2: return launch_combine_tc_w<2>(p, groups, direct ? 1 : 0, s);
+        default: return launch_combine_tc_w<1>(p, groups, direct ? 1 : 0, s);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // KV append: one thread per 16-byte chunk of every (sequence, K/V, kv head) row.
 // Consecutive threads cover consecutive chunks of one row, so both the read of

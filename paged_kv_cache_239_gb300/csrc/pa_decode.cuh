@@ -488,61 +488,25 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     }
 }
 
-// Merges the partitions of every (sequence, query head) with more than one:
+// Merges the partials of one (sequence, query head) gh:
 //   M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c .
-// W warps (1, 2, 4 or 8) serve one (sequence, head); a 256-thread CTA serves
-// 8 / W of them.  Partial c of (sequence, head) gh sits at slot gh * Cmax + c
-// (fixed-size partitions), or, after the tcgen05 kernel (p.tc_desc set), at
-// slot ((first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + head in chunk: piece
-// c came from CTA first + c, and only the first piece can be a CTA's second.  Warp w takes partitions w, w + W, ... four at a time (four
-// independent loads in flight per lane; a lane owns D/32 consecutive
-// elements), then the W partial sums are merged through shared memory.
-template <int D, int W>
-__global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, int B) {
-    pdl_trigger();
-    pdl_wait();
+// W warps (1, 2, 4 or 8) serve one head; a 256-thread CTA serves 8 / W of them
+// (hl: this warp's head slot in the CTA, w: its warp within the head).  Warp w
+// takes partials w, w + W, ... four at a time (four independent loads in
+// flight per lane; a lane owns D/32 consecutive elements), then the W partial
+// sums are merged through shared memory.  Every thread of the CTA calls it
+// (it synchronises the CTA); nparts <= 1 writes nothing.  slot_of(c) is the
+// workspace slot of partial c.
+template <int D, int W, typename SlotOf>
+__device__ __forceinline__ void combine_head(const DecodeParams& p, long long gh, int nparts,
+                                             SlotOf slot_of, int hl, int w) {
     constexpr int PL = D / 32;
-    constexpr int HPC = 8 / W;  // heads per CTA
     __shared__ float s_acc[8][D];
     __shared__ float s_l[8];
     __shared__ float s_m[8];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int hl = warp / W;    // head slot in this CTA
-    const int w = warp % W;     // warp within the head
-    const long long gh = (long long)blockIdx.x * HPC + hl;  // b * H + h
-    const bool live = gh < (long long)p.batch * p.H;
-    int nparts = 0;
-    long long base = gh * p.Cmax;  // slot of partial c: base + c, or see below
-    int first = 0, slot0 = 0, chunk = 1;
-    if (live) {
-        const int b = (int)(gh / p.H);
-        if (p.tc_desc != nullptr) {
-            const int h = (int)(gh % p.H);
-            const int kvh = h / p.gsize, hg = h % p.gsize;
-            chunk = p.gsize / p.nchunks;
-            const int4 d = p.tc_desc[(long long)b * p.Hkv * p.nchunks + kvh * p.nchunks +
-                                     hg / chunk];
-            first = d.x;
-            nparts = d.y;
-            slot0 = d.z;
-            base = hg % chunk;
-            // (a descriptor the decode never wrote -- it stopped on a timeout --
-            // must not send the loads outside the partial slots)
-            if (first < 0 || nparts < 0 || first > p.tc_grid - nparts || (slot0 & ~1)) nparts = 0;
-        } else {
-            int n = __ldg(p.lens + b);
-            if (n < 0 || n > p.maxb * B) n = 0;
-            const int nblk = (n + B - 1) / B;
-            nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
-        }
-    }
-    const bool by_cta = p.tc_desc != nullptr;
-    auto slot_of = [&](int c) -> long long {
-        return by_cta ? ((long long)(first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + base
-                      : base + c;
-    };
-    // running max over this head's partitions, per warp then across the W warps
+    // running max over this head's partials, per warp then across the W warps
     float M = -INFINITY;
     if (nparts > 1)
         for (int c = w * 32 + lane; c < nparts; c += W * 32)
@@ -608,6 +572,74 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, i
             o[i] = Lt > 0.f ? a / Lt : 0.f;
         }
     }
+}
+
+// Merges the fixed-size partitions of every (sequence, query head) with more
+// than one (the mma.sync and CUDA-core kernels): partial c of head gh sits at
+// slot gh * Cmax + c.
+template <int D, int W>
+__global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, int B) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int HPC = 8 / W;  // heads per CTA
+    const int warp = threadIdx.x >> 5;
+    const int hl = warp / W;
+    const int w = warp % W;
+    const long long gh = (long long)blockIdx.x * HPC + hl;  // b * H + h
+    int nparts = 0;
+    if (gh < (long long)p.batch * p.H) {
+        int n = __ldg(p.lens + gh / p.H);
+        if (n < 0 || n > p.maxb * B) n = 0;
+        const int nblk = (n + B - 1) / B;
+        nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
+    }
+    const long long base = gh * p.Cmax;
+    combine_head<D, W>(p, gh, nparts, [&](int c) -> long long { return base + c; }, hl, w);
+}
+
+// Merges the pieces of the (sequence, head group) pairs the tcgen05 kernel
+// cut at its CTAs' range ends.  CTA group k (chunk / (8 / W) CTAs, one per 8 /
+// W heads of the chunk) serves pair k (direct: fewer pairs than decode CTAs,
+// so most are cut) or the pair tc_cut[k] whose first piece decode CTA k holds
+// (-1: none).  The pair's descriptor {first CTA, pieces, slot of the first
+// piece} places piece c at slot ((first + c) * 2 + (c == 0 ? slot0 : 0)) *
+// chunk + head in chunk: piece c came from CTA first + c, and only the first
+// piece can be a CTA's second.
+template <int D, int W>
+__global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p, int direct) {
+    pdl_trigger();
+    pdl_wait();
+    constexpr int HPC = 8 / W;
+    const int warp = threadIdx.x >> 5;
+    const int hl = warp / W;
+    const int w = warp % W;
+    const int chunk = p.gsize / p.nchunks;
+    const int cpp = chunk / HPC;  // CTAs per pair
+    const long long k = blockIdx.x / cpp;
+    const int hh = (int)(blockIdx.x % cpp) * HPC + hl;  // head within the chunk
+    const long long npairs = (long long)p.batch * p.Hkv * p.nchunks;
+    const long long pair = direct ? k : (long long)__ldg(p.tc_cut + k);
+    int nparts = 0, first = 0, slot0 = 0;
+    long long gh = 0;
+    if (pair >= 0 && pair < npairs) {
+        const int4 d = p.tc_desc[pair];
+        first = d.x;
+        nparts = d.y;
+        slot0 = d.z;
+        // (a descriptor the decode never wrote -- it stopped on a timeout --
+        // must not send the loads outside the partial slots)
+        if (first < 0 || nparts < 0 || first > p.tc_grid - nparts || (slot0 & ~1)) nparts = 0;
+        const long long gpairs = (long long)p.Hkv * p.nchunks;
+        const int g = (int)(pair % gpairs);
+        gh = (pair / gpairs) * p.H + (long long)(g / p.nchunks) * p.gsize +
+             (long long)(g % p.nchunks) * chunk + hh;
+    }
+    combine_head<D, W>(
+        p, gh, nparts,
+        [&](int c) -> long long {
+            return ((long long)(first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + hh;
+        },
+        hl, w);
 }
 
 }  // namespace pa

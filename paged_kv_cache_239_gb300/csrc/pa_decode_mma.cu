@@ -153,4 +153,21 @@ cudaError_t encode_pool_tmaps(const PoolGeom& g, void* tmaps, int* slot_blk, int
     return cudaSuccess;
 }
 
+// A 2-D map over `rows` contiguous rows of 128 bf16 (256 bytes): boxes of
+// 64 columns x box_rows rows with the 128-byte swizzle.
+cudaError_t encode_rows_tmap(void* tmap, const void* base, long long rows, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    if (rows <= 0 || box_rows <= 0 || box_rows > 256) return cudaErrorInvalidValue;
+    cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace pa

@@ -12,6 +12,10 @@ namespace {
 
 template <int B, int G>
 cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream_t stream) {
+    // q of one piece is copied as two boxes of 64 columns x G heads
+    CUtensorMap tq;
+    cudaError_t eq = encode_rows_tmap(&tq, p.q, (long long)p.batch * p.H, G);
+    if (eq != cudaSuccess) return eq;
     using Cfg = UmmaCfg<B, G>;
     auto kern = pa_decode_umma_kernel<B, G>;
     static std::mutex mu;
@@ -33,7 +37,7 @@ cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream
     // persistent: one CTA per SM (the shared memory admits no second one),
     // each taking an equal share of the tiles
     return launch_pdl(kern, dim3((unsigned)p.tc_grid), dim3(Cfg::THREADS), Cfg::SMEM_BYTES,
-                      stream, p, tm[0], tm[1]);
+                      stream, p, tm[0], tm[1], tq);
 }
 
 template <int B>

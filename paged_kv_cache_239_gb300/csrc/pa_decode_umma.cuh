@@ -17,10 +17,11 @@
 // every CTA takes an equal contiguous share of them (see the schedule below),
 // so ragged lengths cost no tail.  Warp-specialised roles connected by
 // mbarriers:
-//  * warp 0 (K producer): block-table walk (entries loaded a tile ahead), the
-//    fused append's K row, q of each piece into a swizzled K-major tile
-//    (cp.async, two buffers), and 5-D tensor-map TMA loads of 128-token K
-//    tiles (8 boxes of 16 rows per 64-column half, SWIZZLE_128B) into the K
+//  * warp 0 (K producer): block-table walk (entries loaded a tile ahead, a
+//    piece's first ones and its appended row a piece ahead), the fused
+//    append's K row, q of each piece into a swizzled K-major tile (2-D
+//    tensor-map TMA, two buffers), and 5-D tensor-map TMA loads of 128-token
+//    K tiles (8 boxes of 16 rows per 64-column half, SWIZZLE_128B) into the K
 //    ring;
 //  * warp 2 (V producer): computes the CTA's share at start; the same walk for
 //    V tiles into the V ring, the fused append's V row, bad ids / lengths.
@@ -322,15 +323,6 @@ __device__ __forceinline__ uint32_t sw128(int r, int j) {
     return (uint32_t)(r * 128 + (((j & 7) ^ (r & 7)) << 4));
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only), and the wait for all
-// of this thread's outstanding ones.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // Max (or sum) of v[j] over the warp's 32 lanes for each of N = 2^k values,
 // as a reduce-scatter butterfly: at each step a lane sends the half of its
 // values it does not keep, so N + N/2 + ... shuffles become N - 1 + 5 - log2 N
@@ -371,7 +363,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 template <int B, int G>
 __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
     pa_decode_umma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                          const __grid_constant__ CUtensorMap tmv) {
+                          const __grid_constant__ CUtensorMap tmv,
+                          const __grid_constant__ CUtensorMap tmq) {
     pdl_trigger();
     using C = UmmaCfg<B, G>;
     extern __shared__ unsigned char smem_raw[];
@@ -391,7 +384,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::NBAR; ++i)
-            mbar_init(bar0 + 8 * i, (i == C::P_FULL || i == C::P_FULL + 1) ? C::NSM : 1);
+            mbar_init(bar0 + 8 * i, (i == C::P_FULL || i == C::P_FULL + 1) ? C::NSW : 1);
         *abort_all = 0;
         fence_mbar_init();
     }
@@ -399,6 +392,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmk);
         prefetch_tensormap(&tmv);
+        prefetch_tensormap(&tmq);
     }
     // (nothing above reads what the previous kernel may have written: the
     // set-up overlaps its tail)
@@ -411,9 +405,13 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
 
     if (warp == 0 || warp == 2) {
         // ============================= producers: warp 0 K (and q), warp 2 V
-        // Both walk the same pieces and table entries.  The fused append's new
-        // row is stored by each producer for its own half (K or V) before that
-        // producer's copies of the piece; warp 2 reports bad ids and lengths.
+        // Both walk the same pieces and table entries.  Everything a piece
+        // needs from global memory before its first copy (its first table
+        // entries, the appended row's position and bytes) is loaded one piece
+        // ahead: under a full HBM stream a dependent load costs microseconds.
+        // The fused append's new row is stored by each producer for its own
+        // half (K or V) right before the copy of the tile that holds it; warp
+        // 2 reports bad ids and lengths.
         const bool is_v = (warp == 2);
         const CUtensorMap* tm = is_v ? &tmv : &tmk;
         const int NS = is_v ? C::SV : C::SK;
@@ -421,7 +419,12 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         const uint32_t empty0 = bar0 + 8 * (is_v ? C::V_EMPTY : C::K_EMPTY);
         const uint32_t ring = sbase + (is_v ? C::OFF_V : 0);
         const uint64_t policy = l2_policy_evict_first();
-        int kt = 0, qi = 0;
+        const bool append = p.new_k != nullptr;
+        const unsigned char* new_rows =
+            static_cast<const unsigned char*>(is_v ? p.new_v : p.new_k);
+        unsigned short* pool_rows = const_cast<unsigned short*>(
+            reinterpret_cast<const unsigned short*>(is_v ? p.v_base : p.k_base));
+        int kt = 0, qi = 0, q_last = -1;
         bool aborted = false;
         // block-table entry of box `lane` of tile i of a piece (0 if none)
         auto box_block = [&](const UItem& pc, int i) {
@@ -430,46 +433,55 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                        ? __ldg(p.bt + (long long)pc.b * p.maxb + tok / B)
                        : 0;
         };
+        // the appended row of a piece's (sequence, KV head): its position and
+        // (lanes < 16) one 16-byte chunk of its 256 bytes
+        auto row_pos = [&](const UItem& pc) { return append ? __ldg(p.positions + pc.b) : -1; };
+        auto row_val = [&](const UItem& pc) {
+            return (append && lane < 16)
+                       ? __ldg(reinterpret_cast<const uint4*>(
+                                   new_rows + ((long long)pc.b * p.Hkv + pc.kvh) * 256) +
+                               lane)
+                       : make_uint4(0, 0, 0, 0);
+        };
         UWalk w;
         umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
         UItem it, nx;
         bool have = umma_walk_next<B, G>(p, w, it);
         int blk_first = have ? box_block(it, 0) : 0;
+        int pos = have ? row_pos(it) : -1;
+        uint4 rowv = have ? row_val(it) : make_uint4(0, 0, 0, 0);
         while (have && !aborted) {
-            // one piece ahead: the next piece's first table entries are loaded
-            // now, so its first copies need not wait for them
             const bool have_nx = umma_walk_next<B, G>(p, w, nx);
             const int blk_first_nx = have_nx ? box_block(nx, 0) : 0;
+            const int pos_nx = have_nx ? row_pos(nx) : -1;
+            const uint4 rowv_nx = have_nx ? row_val(nx) : make_uint4(0, 0, 0, 0);
             // (the piece at tile 0 of head group 0 reports for the sequence)
             const bool reporter = is_v && it.g == 0 && it.u == 0 && lane == 0;
             if (reporter && it.bad_len) atomicOr(p.status, kStatusBadLength);
-            const int* bt_row = p.bt + (long long)it.b * p.maxb;
-            if (p.new_k != nullptr) {
-                // fused append: the piece holding the new row's tile (the
-                // first piece if the row lies past the context) stores it --
-                // every head chunk its own identical copy -- before its copies
-                const int pos = __ldg(p.positions + it.b);
-                if (pos < 0 || pos / B >= p.maxb) {
-                    if (reporter) atomicOr(p.status, kStatusBadLength);
-                } else if (pos < it.n ? (pos / 128 >= it.u && pos / 128 < it.u + it.units)
-                                      : it.u == 0) {
-                    const int blk = __ldg(bt_row + pos / B);
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        if (is_v && lane == 0) atomicOr(p.status, kStatusBadBlock);
-                    } else if (lane < 16) {  // 16 chunks of 16 bytes per 128-element row
-                        const long long src = ((long long)it.b * p.Hkv + it.kvh) * 256 + lane * 16;
-                        const long long off = (long long)blk * p.s_blk + p.tile_off +
-                                              (long long)it.kvh * p.s_head + (long long)(pos % B) * 128;
-                        const uint4 val = __ldg(reinterpret_cast<const uint4*>(
-                            static_cast<const unsigned char*>(is_v ? p.new_v : p.new_k) + src));
-                        unsigned short* dst = const_cast<unsigned short*>(
-                            reinterpret_cast<const unsigned short*>(is_v ? p.v_base : p.k_base)) +
-                            off;
-                        reinterpret_cast<uint4*>(dst)[lane] = val;
-                        fence_proxy_async_global();
-                    }
+            // stores the appended row into block `blk` (every head chunk its
+            // own identical copy), ordered before this warp's later copies
+            auto store_row = [&](int blk) {
+                if (blk < 0 || blk >= p.num_blocks) {
+                    if (is_v && lane == 0) atomicOr(p.status, kStatusBadBlock);
+                } else if (lane < 16) {
+                    const long long off = (long long)blk * p.s_blk + p.tile_off +
+                                          (long long)it.kvh * p.s_head + (long long)(pos % B) * 128;
+                    reinterpret_cast<uint4*>(pool_rows + off)[lane] = rowv;
+                    fence_proxy_async_global();
                 }
                 __syncwarp();
+            };
+            // the piece holding the row's tile stores it before that tile's
+            // copy; a row past the context is stored by the pair's first piece
+            int store_tile = -1;
+            if (append) {
+                if (pos < 0 || pos / B >= p.maxb) {
+                    if (reporter) atomicOr(p.status, kStatusBadLength);
+                } else if (pos < it.n) {
+                    if (pos >= it.t0 && pos < it.t1) store_tile = (pos - it.t0) / C::TT;
+                } else if (it.u == 0) {
+                    store_row(__ldg(p.bt + (long long)it.b * p.maxb + pos / B));
+                }
             }
 
             // 128-token tiles: lane r < 8 walks box r (16 rows) of the tile; the
@@ -489,6 +501,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     aborted = true;
                     break;
                 }
+                if (i == store_tile)  // (the row's box lane holds its block id)
+                    store_row(__shfl_sync(kFullMask, blk, ((pos - it.t0) % C::TT) / 16));
                 const bool bad = valid && (blk < 0 || blk >= p.num_blocks);
                 valid = valid && !bad;
                 const unsigned vmask = __ballot_sync(kFullMask, valid);
@@ -513,8 +527,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 }
                 if (!is_v && i == 0) {
                     // q of the piece's G heads -> K-major swizzled tile
-                    // [half][G][128 B], once its first K copy is on its way
-                    // (buffer qi & 1: free once the last S of piece qi - 2 is done)
+                    // [half][G][128 B] by two tensor-map copies, once its first
+                    // K copy is on its way (buffer qi & 1: free once the last S
+                    // of piece qi - 2 is done)
                     if (qi >= 2 &&
                         !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + (qi & 1)),
                                                          ((qi >> 1) - 1) & 1, abort_all,
@@ -523,30 +538,31 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                         ++kt;  // (tile 0's copy is in flight: the exit path waits for it)
                         break;
                     }
-                    const uint32_t qbuf = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
-                    const uint4* qsrc = reinterpret_cast<const uint4*>(
-                        static_cast<const unsigned short*>(p.q) +
-                        ((long long)it.b * p.H + it.hbase) * 128);
-#pragma unroll
-                    for (int j = lane; j < G * 16; j += 32) {
-                        const int g = j >> 4, c16 = j & 15;
-                        cp_async16(qbuf + (c16 >> 3) * (G * 128) + sw128(g, c16), qsrc + j);
+                    if (lane == 0) {
+                        const uint32_t qbuf = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
+                        const uint32_t qbar = bar0 + 8 * (C::Q_FULL + (qi & 1));
+                        const int qrow = it.b * p.H + it.hbase;
+                        mbar_arrive_expect_tx(qbar, (uint32_t)C::Q_BYTES);
+                        tma_load_2d(qbuf, &tmq, qbar, 0, qrow);
+                        tma_load_2d(qbuf + G * 128, &tmq, qbar, 64, qrow);
                     }
-                    cp_async_wait_all();
-                    fence_proxy_async_smem();
+                    q_last = qi;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar0 + 8 * (C::Q_FULL + (qi & 1)));
                 }
             }
             if (!aborted && it.ntiles > 0) ++qi;
             it = nx;
             have = have_nx;
             blk_first = blk_first_nx;
+            pos = pos_nx;
+            rowv = rowv_nx;
         }
         if (aborted || *abort_all) {
             // copies still in flight land before the CTA can exit
             for (int k = kt > NS ? kt - NS : 0; k < kt; ++k)
                 (void)mbar_wait_bounded(full0 + 8 * (k % NS), (k / NS) & 1);
+            for (int k = q_last > 0 ? q_last - 1 : 0; !is_v && k <= q_last; ++k)
+                (void)mbar_wait_bounded(bar0 + 8 * (C::Q_FULL + (k & 1)), (k >> 1) & 1);
         }
     } else if (warp == 1) {
         // ============================================ MMA issuer (warp 1, lane 0)
@@ -676,19 +692,35 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         float lp[HG];  // this thread's share of the softmax denominators
         UWalk w;
         umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
+        // the block id of this thread's token in a piece's first tile, loaded
+        // one piece ahead (later tiles' ids are loaded a tile ahead)
+        auto first_block = [&](const UItem& pc) {
+            const int tok = pc.t0 + r;
+            return (pc.ntiles > 0 && tok < pc.t1) ? __ldg(p.bt + (long long)pc.b * p.maxb + tok / B)
+                                                  : -1;
+        };
+        // (this CTA's cut pair, if any, is recorded below; none so far)
+        if (warp == C::SM_WARP0 && lane == 0 && p.tc_cut != nullptr) p.tc_cut[blockIdx.x] = -1;
         UItem it;
-        while (!stop && umma_walk_next<B, G>(p, w, it)) {
+        bool have = umma_walk_next<B, G>(p, w, it);
+        int blk0 = have ? first_block(it) : -1;
+        while (!stop && have) {
             const long long head0 = (long long)it.b * p.H + it.hbase + h0;
             if (it.u == 0 && warp == C::SM_WARP0 && lane == 0 && p.tc_desc != nullptr) {
                 // where the combine finds this pair's pieces: CTAs first ..
-                // first + pieces - 1 (the owners of its first and last unit)
+                // first + pieces - 1 (the owners of its first and last unit);
+                // a pair that continues past this CTA is its cut pair (at most
+                // one: the range's last piece)
                 const int pieces = sched_pieces(it, w);
-                p.tc_desc[(long long)it.b * p.Hkv * p.nchunks + it.g] =
-                    make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
+                const long long pair = (long long)it.b * p.Hkv * p.nchunks + it.g;
+                p.tc_desc[pair] = make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
+                if (!it.whole) p.tc_cut[blockIdx.x] = (int)pair;
             }
             if (it.ntiles == 0) {  // empty context: output 0 (always a whole piece)
 #pragma unroll
                 for (int g = 0; g < HG; ++g) p.out[(head0 + g) * 128 + r] = 0.f;
+                have = umma_walk_next<B, G>(p, w, it);
+                blk0 = have ? first_block(it) : -1;
                 continue;
             }
 #pragma unroll
@@ -701,7 +733,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 const int tok = it.t0 + i * C::TT + r;
                 return (i < it.ntiles && tok < it.t1) ? __ldg(bt_row + tok / B) : -1;
             };
-            int blk_next = tok_block(0);
+            int blk_next = blk0;
             for (int i = 0; i < it.ntiles; ++i, ++kt) {
                 const int stage = kt % C::SV;  // V stage
                 const int blk = blk_next;
@@ -791,7 +823,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float mm = mv[e] == -INFINITY ? 0.f : mv[e];
-                        const float pv = exp2f(x[g + e] - mm);
+                        const float pv = ex2_approx(x[g + e] - mm);
                         lp[g + e] += pv;
                         x[g + e] = pv;
                     }
@@ -838,11 +870,18 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                                               sw128(r, (nl & 63) >> 3)) =
                         make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
+                // one arrival per warp, after all its lanes' writes
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(bar0 + 8 * (C::P_FULL + (kt & 1)));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8 * (C::P_FULL + (kt & 1)));
             }
             if (stop) break;
+            // the next piece, and its first tile's block id (loaded while this
+            // piece's output is finished)
+            UItem nx;
+            const bool have_nx = umma_walk_next<B, G>(p, w, nx);
+            const int blk0_nx = have_nx ? first_block(nx) : -1;
 
             // ---- piece epilogue: denominators, O = O_hi + O_lo, output ----
             {
@@ -888,6 +927,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 }
             }
             tc_fence_before();
+            it = nx;
+            have = have_nx;
+            blk0 = blk0_nx;
         }
     }
 

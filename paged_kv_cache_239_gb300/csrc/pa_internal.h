@@ -65,6 +65,9 @@ struct DecodeParams {
     // the partials then sit in part_o / part_ml as [CTA][2 slots][chunk head]
     int tc_grid;
     int4* tc_desc;
+    // tcgen05 kernel: per decode CTA, the (sequence, head group) pair whose
+    // first piece it holds and which continues past its range (-1: none)
+    int* tc_cut;
 };
 
 struct WriteParams {
@@ -115,6 +118,9 @@ cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, i
 // swizzle) into tmaps[0..1]; slots receives the outer-dimension order.
 cudaError_t encode_pool_tmaps(const PoolGeom& g, void* tmaps, int* slot_blk, int* slot_layer,
                               int* slot_head);
+// Encodes a 2-D tensor map over `rows` contiguous rows of 128 bf16 (boxes of 64
+// columns x box_rows rows, 128-byte swizzle) into one CUtensorMap at tmap.
+cudaError_t encode_rows_tmap(void* tmap, const void* base, long long rows, int box_rows);
 
 // tcgen05 kernel for bf16 pools, head_dim 128, groups that are multiples of
 // 16 (chunks of 64, 32 or 16 heads; decode_umma_chunk gives the chunk, 0 if
@@ -125,6 +131,10 @@ cudaError_t launch_decode_umma(const DecodeParams& p, const void* tmaps, int B, 
                                cudaStream_t s);
 
 cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s);
+// Merges the tcgen05 kernel's cut pairs: every pair (direct) or the pairs its
+// CTAs recorded in tc_cut; pieces_hint estimates the pieces per cut pair.
+cudaError_t launch_combine_tc(const DecodeParams& p, int D, bool direct, int pieces_hint,
+                              cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s);
 cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s);
