@@ -36,6 +36,13 @@
  *    bit is set in the device status word, read with pa_get_status().
  *  - The first launching call on a device looks up the device status word; do
  *    that call (or pa_get_status) once before capturing a stream into a graph.
+ *  - Per device, for the life of the process, the library caches the status
+ *    word's address, the SM count and the no-allocation scratch address
+ *    (pa_decode_attention_noalloc).  These do not survive cudaDeviceReset():
+ *    do not use the library on a device after resetting it in the same
+ *    process.
+ *  - Each declaration below names the passage of the source pages it restates
+ *    ("Cites:"), or says that the pages have no counterpart.
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
@@ -80,7 +87,10 @@ enum {
 #define PA_STATUS_TIMEOUT 0x4u      /* a bounded wait for a shared-memory copy gave up */
 #define PA_STATUS_NO_FREE_BLOCKS 0x8u /* the device free stack ran dry during an allocation */
 
-/* Human-readable description of the calling thread's last error ("" if none). */
+/* Human-readable description of the calling thread's last error ("" if none).
+ * Cites: no counterpart on the pages (this interface's error reporting); the one
+ * error the pages name is the allocator's "Out of KV-Cache Physical Blocks"
+ * (mini-infer, "Python Implementation: Physical Block Pool"). */
 PA_API const char* pa_last_error_string(void);
 
 /* ----------------------------------------------------------------------------
@@ -95,6 +105,9 @@ PA_API const char* pa_last_error_string(void);
  *   geometry   all > 0; head_dim * sizeof(dtype) must be a multiple of 16.
  * The free stack starts as 0..num_blocks-1; pa_alloc_block pops the END, so
  * the first id handed out is num_blocks-1.
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool" (the pool
+ * tensor's shape and order, one allocation at start-up, the free list
+ * range(num_blocks)) and "The Solution" (fixed-size physical blocks).
  */
 PA_API int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num_layers,
                    int num_kv_heads, int block_size, int head_dim, pa_dtype dtype);
@@ -112,6 +125,8 @@ PA_API int pa_pool_create(pa_pool** out, void* pool_dev, int num_blocks, int num
  * from one base must not overlap (checked).  K and V tiles must not overlap
  * each other (not checked).  pa_pool_create is this call with the fused
  * layout's strides.
+ * Cites: "vllmini", "The CUDA Block Kernel" (the kernel takes k_cache and
+ * v_cache as separate arguments).
  */
 typedef struct pa_pool_layout {
     void* k_base;
@@ -125,7 +140,10 @@ PA_API int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, i
                                   int num_layers, int num_kv_heads, int block_size, int head_dim,
                                   pa_dtype dtype);
 
-/* Release the handle (not the caller's device tensor).  NULL is accepted. */
+/* Release the handle (not the caller's device tensor).  NULL is accepted.
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool" (the pool
+ * tensor is allocated once by its owner; the page shows no teardown, so this
+ * call only drops what pa_pool_create made: the handle and its free stack). */
 PA_API int pa_pool_destroy(pa_pool* pool);
 
 /* Built shapes: head_dim 64 or 128, block_size 16 or 32; GQA group
@@ -151,7 +169,9 @@ PA_API int pa_pool_destroy(pa_pool* pool);
  * end and the combine kernel merges those.  partition_blocks does not apply to
  * it (pa_decode_partition_blocks reports max_blocks_per_seq); its workspace,
  * needed whenever more than one CTA runs, grows with the SM count (two slots
- * of partials per CTA) and the number of (sequence, head group) pairs. */
+ * of partials per CTA) and the number of (sequence, head group) pairs.
+ * Cites: no counterpart on the pages (a choice among this library's kernels);
+ * each computes the decode of "vllmini", "The CUDA Block Kernel". */
 enum {
     PA_DECODE_AUTO = 0,
     PA_DECODE_CUDA_CORES = 1,
@@ -165,27 +185,42 @@ PA_API int pa_pool_set_decode_kernel(pa_pool* pool, int kind);
  * PA_DECODE_TENSOR_CORES or PA_DECODE_TCGEN05 in *kind.  PA_ERR_UNSUPPORTED
  * (with the reason) when no kernel serves the shape or the forced one cannot;
  * PA_ERR_INVALID_ARG when num_heads is not a positive multiple of the pool's
- * KV heads.  Host only: touches no device. */
+ * KV heads.  Host only: touches no device.
+ * Cites: no counterpart on the pages (as pa_pool_set_decode_kernel). */
 PA_API int pa_decode_kernel_choice(const pa_pool* pool, int num_heads, int* kind);
 
 /* Bytes of one physical block: 2 * num_layers * num_kv_heads * block_size *
- * head_dim * element size (K and V of every layer and KV head). */
+ * head_dim * element size (K and V of every layer and KV head).
+ * Cites: mini-infer, "Memory Waste Analysis" (its block-size formula, which
+ * omits the K/V factor and the element size) and "Python Implementation:
+ * Physical Block Pool" (the tensor those factors come from). */
 PA_API int pa_pool_block_bytes(const pa_pool* pool, size_t* bytes);
 
 /* Replace the free stack by `order` (a permutation of 0..num_blocks-1, n ==
  * num_blocks); allowed only while every block is free.  The LAST entry is
- * handed out first. */
+ * handed out first.
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool" (the free
+ * list that allocation pops from the end); the page always starts it as
+ * range(num_blocks), seeding another order has no counterpart there. */
 PA_API int pa_pool_seed_free_stack(pa_pool* pool, const int* order, int n);
 
 /* Pop one block id from the free stack.  PA_ERR_NO_FREE_BLOCKS when empty
- * ("Out of KV-Cache Physical Blocks"). */
+ * ("Out of KV-Cache Physical Blocks").
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool"
+ * (allocate_block: pop from the end of the free list, MemoryError when empty);
+ * "kv-cache" skill, section 2 (a block is taken as a sequence grows). */
 PA_API int pa_alloc_block(pa_pool* pool, int* block_id);
 
 /* Push `block_id` back; it becomes the next id handed out.  Ids outside the
- * pool are PA_ERR_INVALID_ARG, ids not currently allocated PA_ERR_DOUBLE_FREE. */
+ * pool are PA_ERR_INVALID_ARG, ids not currently allocated PA_ERR_DOUBLE_FREE.
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool" (free_block
+ * appends the id to the free list); the page checks nothing, rejecting foreign
+ * and double frees is this library's reading. */
 PA_API int pa_free_block(pa_pool* pool, int block_id);
 
-/* Number of ids on the free stack. */
+/* Number of ids on the free stack.
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool" (the length of
+ * the free list). */
 PA_API int pa_num_free(const pa_pool* pool, int* n);
 
 /* ----------------------------------------------------------------------------
@@ -197,15 +232,18 @@ PA_API int pa_num_free(const pa_pool* pool, int* n);
  * pa_pool_seed_free_stack are refused.
  * ------------------------------------------------------------------------- */
 
-/* Bytes of the device stack array: (num_blocks + 1) * 4. */
+/* Bytes of the device stack array: (num_blocks + 1) * 4.
+ * Cites: as the section above. */
 PA_API int pa_device_stack_bytes(const pa_pool* pool, size_t* bytes);
 
 /* Copy the host free stack into dev_stack (waits for `stream`) and hand the
- * stack to the device. */
+ * stack to the device.
+ * Cites: as the section above (the same free list, moved to the device). */
 PA_API int pa_device_stack_upload(pa_pool* pool, void* dev_stack, pa_stream_t stream);
 
 /* Wait for `stream`, copy the device stack back into the host allocator
- * (validating every id) and return the stack to the host. */
+ * (validating every id) and return the stack to the host.
+ * Cites: as the section above. */
 PA_API int pa_device_stack_download(pa_pool* pool, const void* dev_stack, pa_stream_t stream);
 
 /*
@@ -215,6 +253,9 @@ PA_API int pa_device_stack_download(pa_pool* pool, const void* dev_stack, pa_str
  * pa_alloc_block calls would hand out in that order.  When the stack runs dry
  * the remaining such entries are set to -1 and PA_STATUS_NO_FREE_BLOCKS is
  * raised.  One kernel launch; no host round trip.
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool"
+ * (allocate_block, once per sequence that needs a block); "kv-cache" skill,
+ * section 2 (a new block when a sequence crosses a block boundary).
  */
 PA_API int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
                                   int max_blocks_per_seq, const int* positions, int batch,
@@ -227,6 +268,8 @@ PA_API int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tab
  * skipped and flagged (PA_STATUS_BAD_BLOCK_ID); pushing an id that is already
  * free is not detected on the device (pa_device_stack_download rejects the
  * resulting stack).
+ * Cites: mini-infer, "Python Implementation: Physical Block Pool" (free_block,
+ * once per block of a finished sequence).
  */
 PA_API int pa_device_free_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
                                  int max_blocks_per_seq, const int* context_lens,
@@ -247,6 +290,11 @@ PA_API int pa_device_free_blocks(pa_pool* pool, void* dev_stack, int* block_tabl
  *   positions     device int32 [batch]; p/B < max_blocks_per_seq required.
  * Rows whose position or block id is out of range are skipped and flagged in
  * the status word (PA_STATUS_BAD_LENGTH / PA_STATUS_BAD_BLOCK_ID).
+ * Cites: mini-infer, "The Solution" (logical block p / B of a sequence is the
+ * physical block its table names; the token sits at offset p % B) and "Python
+ * Implementation: Physical Block Pool" (the K/V, layer and KV-head axes of the
+ * pool tensor); "kv-cache" skill, section 2 "PagedAttention Architecture"
+ * (blocks filled one token at a time as generation proceeds).
  */
 PA_API int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
                 const int* block_tables, int max_blocks_per_seq, const int* positions,
@@ -276,7 +324,14 @@ PA_API int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
  * heuristically chosen number of blocks; with more than one partition a second
  * kernel merges the per-partition results (log-sum-exp combine).  The tcgen05
  * kernel instead cuts the batch's 128-token tiles into equal shares per SM
- * (see PA_DECODE_TCGEN05) and the same combine merges the cut contexts.
+ * (see PA_DECODE_TCGEN05) and a combine merges the cut contexts.
+ * Cites: "vllmini", "The CUDA Block Kernel" (the argument list out, q,
+ * caches, block_tables, context_lens, block_size, num_heads, head_size; every
+ * token resolved through the block table on the fly) and "PagedAttention
+ * Metaphor" (logical block i of a sequence in physical block block_table[i]);
+ * "vllmini", introduction (each decode step reads the K/V of all past tokens).
+ * The scale argument, the query-to-KV-head grouping and the n = 0 result are
+ * readings: the pages state none of them.
  */
 PA_API int pa_decode_attention(float* out, const void* q, const pa_pool* pool, int layer,
                         const int* block_tables, int max_blocks_per_seq,
@@ -290,6 +345,9 @@ PA_API int pa_decode_attention(float* out, const void* q, const pa_pool* pool, i
  * A partition covering the whole table (partition_blocks >= max_blocks_per_seq)
  * runs a single kernel and needs no workspace.  The tcgen05 kernel ignores
  * partition_blocks (its split depends on the lengths only).
+ * Cites: as pa_decode_attention; splitting a context into partitions has no
+ * counterpart on the pages (it is this library's way to spread a few long
+ * contexts over the whole GPU).
  */
 PA_API int pa_decode_attention_partitioned(float* out, const void* q, const pa_pool* pool, int layer,
                                     const int* block_tables, int max_blocks_per_seq,
@@ -307,6 +365,8 @@ PA_API int pa_decode_attention_partitioned(float* out, const void* q, const pa_p
  * block receiving the new token must not be read by another sequence of the
  * same call.  Bad positions / ids are flagged in the status word as for
  * pa_write_kv.  Arguments as for pa_write_kv and pa_decode_attention_partitioned.
+ * Cites: as pa_write_kv and pa_decode_attention (the pages run the two as
+ * separate steps; doing them in one launch is this library's).
  */
 PA_API int pa_write_kv_and_decode(float* out, const void* q, pa_pool* pool, int layer,
                                   const void* k, const void* v, const int* positions,
@@ -317,14 +377,16 @@ PA_API int pa_write_kv_and_decode(float* out, const void* q, pa_pool* pool, int 
                                   pa_stream_t stream);
 
 /* The partition size (in blocks) that pa_decode_attention picks for these
- * sizes on the current device.  Queries the device's SM count. */
+ * sizes on the current device.  Queries the device's SM count.
+ * Cites: no counterpart on the pages (see pa_decode_attention_partitioned). */
 PA_API int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_heads,
                                int max_blocks_per_seq, int* partition_blocks);
 
 /* Workspace bytes needed by pa_decode_attention_partitioned with the same
  * arguments (partition_blocks = 0: the heuristic choice, which queries the
  * current device; the tcgen05 kernel always queries it).  0 when a single
- * partition covers the table (tcgen05 kernel: when a single CTA runs). */
+ * partition covers the table (tcgen05 kernel: when a single CTA runs).
+ * Cites: no counterpart on the pages (the scratch of the split contexts). */
 PA_API int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_heads,
                              int max_blocks_per_seq, int partition_blocks, size_t* bytes);
 
@@ -341,8 +403,11 @@ PA_API int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_head
  * loads the library's kernels holds until the process exits.  The call makes
  * no cudaMalloc/cudaFree and no allocating library call.
  *  - A call that needs more scratch than PA_NOALLOC_SCRATCH_BYTES (see
- *    pa_decode_workspace_size) fails with PA_ERR_WORKSPACE before any launch;
- *    a larger partition_blocks needs less.
+ *    pa_decode_workspace_size) fails with PA_ERR_WORKSPACE before any launch.
+ *    On the mma.sync and CUDA-core kernels a larger partition_blocks needs
+ *    less; the tcgen05 kernel ignores partition_blocks (its scratch follows the
+ *    SM count and the number of (sequence, head group) pairs), so such a call
+ *    needs pa_decode_attention with a caller-provided workspace instead.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) and caches it; make that first call before any
  *    stream capture.
@@ -353,6 +418,7 @@ PA_API int pa_decode_workspace_size(const pa_pool* pool, int batch, int num_head
  */
 #define PA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
+/* Cites: no counterpart on the pages (see above). */
 PA_API int pa_decode_attention_noalloc(float* out, const void* q, const pa_pool* pool, int layer,
                                 const int* block_tables, int max_blocks_per_seq,
                                 const int* context_lens, int batch, int block_size,
@@ -370,6 +436,10 @@ PA_API int pa_decode_attention_noalloc(float* out, const void* q, const pa_pool*
  * length are zero-filled).  k_out, v_out 16-byte aligned; mask uint8
  * [batch, max_len].  Lengths above max_len or above the table are flagged
  * (PA_STATUS_BAD_LENGTH) and treated as 0.
+ * Cites: mini-infer, "Zero-Copy Batched Attention Gather" (all active
+ * sequences' past K/V of one layer into one [B, T, H, D] tensor plus a mask;
+ * the listing stops after the call, so T = max_len, mask 1 = valid and the
+ * zero rows past each length are readings).
  */
 PA_API int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* pool, int layer,
                  const int* block_tables, int max_blocks_per_seq, const int* context_lens,
@@ -383,11 +453,18 @@ PA_API int pa_gather_kv(void* k_out, void* v_out, uint8_t* mask, const pa_pool* 
  * barrier no copy or thread ever completes.  The bounded wait used by every
  * kernel of this library gives up (here after 20 ms), PA_STATUS_TIMEOUT is
  * raised in the status word and the kernel returns; the context stays usable.
- * No fault, trap or hang is involved. */
+ * No fault, trap or hang is involved.
+ * Cites: no counterpart on the pages (this library's failure detection). */
 PA_API int pa_selftest_wait_timeout(pa_stream_t stream);
 
 /* Wait for `stream`, return the current device's status bits (PA_STATUS_*)
- * accumulated since the last call, and clear them.  Blocking. */
+ * accumulated since the last call, and clear them.  Blocking.
+ * The word is one per device, not per pool: every kernel of the library, of
+ * any pool on that device, sets its bits in the same word, so the call takes
+ * no pool argument.
+ * Cites: no counterpart on the pages beyond the allocator's exhaustion error
+ * (mini-infer, "Python Implementation: Physical Block Pool"); the bad-id and
+ * bad-length bits report table entries and lengths the pages assume valid. */
 PA_API int pa_get_status(unsigned int* status, pa_stream_t stream);
 
 #ifdef __cplusplus

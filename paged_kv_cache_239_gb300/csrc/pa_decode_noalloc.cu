@@ -67,12 +67,23 @@ extern "C" int pa_decode_attention_noalloc(float* out, const void* q, const pa_p
                                       &need);
     if (rc != PA_OK) return rc;
     if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) {
-        char msg[320];
+        // The advice depends on the kernel the call would run: the tcgen05
+        // kernel's scratch does not depend on partition_blocks.
+        int kind = PA_DECODE_AUTO;
+        rc = pa_decode_kernel_choice(pool, num_heads, &kind);
+        if (rc != PA_OK) return rc;
+        const char* advice =
+            kind == PA_DECODE_TCGEN05
+                ? "the tcgen05 kernel this call runs ignores partition_blocks (its scratch "
+                  "follows the SM count and the (sequence, head group) pairs): use "
+                  "pa_decode_attention with a caller-provided workspace"
+                : "pass a larger partition_blocks or use pa_decode_attention with a "
+                  "caller-provided workspace";
+        char msg[512];
         std::snprintf(msg, sizeof msg,
                       "pa_decode_attention_noalloc: this call needs %zu bytes of split-K scratch "
-                      "but the built-in scratch holds %zu; pass a larger partition_blocks or use "
-                      "pa_decode_attention with a caller-provided workspace",
-                      need, (size_t)PA_NOALLOC_SCRATCH_BYTES);
+                      "but the built-in scratch holds %zu; %s",
+                      need, (size_t)PA_NOALLOC_SCRATCH_BYTES, advice);
         return pa::set_last_error(PA_ERR_WORKSPACE, msg);
     }
     void* scratch = nullptr;

@@ -57,22 +57,21 @@ def oracle_decode(wl, pool_t, q_t, layer, tables=None, lens=None, scale=None):
                                    wl.scale if scale is None else scale)
 
 
-def oracle_decode_sampled(wl, pool_gpu, q_gpu, layer, seqs, tables=None, lens=None):
-    """Oracle for a few sequences of a pool too large to copy: the blocks each
-    sequence uses (one layer) are copied to the host and the table renumbered."""
+def layer_subpool(wl, pool_gpu, layer, tables=None, lens=None):
+    """One layer of the blocks every sequence uses, copied to the host as a
+    pool [n, 2, 1, Hkv, B, D] (the layer is sliced before the rows are picked,
+    so a 71 GB pool costs one layer's bytes), with the tables renumbered to it:
+    sequence b's blocks sit at consecutive ids in table order."""
     tables = wl.block_tables if tables is None else tables
     lens = wl.context_lens if lens is None else lens
-    res = {}
-    for b in seqs:
-        n = int(lens[b])
-        nblk = max(1, -(-n // wl.block_size))
-        ids = torch.from_numpy(tables[b, :nblk].astype(np.int64)).to(pool_gpu.device)
-        sub = pool_gpu.index_select(0, ids)[:, :, layer:layer + 1].contiguous().cpu()
-        q = q_gpu[b:b + 1].cpu()
-        res[b] = oracle.decode_attention(W.as_oracle_array(q), W.as_oracle_array(sub), 0,
-                                         np.arange(nblk, dtype=np.int32)[None], [n],
-                                         wl.num_heads, wl.scale)[0]
-    return res
+    ids, rows = [], np.full(tables.shape, -1, np.int32)
+    for b in range(len(lens)):
+        nblk = -(-int(lens[b]) // wl.block_size)
+        rows[b, :nblk] = np.arange(len(ids), len(ids) + nblk, dtype=np.int32)
+        ids.extend(int(x) for x in tables[b, :nblk])
+    idx = torch.tensor(ids, dtype=torch.long, device=pool_gpu.device)
+    sub = pool_gpu[:, :, layer].index_select(0, idx).unsqueeze(2).contiguous().cpu()
+    return sub, rows
 
 
 def max_abs_err(gpu_out, ref):

@@ -34,6 +34,29 @@ def test_only_header_functions_are_exported(pa_lib):
     assert sorted(funcs) == pa_lib.header_symbols()
 
 
+def test_every_declaration_cites_its_passage():
+    """Each exported call's comment names the page and section it restates, or
+    says that the pages have no counterpart ("Cites:")."""
+    import os
+
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                        "pagedattn.h")
+    lines = open(path).read().split("\n")
+    missing = []
+    for i, line in enumerate(lines):
+        if not line.startswith("PA_API"):
+            continue
+        j = i - 1
+        while j >= 0 and not lines[j].rstrip().endswith("*/"):
+            j -= 1
+        k = j
+        while k >= 0 and "/*" not in lines[k]:
+            k -= 1
+        if "Cites:" not in "\n".join(lines[k:j + 1]):
+            missing.append(line.split("(")[0].split()[-1])
+    assert not missing, f"declarations without a citation: {missing}"
+
+
 def _pool(pa_lib, nb=8, L=2, Hkv=2, B=16, D=64, dtype=1):
     return pa_lib.pa_pool_create(FAKE_DEV_PTR, nb, L, Hkv, B, D, dtype)
 

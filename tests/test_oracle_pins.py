@@ -243,3 +243,33 @@ def test_append_then_decode_uses_new_token(oracle_lib):
     for b, n in enumerate(lens1):
         assert np.all(vv[b, n - 1] == 3.5)
         np.testing.assert_allclose(out[b], vv[b, :n].astype(np.float64).mean(0), atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype,Hkv,B,extra", [("bf16", 2, 16, 7), ("f32", 3, 32, 1),
+                                               ("bf16", 1, 16, 40)])
+def test_gather_matches_numpy_slicing_with_padding(oracle_lib, dtype, Hkv, B, extra):
+    """The batched gather (mini-infer, "Zero-Copy Batched Attention Gather"; its
+    listing stops after the call, so the output beyond each length is a reading:
+    zero rows and mask 0) against NumPy advanced indexing of the six-dimensional
+    pool array, with max_len past the longest context so every sequence has a
+    padded tail.  An inverted mask, a padding that is not zeroed, a swapped KV
+    head or K/V half, or a wrong layer or slot fails it."""
+    lens = [0, 1, B - 1, B, B + 1, 3 * B + 5]
+    wl = W.custom("gpad", dtype, 3, 2 * Hkv, Hkv, 64, B, lens, seed=31 + Hkv, spare_blocks=3,
+                  interleave=True)
+    pool = _pool_np(W.make_pool(wl))
+    layer = 2
+    T = int(max(lens)) + extra
+    k, v, mask = oracle.gather_kv(pool, layer, wl.block_tables, wl.context_lens, T)
+    assert k.shape == v.shape == (len(lens), T, Hkv, 64)
+    assert mask.shape == (len(lens), T) and mask.dtype == bool
+    for b, n in enumerate(lens):
+        t = np.arange(n)
+        blk = wl.block_tables[b, t // B]
+        # advanced indices separated by a slice: result [n, Hkv, D]
+        np.testing.assert_array_equal(k[b, :n], pool[blk, 0, layer, :, t % B, :])
+        np.testing.assert_array_equal(v[b, :n], pool[blk, 1, layer, :, t % B, :])
+        assert mask[b, :n].all() and not mask[b, n:].any()
+        assert not k[b, n:].any() and not v[b, n:].any()
+    # the padded region is genuinely present for every sequence
+    assert (~mask).sum() == sum(T - n for n in lens)

@@ -11,8 +11,8 @@ import oracle
 from oracle.allocator import FreeBlockStack
 from paged_kv_cache_239_gb300 import binding as B
 from paged_kv_cache_239_gb300 import workloads as W
-from gpu_helpers import (TOL, GpuPool, device_tables, gpu_decode, max_abs_err, oracle_decode,
-                         oracle_decode_sampled)
+from gpu_helpers import (TOL, GpuPool, device_tables, gpu_decode, layer_subpool, max_abs_err,
+                         oracle_decode)
 
 pytestmark = pytest.mark.gpu
 
@@ -108,27 +108,54 @@ def test_decode_long_context_split(cuda_device):
 
 
 @pytest.mark.slow
-def test_decode_large_batch_sampled(cuda_device):
+def test_decode_large_batch_every_sequence(cuda_device):
     """Full-size large-batch workload (about 71 GB of pool) in the launch
-    configuration the benchmark times; sampled sequences against the oracle."""
+    configuration the benchmark times: every sequence and head of the first
+    and the last layer against the oracle, element by element, on the
+    automatic kernel and the CUDA-core kernel; then the benchmark's own call
+    (the new token appended at the last context slot inside the decode
+    launch) on the last layer, the whole layer's pool bytes compared too."""
     wl = W.named(3)
     pool = W.make_pool(wl, device=cuda_device)
     qs = W.make_queries(wl, 2, device=cuda_device)
+    ks, vs = W.make_new_tokens(wl, 1, device=cuda_device)
     gp = GpuPool(wl, pool)
     bt, ln = device_tables(wl, cuda_device)
-    rng = np.random.default_rng(0)
-    order = np.argsort(wl.context_lens)
-    seqs = sorted(set([int(order[0]), int(order[-1])] + [int(x) for x in rng.choice(wl.batch, 10,
-                                                                                     replace=False)]))
-    for layer in (0, wl.num_layers - 1):
-        refs = oracle_decode_sampled(wl, pool, qs[layer % 2], layer, seqs)
+    last = wl.num_layers - 1
+    for layer in (0, last):
+        q = qs[layer % 2]
+        sub, rows = layer_subpool(wl, pool, layer)
+        ref = oracle.decode_attention(W.as_oracle_array(q.cpu()), W.as_oracle_array(sub), 0,
+                                      rows, wl.context_lens, wl.num_heads, wl.scale)
         for kind in (B.PA_DECODE_AUTO, B.PA_DECODE_CUDA_CORES):
             B.pa_pool_set_decode_kernel(gp.h, kind)
-            out = gpu_decode(gp, qs[layer % 2], layer, bt, ln)
+            out = gpu_decode(gp, q, layer, bt, ln)
             torch.cuda.synchronize()
             assert torch.isfinite(out).all()
-            for b, ref in refs.items():
-                assert max_abs_err(out[b], ref) <= 2e-3, (layer, b, kind)
+            err = max_abs_err(out, ref)
+            assert err <= 2e-3, (layer, kind, err)
+    _check_status()
+
+    # the benchmark's step for one layer: append at position n - 1, decode over n
+    B.pa_pool_set_decode_kernel(gp.h, B.PA_DECODE_AUTO)
+    sub, rows = layer_subpool(wl, pool, last)
+    host = W.as_oracle_array(sub).copy()
+    pos = (ln - 1).contiguous()
+    oracle.write_kv(host, 0, W.as_oracle_array(ks[0].cpu()), W.as_oracle_array(vs[0].cpu()), rows,
+                    wl.context_lens - 1)
+    ref = oracle.decode_attention(W.as_oracle_array(qs[1].cpu()), host, 0, rows,
+                                  wl.context_lens, wl.num_heads, wl.scale)
+    need = B.pa_decode_workspace_size(gp.h, wl.batch, wl.num_heads, wl.max_blocks, 0)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=cuda_device)
+    out = torch.full((wl.batch, wl.num_heads, wl.head_dim), float("nan"), device=cuda_device)
+    B.pa_write_kv_and_decode(out, qs[1], gp.h, last, ks[0], vs[0], pos, bt, wl.max_blocks, ln,
+                             wl.batch, wl.block_size, wl.num_heads, wl.num_kv_heads,
+                             wl.head_dim, wl.scale, 0, ws, need)
+    torch.cuda.synchronize()
+    err = max_abs_err(out, ref)
+    assert err <= 2e-3, err
+    after, _ = layer_subpool(wl, pool, last)
+    assert np.array_equal(W.as_oracle_array(after), host), "appended layer differs from the oracle"
     _check_status()
     gp.close()
     del pool
