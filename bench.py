@@ -12,6 +12,13 @@ needed between steps.  By default the K timed steps run as one CUDA graph
 replay (the calls captured once, each decode call bracketed by event-record
 nodes for its per-call time); --no-graph launches every call from the host.
 
+After the headline line's own measurements, the same run measures the other
+workloads one at a time (graph-timed, each with its clock record) and adds them
+to the line as "workloads": the batched gather on the large-batch pool, the
+mini-infer-shaped 24-layer step, the long-context call, the large-batch lengths
+with 16-, 32- and 64-query-head groups (the tcgen05 kernel), and the append +
+decode loop with the free stack on the device.  --no-workloads skips them.
+
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 Under torchrun every rank runs an independent replica (weak scaling, no
 collective on the data path); the timed region is bracketed by barriers and the
@@ -74,15 +81,15 @@ def decode_flops(wl) -> int:
 
 
 # DRAM bytes (read + write) of one layer's pa_write_kv_and_decode call on this
-# workload, one ncu capture of both kernels of the call (--metrics
-# dram__bytes_read.sum,dram__bytes_write.sum): pa_decode_mma_kernel with the
-# fused append 2,231,260,160 read + 6,223,104 written, pa_combine_kernel
-# 9,856,000 read + 0 written; see profiles/.  Valid only for the sources they
-# were taken from (the kernels, the shared device code, and the dispatch /
-# partition choice in pa_api.cpp).
+# workload, one ncu capture per kernel on the 1-layer pool (--metrics
+# dram__bytes_read.sum,dram__bytes_write.sum, -k one kernel, -c 2):
+# pa_decode_mma_kernel with the fused append 2,231,241,984 read + 6,255,616
+# written, pa_combine_kernel 9,850,880 read + 0 written; see profiles/.  Valid
+# only for the sources they were taken from (the kernels, the shared device
+# code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231260160 + 6223104 + 9856000,
-    "sources_sha256": "de4596a6aef044b0a42b301d7ceb33bd5f7d1e6bbd0763a2e6386a2749048f9e",
+    "bytes_per_launch": 2231241984 + 6255616 + 9850880,
+    "sources_sha256": "b383f4529ebb6323376e3d78b7933d45d9685f63ea849458b657c07f901d4013",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h", "pa_api.cpp", "pa_fused_append.cuh"]
@@ -101,6 +108,13 @@ def decode_traffic():
     if decode_sources_sha256() == DECODE_TRAFFIC["sources_sha256"]:
         return DECODE_TRAFFIC["bytes_per_launch"]
     return None
+
+
+# The GB300's nominal HBM3e bandwidth (8 stacks, ~7.9 TB/s): the denominator of
+# the "fraction of HBM peak" the target is stated in.  The roofline itself is
+# taken against the measured copy bandwidth (MEASURED_PEAKS.json), which a
+# read-mostly stream can exceed.
+NOMINAL_HBM_GBS = 7900.0
 
 
 def measured_peaks():
@@ -569,7 +583,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             "l2": l2_note(wl, L),
             "parallelism": f"replicas x{world}",
         },
-        "pct_hbm_peak": 100.0 * value / peak,
+        "pct_of_measured_copy_peak": 100.0 * value / peak,
+        "pct_of_nominal_hbm_peak": 100.0 * value / NOMINAL_HBM_GBS,
         "decode_tokens_per_s": wl.batch * steps * world / (total_ms / 1e3),
         "roofline": {"bound": "hbm",
                      "kernel": ("pa_write_kv_and_decode (append + decode + combine)" if args.fused
@@ -600,8 +615,172 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "gpu_launches": launches_per_step * steps,
         "clocks": clocks.summary(),
     }
+    if not args.no_workloads and world == 1:
+        # the other workloads, each measured alone after the headline (the
+        # gather on this pool first, then the pool is freed)
+        extra = [measure_gather(B, torch, wl, pool, h, bt, lens, dev, layers=4)]
+        B.pa_pool_destroy(h)
+        h = None
+        del pool, qs, ks, vs, outs, ws, sets, graph, step_graph
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        extra += run_extra_workloads(args, B, torch, W, dev)
+        line["workloads"] = extra
     print(json.dumps(line), flush=True)
-    B.pa_pool_destroy(h)
+    if h is not None:
+        B.pa_pool_destroy(h)
+
+
+def timed_graph_calls(torch, dev, call, ncalls, target_s=0.5):
+    """CUDA-graph replays of `ncalls` calls (call(i)), warmed up, repeated
+    until about target_s seconds have been timed with CUDA events on the
+    replaying stream; returns (ms per call, clock summary)."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for i in range(ncalls):       # warm-up, outside the graph
+            call(i, side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(ncalls):
+                call(i, side)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    reps = max(3, min(200, int(target_s * 1e3 / max(e0.elapsed_time(e1), 1e-3))))
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+    del g
+    return e0.elapsed_time(e1) / (reps * ncalls), clocks.summary()
+
+
+def measure_step(B, torch, W, dev, wl, name, note=""):
+    """Fused append + decode over every layer of a workload's pool (the
+    benchmark step's call), graph-timed."""
+    pool = W.make_pool(wl, device=dev)
+    L = wl.num_layers
+    qs = W.make_queries(wl, L, device=dev)
+    ks, vs = W.make_new_tokens(wl, L, device=dev)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    lens = torch.from_numpy(wl.context_lens).to(dev)
+    pos = (lens - 1).contiguous()
+    h = B.pa_pool_create(pool, wl.num_blocks, L, wl.num_kv_heads, wl.block_size, wl.head_dim,
+                         pool.dtype)
+    try:
+        kind = B.pa_decode_kernel_choice(h, wl.num_heads)
+        need = B.pa_decode_workspace_size(h, wl.batch, wl.num_heads, wl.max_blocks, 0)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        outs = torch.empty((L, wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32,
+                           device=dev)
+        lib = B.lib()
+
+        def call(i, stream):
+            l = i % L
+            rc = lib.pa_write_kv_and_decode(outs[l].data_ptr(), qs[l].data_ptr(), h, l,
+                                            ks[l].data_ptr(), vs[l].data_ptr(), pos.data_ptr(),
+                                            bt.data_ptr(), wl.max_blocks, lens.data_ptr(),
+                                            wl.batch, wl.block_size, wl.num_heads,
+                                            wl.num_kv_heads, wl.head_dim, wl.scale, 0,
+                                            ws.data_ptr(), need, stream.cuda_stream)
+            if rc:
+                raise RuntimeError(B.last_error())
+
+        ms, clk = timed_graph_calls(torch, dev, call, max(L, 8))
+        st = B.pa_get_status()
+        if st:
+            raise RuntimeError(f"device status {st:#x} in workload {name}")
+    finally:
+        B.pa_pool_destroy(h)
+    peak, kind_p = measured_peaks()
+    nbytes = decode_bytes(wl)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res = {"workload": name, "value": gbs, "unit": UNIT,
+           "frac_of_measured_copy_peak": gbs / peak, "frac_of_nominal_hbm_peak":
+           gbs / NOMINAL_HBM_GBS, "ms_per_call": ms, "decode_kernel": kernel_name(B, kind),
+           "decode_tokens_per_s": wl.batch / (ms * L / 1e3),
+           "shape": {"batch": wl.batch, "num_heads": wl.num_heads,
+                     "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                     "block_size": wl.block_size, "num_layers": L},
+           "timing": "graph replays of the fused append + decode call over the pool's layers, "
+                     "CUDA events", "clocks": clk}
+    if note:
+        res["note"] = note
+    del pool, qs, ks, vs, outs, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_gather(B, torch, wl, pool, h, bt, lens, dev, layers):
+    """Row N1: pa_gather_kv of `layers` layers of a workload's pool, graph-timed."""
+    T = int(wl.context_lens.max())
+    shape = (wl.batch, T, wl.num_kv_heads, wl.head_dim)
+    k = torch.empty(shape, dtype=pool.dtype, device=dev)
+    v = torch.empty(shape, dtype=pool.dtype, device=dev)
+    m = torch.empty((wl.batch, T), dtype=torch.uint8, device=dev)
+    lib = B.lib()
+
+    def call(i, stream):
+        rc = lib.pa_gather_kv(k.data_ptr(), v.data_ptr(), m.data_ptr(), h, i % layers,
+                              bt.data_ptr(), wl.max_blocks, lens.data_ptr(), wl.batch, T,
+                              stream.cuda_stream)
+        if rc:
+            raise RuntimeError(B.last_error())
+
+    ms, clk = timed_graph_calls(torch, dev, call, layers)
+    assert B.pa_get_status() == 0
+    rd = int(wl.context_lens.astype(np.int64).sum()) * 2 * wl.num_kv_heads * wl.head_dim * wl.elem_bytes
+    wr = 2 * wl.batch * T * wl.num_kv_heads * wl.head_dim * wl.elem_bytes + wl.batch * T
+    nb = rd + wr + int(sum(-(-int(n) // wl.block_size) for n in wl.context_lens)) * 4
+    peak, _ = measured_peaks()
+    gbs = nb / (ms / 1e3) / 1e9
+    del k, v, m
+    torch.cuda.empty_cache()
+    return {"workload": f"gather_kv ({wl.name} layers)", "value": gbs, "unit": UNIT,
+            "frac_of_measured_copy_peak": gbs / peak,
+            "frac_of_nominal_hbm_peak": gbs / NOMINAL_HBM_GBS, "ms_per_call": ms,
+            "bytes_per_call": nb, "timing": "graph replays of pa_gather_kv over 4 layers",
+            "clocks": clk}
+
+
+def run_extra_workloads(args, B, torch, W, dev):
+    """The named workloads other than the headline, and the large-batch
+    lengths with the large query groups the tcgen05 kernel serves."""
+    res = []
+    res.append(measure_step(B, torch, W, dev, W.named(2), "mini_infer_bf16",
+                            "K/V per layer below L2; consecutive layers read disjoint slices"))
+    res.append(measure_step(B, torch, W, dev, W.named(4), "long_context_bf16",
+                            "one layer: every call re-reads the same 1.35 GB (10x L2)"))
+    for H, Hkv in ((32, 2), (32, 1), (64, 1)):
+        wl = W.named(3)
+        wl.num_heads, wl.num_kv_heads, wl.num_layers = H, Hkv, 16 if Hkv == 1 else 8
+        res.append(measure_step(B, torch, W, dev, wl,
+                                f"large_batch_bf16 lengths, {H} query / {Hkv} KV heads "
+                                f"(group {H // Hkv})"))
+    res.append(measure_loop(B, torch, W, dev))
+    return res
+
+
+def measure_loop(B, torch, W, dev):
+    """Workload 5, the append + decode loop with the free stack on the device,
+    each run of 64 steps one CUDA graph."""
+    import types
+
+    a = types.SimpleNamespace(workload=5, warmup=3, steps=16, device_alloc=True)
+    buf = {}
+    run_loop(a, dev.index or 0, _result=buf)
+    return buf["result"]
 
 
 def _setup(args, local_rank, cfg):
@@ -661,7 +840,7 @@ def run_gather(args, local_rank: int) -> None:
     B.pa_pool_destroy(h)
 
 
-def run_loop(args, local_rank: int) -> None:
+def run_loop(args, local_rank: int, _result=None) -> None:
     """The append+decode loop (workload 5 by default): every step takes a block
     for each sequence crossing a block boundary (host free stack), copies the
     changed table rows, appends one token per sequence and decodes over n+1.
@@ -721,7 +900,8 @@ def run_loop(args, local_rank: int) -> None:
         return lens
 
     if args.device_alloc:
-        return run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev)
+        return run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev,
+                               _result)
     for _ in range(max(1, args.warmup // 3)):
         reset()
         run()
@@ -749,7 +929,8 @@ def run_loop(args, local_rank: int) -> None:
     B.pa_pool_destroy(h)
 
 
-def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev):
+def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev,
+                    _result=None):
     """The same loop with the free stack on the device: each step is
     pa_device_alloc_blocks + pa_write_kv_and_decode + a length increment, and a
     whole run of `nsteps` steps is one CUDA graph replay (no host round trip)."""
@@ -794,14 +975,15 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
     torch.cuda.synchronize()
     runs = max(1, args.steps // 4)
     ms = 0.0
-    for _ in range(runs):
-        reset()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        ms += e0.elapsed_time(e1)
+    with ClockSampler(torch.cuda.current_device()) as clocks:
+        for _ in range(runs):
+            reset()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
     st = B.pa_get_status()
     assert st == 0, st
     kv = 0
@@ -810,14 +992,20 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
         kv += int(n.sum()) * 2 * wl.num_kv_heads * wl.head_dim * wl.elem_bytes
     peak, kind = measured_peaks()
     gbs = kv * runs / (ms / 1e3) / 1e9
-    print(json.dumps({"row": "loop_device", "workload": wl.name, "steps_per_run": nsteps,
-                      "runs": runs, "decode_tokens_per_s": wl.batch * nsteps * runs / (ms / 1e3),
-                      "kv_gbs": gbs, "frac_of_peak": gbs / peak, "ms_per_step": ms / (runs * nsteps),
-                      "partition_blocks": pb,
-                      "timing": "CUDA events around one graph replay per run (device allocation, "
-                                "fused append+decode, length update)"}), flush=True)
+    res = {"workload": wl.name, "value": gbs, "unit": UNIT, "steps_per_run": nsteps,
+           "runs": runs, "decode_tokens_per_s": wl.batch * nsteps * runs / (ms / 1e3),
+           "frac_of_measured_copy_peak": gbs / peak,
+           "frac_of_nominal_hbm_peak": gbs / NOMINAL_HBM_GBS,
+           "ms_per_step": ms / (runs * nsteps), "partition_blocks": pb,
+           "decode_kernel": kernel_name(B, B.pa_decode_kernel_choice(h, wl.num_heads)),
+           "timing": "CUDA events around one graph replay per run (device allocation, fused "
+                     "append+decode, length update)", "clocks": clocks.summary()}
     B.pa_device_stack_download(h, stack)
     B.pa_pool_destroy(h)
+    if _result is not None:
+        _result["result"] = res
+        return
+    print(json.dumps({"row": "loop_device", **res}), flush=True)
 
 
 def main():
@@ -851,6 +1039,8 @@ def main():
                          "--num-heads 64 --kv-heads 1 for the tcgen05 kernel)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads measured after the headline")
     ap.add_argument("--pool-layers", type=int, default=0,
                     help="build the pool with this many layers (0 = the workload's 32); "
                          "for small profiler captures, not for reported numbers")
@@ -862,6 +1052,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        raise SystemExit(f"--gpus {args.gpus} but {world} process(es): for N > 1 launch one "
+                         f"process per GPU with torch.distributed.run (WORLD_SIZE = N)")
     if world > 1:
         import torch.distributed as dist
 
