@@ -107,8 +107,9 @@ size_t workspace_bytes_for(int batch, int H, int Cmax, int D) {
 }
 
 // tcgen05 kernel: two partial slots of `chunk` heads per CTA (its first and
-// last piece), one int4 descriptor per (sequence, head group), then one int
-// per CTA naming the cut pair whose first piece it holds.
+// last piece), one int4 descriptor per (sequence, head group), then one int4
+// per CTA naming the cut pair whose first piece it holds (with its
+// descriptor).
 size_t tc_partial_slots(int grid, int chunk) { return (size_t)grid * 2 * chunk; }
 size_t tc_desc_offset(int grid, int chunk, int D) {
     const size_t S = tc_partial_slots(grid, chunk);
@@ -119,7 +120,7 @@ size_t tc_cut_offset(int grid, int chunk, int D, long long pairs) {
 }
 size_t tc_workspace_bytes(int grid, int chunk, int D, long long pairs) {
     if (grid <= 1) return 0;
-    return tc_cut_offset(grid, chunk, D, pairs) + (size_t)grid * sizeof(int);
+    return tc_cut_offset(grid, chunk, D, pairs) + (size_t)grid * sizeof(int4);
 }
 
 int check_pool(const pa_pool* pool) {
@@ -648,7 +649,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     float* part_o = nullptr;
     float* part_ml = nullptr;
     int4* tc_desc = nullptr;
-    int* tc_cut = nullptr;
+    int4* tc_cut = nullptr;
     if (sh.ws_bytes > 0) {
         if (!workspace || workspace_bytes < sh.ws_bytes || !aligned(workspace, 256))
             return fail(PA_ERR_WORKSPACE,
@@ -661,7 +662,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
             const long long pairs = (long long)batch * g.Hkv * (sh.G / sh.chunk);
             part_ml = reinterpret_cast<float*>(ws + align256(S * g.D * sizeof(float)));
             tc_desc = reinterpret_cast<int4*>(ws + tc_desc_offset(sh.tc_grid, sh.chunk, g.D));
-            tc_cut = reinterpret_cast<int*>(ws + tc_cut_offset(sh.tc_grid, sh.chunk, g.D, pairs));
+            tc_cut = reinterpret_cast<int4*>(ws + tc_cut_offset(sh.tc_grid, sh.chunk, g.D, pairs));
         } else {
             part_ml = reinterpret_cast<float*>(
                 ws + align256((size_t)batch * num_heads * sh.Cmax * g.D * sizeof(float)));

@@ -492,10 +492,12 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
 //   M = max_c m_c,  out = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c .
 // W warps (1, 2, 4 or 8) serve one head; a 256-thread CTA serves 8 / W of them
 // (hl: this warp's head slot in the CTA, w: its warp within the head).  Warp w
-// takes partials w, w + W, ... four at a time (four independent loads in
-// flight per lane; a lane owns D/32 consecutive elements), then the W partial
-// sums are merged through shared memory.  Every thread of the CTA calls it
-// (it synchronises the CTA); nparts <= 1 writes nothing.  slot_of(c) is the
+// takes partials w, w + W, ... four at a time (four independent loads of
+// (m, l, O) in flight per lane; a lane owns D/32 consecutive elements) and
+// keeps a running maximum, rescaling its sums when it rises, so the partials
+// are read in one pass; the W warps' (max, sum, O) are then merged through
+// shared memory the same way.  Every thread of the CTA calls it (it
+// synchronises the CTA); nparts <= 1 writes nothing.  slot_of(c) is the
 // workspace slot of partial c.
 template <int D, int W, typename SlotOf>
 __device__ __forceinline__ void combine_head(const DecodeParams& p, long long gh, int nparts,
@@ -506,36 +508,24 @@ __device__ __forceinline__ void combine_head(const DecodeParams& p, long long gh
     __shared__ float s_m[8];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // running max over this head's partials, per warp then across the W warps
-    float M = -INFINITY;
-    if (nparts > 1)
-        for (int c = w * 32 + lane; c < nparts; c += W * 32)
-            M = fmaxf(M, __ldg(p.part_ml + 2 * slot_of(c)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
-    if (lane == 0) s_m[warp] = M;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < W; ++i) M = fmaxf(M, s_m[hl * W + i]);
-
+    float M = -INFINITY, L = 0.f;
     float acc[PL];
 #pragma unroll
     for (int i = 0; i < PL; ++i) acc[i] = 0.f;
-    float L = 0.f;
     if (nparts > 1) {
         for (int c0 = w; c0 < nparts; c0 += 4 * W) {
-            float wt[4], ov[4][PL];
+            float mv[4], lv[4], ov[4][PL];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int c = c0 + u * W;
-                wt[u] = 0.f;
+                mv[u] = -INFINITY;
+                lv[u] = 0.f;
 #pragma unroll
                 for (int i = 0; i < PL; ++i) ov[u][i] = 0.f;
                 if (c < nparts) {
                     const long long sl = slot_of(c);
-                    const float mc = __ldg(p.part_ml + 2 * sl);
-                    wt[u] = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-                    L += wt[u] * __ldg(p.part_ml + 2 * sl + 1);
+                    mv[u] = __ldg(p.part_ml + 2 * sl);
+                    lv[u] = __ldg(p.part_ml + 2 * sl + 1);
                     const float* oc = p.part_o + sl * D + lane * PL;
                     if constexpr (PL == 4) {
                         const float4 v = __ldg(reinterpret_cast<const float4*>(oc));
@@ -549,28 +539,59 @@ __device__ __forceinline__ void combine_head(const DecodeParams& p, long long gh
                     }
                 }
             }
+            float mn = M;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 4; ++u) mn = fmaxf(mn, mv[u]);
+            if (mn == -INFINITY) continue;  // (nothing but empty partials so far)
+            const float sc = (M == -INFINITY) ? 0.f : exp2f(M - mn);
+            L *= sc;
 #pragma unroll
-                for (int i = 0; i < PL; ++i) acc[i] += wt[u] * ov[u][i];
+            for (int i = 0; i < PL; ++i) acc[i] *= sc;
+            M = mn;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float wt = (mv[u] == -INFINITY) ? 0.f : exp2f(mv[u] - M);
+                L += wt * lv[u];
+#pragma unroll
+                for (int i = 0; i < PL; ++i) acc[i] += wt * ov[u][i];
+            }
         }
     }
+    if constexpr (W > 1) {
 #pragma unroll
-    for (int i = 0; i < PL; ++i) s_acc[warp][lane * PL + i] = acc[i];
-    if (lane == 0) s_l[warp] = L;
+        for (int i = 0; i < PL; ++i) s_acc[warp][lane * PL + i] = acc[i];
+        if (lane == 0) {
+            s_l[warp] = L;
+            s_m[warp] = M;
+        }
+    }
     __syncthreads();
     if (nparts > 1 && w == 0) {
-        float Lt = 0.f;
+        if constexpr (W > 1) {
+            float Mt = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < W; ++i) Lt += s_l[hl * W + i];
-        float* o = p.out + gh * D + lane * PL;
+            for (int k = 0; k < W; ++k) Mt = fmaxf(Mt, s_m[hl * W + k]);
+            float wk[W];
+            float Lt = 0.f;
 #pragma unroll
-        for (int i = 0; i < PL; ++i) {
-            float a = 0.f;
+            for (int k = 0; k < W; ++k) {
+                const float mk = s_m[hl * W + k];
+                wk[k] = (mk == -INFINITY) ? 0.f : exp2f(mk - Mt);
+                Lt += wk[k] * s_l[hl * W + k];
+            }
 #pragma unroll
-            for (int k = 0; k < W; ++k) a += s_acc[hl * W + k][lane * PL + i];
-            o[i] = Lt > 0.f ? a / Lt : 0.f;
+            for (int i = 0; i < PL; ++i) {
+                float a = 0.f;
+#pragma unroll
+                for (int k = 0; k < W; ++k) a += wk[k] * s_acc[hl * W + k][lane * PL + i];
+                acc[i] = a;
+            }
+            L = Lt;
         }
+        float* o = p.out + gh * D + lane * PL;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) o[i] = acc[i] * inv;
     }
 }
 
@@ -601,10 +622,11 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, i
 // cut at its CTAs' range ends.  CTA group k (chunk / (8 / W) CTAs, one per 8 /
 // W heads of the chunk) serves pair k (direct: fewer pairs than decode CTAs,
 // so most are cut) or the pair tc_cut[k] whose first piece decode CTA k holds
-// (-1: none).  The pair's descriptor {first CTA, pieces, slot of the first
-// piece} places piece c at slot ((first + c) * 2 + (c == 0 ? slot0 : 0)) *
-// chunk + head in chunk: piece c came from CTA first + c, and only the first
-// piece can be a CTA's second.
+// (pair -1: none), which carries the pair's descriptor {first CTA, pieces,
+// slot of the first piece} itself (direct: the pair's descriptor).  Piece c
+// sits at slot ((first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + head in
+// chunk: piece c came from CTA first + c, and only the first piece can be a
+// CTA's second.
 template <int D, int W>
 __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p, int direct) {
     pdl_trigger();
@@ -618,11 +640,18 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
     const long long k = blockIdx.x / cpp;
     const int hh = (int)(blockIdx.x % cpp) * HPC + hl;  // head within the chunk
     const long long npairs = (long long)p.batch * p.Hkv * p.nchunks;
-    const long long pair = direct ? k : (long long)__ldg(p.tc_cut + k);
+    long long pair = k;
+    int4 d = make_int4(0, 0, 0, 0);
+    if (direct) {
+        if (k < npairs) d = p.tc_desc[k];
+    } else {
+        const int4 rec = p.tc_cut[k];
+        pair = rec.x;
+        d = make_int4(rec.y, rec.z, rec.w, 0);
+    }
     int nparts = 0, first = 0, slot0 = 0;
     long long gh = 0;
     if (pair >= 0 && pair < npairs) {
-        const int4 d = p.tc_desc[pair];
         first = d.x;
         nparts = d.y;
         slot0 = d.z;

@@ -266,10 +266,11 @@ struct UmmaCfg {
 };
 
 // Work schedule: equal shares of 128-token tiles per persistent CTA (see
-// pa_schedule.cuh), each (sequence, head group) pair charged three extra units
+// pa_schedule.cuh), each (sequence, head group) pair charged two extra units
 // for a piece's fixed cost (q, the first tile's maximum, the output, the next
-// copies' latency).
-constexpr int kUmmaPieceUnits = 3;
+// copies' latency; GB300, once a piece's inputs were loaded a piece ahead: 2
+// ahead of 3 by 1-2 % at 16 and 32 heads, level at 64, 0 and 1 slower).
+constexpr int kUmmaPieceUnits = 2;
 using UItem = SPiece;
 using UWalk = SWalk;
 
@@ -700,7 +701,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                                                   : -1;
         };
         // (this CTA's cut pair, if any, is recorded below; none so far)
-        if (warp == C::SM_WARP0 && lane == 0 && p.tc_cut != nullptr) p.tc_cut[blockIdx.x] = -1;
+        if (warp == C::SM_WARP0 && lane == 0 && p.tc_cut != nullptr)
+            p.tc_cut[blockIdx.x] = make_int4(-1, 0, 0, 0);
         UItem it;
         bool have = umma_walk_next<B, G>(p, w, it);
         int blk0 = have ? first_block(it) : -1;
@@ -714,7 +716,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 const int pieces = sched_pieces(it, w);
                 const long long pair = (long long)it.b * p.Hkv * p.nchunks + it.g;
                 p.tc_desc[pair] = make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
-                if (!it.whole) p.tc_cut[blockIdx.x] = (int)pair;
+                if (!it.whole)
+                    p.tc_cut[blockIdx.x] =
+                        make_int4((int)pair, (int)blockIdx.x, pieces, it.first ? 0 : 1);
             }
             if (it.ntiles == 0) {  // empty context: output 0 (always a whole piece)
 #pragma unroll

@@ -66,8 +66,9 @@ struct DecodeParams {
     int tc_grid;
     int4* tc_desc;
     // tcgen05 kernel: per decode CTA, the (sequence, head group) pair whose
-    // first piece it holds and which continues past its range (-1: none)
-    int* tc_cut;
+    // first piece it holds and which continues past its range, as {pair, first
+    // CTA, pieces, slot of the first piece} (pair -1: none)
+    int4* tc_cut;
 };
 
 struct WriteParams {
