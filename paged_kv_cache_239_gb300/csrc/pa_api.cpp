@@ -210,15 +210,19 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         const long long pairs = (long long)batch * pool->g.Hkv * (G / chunk);
         if (pairs > INT_MAX)
             return fail(PA_ERR_INVALID_ARG, "%lld (sequence, head group) pairs is too many", pairs);
+        // groups served in nc chunks: nc groups of CTAs over the same work
+        const long long nc = G / chunk;
+        const long long kv_pairs = (long long)batch * pool->g.Hkv;
         const long long tiles = ((long long)maxb * pool->g.B + 127) / 128;
-        const long long units = pairs * (tiles > 1 ? tiles : 1);  // upper bound
-        const int grid = (int)(units < sms ? units : sms);
+        const long long units = kv_pairs * (tiles > 1 ? tiles : 1);  // upper bound per group
+        const long long per_group = std::max(1LL, std::min(units, (long long)sms / nc));
+        const int grid = (int)(per_group * nc);
         out->G = G;
         out->kernel = kernel;
         out->PB = maxb;
         // (Cmax only sizes the combine: pieces per pair when all contexts are
         // equally long -- fewer pairs than CTAs means long ones cut in many)
-        out->Cmax = pairs < grid ? (int)((grid + pairs - 1) / pairs) + 1 : 2;
+        out->Cmax = kv_pairs < per_group ? (int)((per_group + kv_pairs - 1) / kv_pairs) + 1 : 2;
         out->chunk = chunk;
         out->tc_grid = grid;
         out->ws_bytes = tc_workspace_bytes(grid, chunk, pool->g.D, pairs);

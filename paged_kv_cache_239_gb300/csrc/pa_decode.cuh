@@ -624,9 +624,9 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, i
 // so most are cut) or the pair tc_cut[k] whose first piece decode CTA k holds
 // (pair -1: none), which carries the pair's descriptor {first CTA, pieces,
 // slot of the first piece} itself (direct: the pair's descriptor).  Piece c
-// sits at slot ((first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + head in
-// chunk: piece c came from CTA first + c, and only the first piece can be a
-// CTA's second.
+// sits at slot ((first + c nchunks) * 2 + (c == 0 ? slot0 : 0)) * chunk +
+// head in chunk: piece c came from CTA first + c nchunks (the CTAs of one head
+// chunk are every nchunks-th), and only the first piece can be a CTA's second.
 template <int D, int W>
 __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p, int direct) {
     pdl_trigger();
@@ -657,7 +657,10 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
         slot0 = d.z;
         // (a descriptor the decode never wrote -- it stopped on a timeout --
         // must not send the loads outside the partial slots)
-        if (first < 0 || nparts < 0 || first > p.tc_grid - nparts || (slot0 & ~1)) nparts = 0;
+        if (first < 0 || nparts < 0 ||
+            (long long)first + (long long)(nparts > 0 ? nparts - 1 : 0) * p.nchunks >= p.tc_grid ||
+            (slot0 & ~1))
+            nparts = 0;
         const long long gpairs = (long long)p.Hkv * p.nchunks;
         const int g = (int)(pair % gpairs);
         gh = (pair / gpairs) * p.H + (long long)(g / p.nchunks) * p.gsize +
@@ -666,7 +669,8 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
     combine_head<D, W>(
         p, gh, nparts,
         [&](int c) -> long long {
-            return ((long long)(first + c) * 2 + (c == 0 ? slot0 : 0)) * chunk + hh;
+            return ((long long)first + (long long)c * p.nchunks) * 2 * chunk +
+                   (long long)(c == 0 ? slot0 : 0) * chunk + hh;
         },
         hl, w);
 }

@@ -419,7 +419,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         const uint32_t full0 = bar0 + 8 * (is_v ? C::V_FULL : C::K_FULL);
         const uint32_t empty0 = bar0 + 8 * (is_v ? C::V_EMPTY : C::K_EMPTY);
         const uint32_t ring = sbase + (is_v ? C::OFF_V : 0);
-        const uint64_t policy = l2_policy_evict_first();
+        // (streamed once: evict first; a group served in chunks is streamed by
+        // the sibling CTAs side by side, all but the first from L2)
+        const uint64_t policy = p.nchunks > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
         const bool append = p.new_k != nullptr;
         const unsigned char* new_rows =
             static_cast<const unsigned char*>(is_v ? p.new_v : p.new_k);
@@ -713,7 +715,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 // first + pieces - 1 (the owners of its first and last unit);
                 // a pair that continues past this CTA is its cut pair (at most
                 // one: the range's last piece)
-                const int pieces = sched_pieces(it, w);
+                const int pieces = sched_pieces(p, it, w);
                 const long long pair = (long long)it.b * p.Hkv * p.nchunks + it.g;
                 p.tc_desc[pair] = make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
                 if (!it.whole)

@@ -135,6 +135,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return pol;
 }
 
+// L2 policy for data read a few times in quick succession (by sibling CTAs).
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 5-D tiled tensor-map (TMA) load global -> shared with L2 hint; completion is
 // signalled as transaction bytes on `bar`.  `tmap` is the generic address of a
 // __grid_constant__ CUtensorMap kernel parameter; c0 (the innermost

@@ -1,20 +1,25 @@
 // pa_schedule.cuh -- equal shares of a decode call's work for persistent CTAs.
 //
 // The unit of work is TU tokens (the tcgen05 kernel: one 128-token tile) of
-// one (sequence b, head group g) pair, g =
-// kv head * nchunks + head chunk; a context of n tokens has max(1, ceil(n /
-// TU)) units (an empty one still owes its zero output).  Every pair is charged
+// one (sequence b, KV head) pair; a context of n tokens has max(1, ceil(n /
+// TU)) units (an empty one still owes its zero output).  A group served as
+// nchunks head chunks splits the grid into nchunks groups of CTAs (CTA j serves
+// chunk j % nchunks): every group takes the same ranges below over the same
+// units, so sibling CTAs j, j + 1, ... stream the same K/V tiles side by side
+// and all but the first find them in L2.  Head group g = kv head * nchunks +
+// chunk.  Every pair is charged
 // OV more units for the fixed cost of starting and finishing a piece of it,
 // placed before its real units and doing no work.  Units are ordered by b, then
-// g, then position, and CTA j of the persistent grid takes the contiguous
-// range [ceil(j T / grid), ceil((j + 1) T / grid)) of the T units (grid <= T):
+// KV head, then position, and CTA j of a group of the persistent grid takes the
+// contiguous range [ceil(j T / grid), ceil((j + 1) T / grid)) of the T units
+// (grid: CTAs per group, <= T):
 // every CTA gets the same share of the work, whatever the mix of lengths.  A
 // range covers whole pairs, except that its first and last piece may be parts
 // of one that neighbouring CTAs share; those write unnormalised partials into
 // the CTA's two slots (first piece slot 0, last slot 1) and the combine kernel
 // merges them, told where by the descriptor the piece holding unit 0 writes
 // ({first CTA, pieces, slot of the first piece}: piece k came from CTA first +
-// k, and only the first piece can be a CTA's second).
+// k * nchunks, and only the first piece can be a CTA's second).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -59,7 +64,7 @@ __device__ __forceinline__ void sched_pair_units(const DecodeParams& p, int b0, 
 template <int B, int TU, int OV>
 __device__ __forceinline__ void sched_compute(const DecodeParams& p, unsigned char* sched,
                                               int lane) {
-    const long long Gq = (long long)p.Hkv * p.nchunks;
+    const long long Gq = p.Hkv;
     int cu[8];
     long long T = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 256) {
@@ -70,8 +75,8 @@ __device__ __forceinline__ void sched_compute(const DecodeParams& p, unsigned ch
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(kFullMask, T, off);
     T *= Gq;
-    const long long grid = min((long long)gridDim.x, T);
-    const long long j = blockIdx.x;
+    const long long grid = min((long long)(gridDim.x / p.nchunks), T);
+    const long long j = blockIdx.x / p.nchunks;
     long long lo = 0, cnt = 0;
     int b_sel = 0, g_sel = 0, o_sel = 0;
     if (j < grid) {
@@ -134,7 +139,7 @@ __device__ __forceinline__ void sched_compute(const DecodeParams& p, unsigned ch
 // length of the next sequence is loaded one sequence ahead (under a full HBM
 // stream a dependent global load costs microseconds).
 struct SWalk {
-    int b, g, o, n, c, n_next;  // o: offset within the pair, charged units first
+    int b, g, o, n, c, n_next;  // g: KV head; o: offset within the pair, charged units first
     bool bad, emitted;
     long long gpos, left;
     const long long* sched;  // T, grid, first unit (read where needed: registers are short)
@@ -177,9 +182,9 @@ __device__ __forceinline__ bool sched_walk_next(const DecodeParams& p, SWalk& w,
     const int u = w.o - OV;
     const int units = (int)min((long long)(w.c - u), w.left);
     it.b = w.b;
-    it.g = w.g;
-    it.kvh = w.g / p.nchunks;
-    it.hc = w.g % p.nchunks;
+    it.kvh = w.g;
+    it.hc = (int)(blockIdx.x % p.nchunks);
+    it.g = w.g * p.nchunks + it.hc;
     it.hbase = it.kvh * p.gsize + it.hc * G;
     it.n = w.n;
     it.c = w.c;
@@ -198,7 +203,7 @@ __device__ __forceinline__ bool sched_walk_next(const DecodeParams& p, SWalk& w,
     w.o += units;
     if (w.o == OV + w.c) {
         w.o = 0;
-        if (++w.g == p.Hkv * p.nchunks) {
+        if (++w.g == p.Hkv) {
             w.g = 0;
             ++w.b;
             if (w.left > 0) sched_walk_seq<B, TU>(p, w, w.n_next);
@@ -207,9 +212,13 @@ __device__ __forceinline__ bool sched_walk_next(const DecodeParams& p, SWalk& w,
     return true;
 }
 
-// Pieces of a pair cut at CTA ranges: CTA `first` .. the owner of its last unit.
-__device__ __forceinline__ int sched_pieces(const SPiece& it, const SWalk& w) {
-    return it.whole ? 1 : (int)((it.gpos + it.c - 1) * w.sched[1] / w.sched[0] - blockIdx.x + 1);
+// Pieces of a pair cut at CTA ranges: this CTA .. the owner of its last unit
+// (within the CTA's group).
+__device__ __forceinline__ int sched_pieces(const DecodeParams& p, const SPiece& it,
+                                            const SWalk& w) {
+    return it.whole ? 1
+                    : (int)((it.gpos + it.c - 1) * w.sched[1] / w.sched[0] -
+                            blockIdx.x / p.nchunks + 1);
 }
 
 }  // namespace pa

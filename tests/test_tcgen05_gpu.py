@@ -25,7 +25,7 @@ def _status_clear():
 
 
 @pytest.mark.parametrize("Hkv,H,Bs", [(1, 16, 16), (2, 32, 16), (1, 64, 32), (2, 128, 16),
-                                       (1, 48, 16), (1, 96, 32)])
+                                       (1, 48, 16), (1, 96, 32), (1, 128, 16), (1, 192, 32)])
 def test_groups_match_oracle_every_partition(cuda_device, Hkv, H, Bs):
     wl = W.custom("tc", "bf16", 2, H, Hkv, 128, Bs, LENS, seed=H + Bs, spare_blocks=3,
                   interleave=True)
