@@ -303,6 +303,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Waits for an mbarrier phase, suspending the thread (no issue slots used)
+// until the phase completes or about `ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool umma_wait(uint32_t bar, uint32_t parity, volatile int* abort_all,
                                           unsigned* status) {
@@ -574,10 +588,19 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             // S buffer is free: at most two tiles ahead of P V; the K stage is
             // released when S completes) and O^T += V^T [P_hi | P_lo] of tile
             // kt_pv (once its P is written and its V is in; the V stage is
-            // released when P V completes).  Polled without blocking on either.
+            // released when P V completes).  Tested without blocking on either;
+            // with nothing to issue the thread suspends on the barrier it
+            // expects next (it shares a scheduler with softmax warps, which
+            // need the issue slots a spinning loop would take).
+            // Descriptors: each buffer's base is encoded once; a K-step adds its
+            // byte offset / 16 to the start-address field (no carry: shared
+            // addresses stay below 256 KB).
             constexpr uint32_t IDQ = umma_idesc_bf16(128, G, 0, 0);
             constexpr uint32_t IDP = umma_idesc_bf16(128, C::PW, 1, 1);
-            const uint32_t pbuf = sbase + C::OFF_P;
+            const uint64_t dP0 = umma_desc_sw128(sbase + C::OFF_P, C::HALF, 1024);
+            const uint64_t dV0 = umma_desc_sw128(sbase + C::OFF_V, C::HALF, 1024);
+            const uint64_t dK0 = umma_desc_sw128(sbase, 0, 1024);
+            const uint64_t dQ0 = umma_desc_sw128(sbase + C::OFF_Q, 0, 1024);
             UWalk wq;
             umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, wq);
             int tiles_left = 0;       // tiles of the current piece still without S
@@ -594,11 +617,11 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     tc_fence_after();
                     const int vs = kt_pv % C::SV;
                     const bool first = (first_bits >> (kt_pv & 1)) & 1u;
-                    const uint32_t vt = sbase + C::OFF_V + vs * C::TILE;
+                    const uint64_t a0 = dV0 + (uint64_t)((vs * C::TILE) >> 4);
 #pragma unroll
                     for (int k = 0; k < C::TT / 16; ++k)
-                        umma_bf16(tmem + C::O_COL, umma_desc_sw128(vt + k * 2048, C::HALF, 1024),
-                                  umma_desc_sw128(pbuf + k * 2048, C::HALF, 1024), IDP,
+                        umma_bf16(tmem + C::O_COL, a0 + (uint64_t)(k * (2048 >> 4)),
+                                  dP0 + (uint64_t)(k * (2048 >> 4)), IDP,
                                   (k > 0 || !first) ? 1u : 0u);
                     umma_commit(bar0 + 8 * (C::PV_DONE + (kt_pv & 1)));
                     umma_commit(bar0 + 8 * (C::V_EMPTY + vs));
@@ -622,18 +645,18 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                         if (!q_ready)
                             q_ready = mbar_test(bar0 + 8 * (C::Q_FULL + (qi & 1)), (qi >> 1) & 1);
                         const int ks = kt_q % C::SK;
-                        const uint32_t qb = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
                         if (q_ready &&
                             mbar_test(bar0 + 8 * (C::K_FULL + ks), (kt_q / C::SK) & 1)) {
                             tc_fence_after();
-                            const uint32_t ktile = sbase + ks * C::TILE;
+                            const uint64_t a0 = dK0 + (uint64_t)((ks * C::TILE) >> 4);
+                            const uint64_t b0 = dQ0 + (uint64_t)(((qi & 1) * C::Q_BYTES) >> 4);
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
                                 const int h = k >> 2, kk = k & 3;
                                 umma_bf16(tmem + (kt_q & 1) * G,
-                                          umma_desc_sw128(ktile + h * C::HALF + kk * 32, 0, 1024),
-                                          umma_desc_sw128(qb + h * (G * 128) + kk * 32, 0, 1024),
-                                          IDQ, k > 0 ? 1u : 0u);
+                                          a0 + (uint64_t)((h * C::HALF + kk * 32) >> 4),
+                                          b0 + (uint64_t)((h * (G * 128) + kk * 32) >> 4), IDQ,
+                                          k > 0 ? 1u : 0u);
                             }
                             umma_commit(bar0 + 8 * (C::S_FULL + (kt_q & 1)));
                             umma_commit(bar0 + 8 * (C::K_EMPTY + ks));
@@ -652,6 +675,19 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     continue;
                 }
                 if (*abort_all) break;
+                // suspend on what gates the next step: the next S (its q, then
+                // its K) while it may run ahead, else the pending P V's P
+                if (!done_q && tiles_left > 0 && kt_q < kt_pv + 2) {
+                    if (!q_ready)
+                        (void)mbar_try_wait_for(bar0 + 8 * (C::Q_FULL + (qi & 1)), (qi >> 1) & 1,
+                                                200);
+                    else
+                        (void)mbar_try_wait_for(bar0 + 8 * (C::K_FULL + kt_q % C::SK),
+                                                (kt_q / C::SK) & 1, 200);
+                } else if (kt_pv < kt_q) {
+                    (void)mbar_try_wait_for(bar0 + 8 * (C::P_FULL + (kt_pv & 1)),
+                                            (kt_pv >> 1) & 1, 200);
+                }
                 const unsigned long long now = globaltimer_ns();
                 if (idle_since == 0) {
                     idle_since = now;
