@@ -2,7 +2,8 @@
 block size, GQA group 1-8, 16, 24, 32, 48, 64, KV heads, batch, ragged lengths with 0 / 1 /
 block multiples), random layer, partition size, pool layout and decode kernel (CUDA cores,
 mma.sync, tcgen05), plus the fused append path -- each case against the oracle on the same
-inputs."""
+inputs.  A second seeded set draws the large groups (96, 128, 192 query heads per KV head)
+that the tcgen05 kernel serves as sibling chunk CTAs."""
 import numpy as np
 import pytest
 import torch
@@ -15,6 +16,7 @@ from gpu_helpers import TOL, max_abs_err
 pytestmark = pytest.mark.gpu
 
 N_CASES = 112
+N_LARGE = 12
 
 
 def _case(i):
@@ -55,9 +57,33 @@ def _make_pool_handle(wl, fused, layout, dev):
     return (kc, vc), h
 
 
+def _large_case(i):
+    rng = np.random.default_rng(5000 + i)
+    Bs = int(rng.choice([16, 32]))
+    Hkv = int(rng.choice([1, 2]))
+    G = int(rng.choice([96, 128, 192]))
+    L = int(rng.integers(1, 3))
+    batch = int(rng.integers(1, 8))
+    special = [0, 1, Bs - 1, Bs, Bs + 1, 2 * Bs, 128, 129]
+    lens = [int(rng.choice(special)) if rng.random() < 0.4 else int(rng.integers(0, 40 * Bs))
+            for _ in range(batch)]
+    layout = str(rng.choice(["fused", "separate", "layer_major"]))
+    if layout == "separate":
+        L = 1
+    return rng, "bf16", 128, Bs, Hkv, G, L, lens, layout
+
+
 @pytest.mark.parametrize("i", range(N_CASES))
 def test_random_case_matches_oracle(cuda_device, i):
-    rng, dtype, D, Bs, Hkv, G, L, lens, layout = _case(i)
+    _run_case(cuda_device, i, *_case(i))
+
+
+@pytest.mark.parametrize("i", range(N_LARGE))
+def test_random_large_group_matches_oracle(cuda_device, i):
+    _run_case(cuda_device, 1000 + i, *_large_case(i))
+
+
+def _run_case(cuda_device, i, rng, dtype, D, Bs, Hkv, G, L, lens, layout):
     H = Hkv * G
     wl = W.custom(f"rnd{i}", dtype, L, H, Hkv, D, Bs, lens, seed=2000 + i,
                   spare_blocks=int(rng.integers(0, 5)), interleave=bool(rng.random() < 0.5),
