@@ -83,13 +83,13 @@ def decode_flops(wl) -> int:
 # DRAM bytes (read + write) of one layer's pa_write_kv_and_decode call on this
 # workload, one ncu capture per kernel on the 1-layer pool (--metrics
 # dram__bytes_read.sum,dram__bytes_write.sum, -k one kernel, -c 2):
-# pa_decode_mma_kernel with the fused append 2,231,241,984 read + 6,255,616
-# written, pa_combine_kernel 9,850,880 read + 0 written; see profiles/.  Valid
+# pa_decode_mma_kernel with the fused append 2,231,267,840 read + 5,906,688
+# written, pa_combine_kernel 9,848,064 read + 0 written; see profiles/.  Valid
 # only for the sources they were taken from (the kernels, the shared device
 # code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231241984 + 6255616 + 9850880,
-    "sources_sha256": "b383f4529ebb6323376e3d78b7933d45d9685f63ea849458b657c07f901d4013",
+    "bytes_per_launch": 2231267840 + 5906688 + 9848064,
+    "sources_sha256": "5d168ed655e82c7d440150595c5bbab4bea18ce7ce39c4949812850d58aad1c8",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h", "pa_api.cpp", "pa_fused_append.cuh"]
