@@ -460,6 +460,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                                lane)
                        : make_uint4(0, 0, 0, 0);
         };
+        // (this CTA's cut pair, if any, is recorded as its pieces are walked;
+        // none so far)
+        if (is_v && lane == 0 && p.tc_cut != nullptr) p.tc_cut[blockIdx.x] = make_int4(-1, 0, 0, 0);
         UWalk w;
         umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
         UItem it, nx;
@@ -475,6 +478,19 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             // (the piece at tile 0 of head group 0 reports for the sequence)
             const bool reporter = is_v && it.g == 0 && it.u == 0 && lane == 0;
             if (reporter && it.bad_len) atomicOr(p.status, kStatusBadLength);
+            if (is_v && it.u == 0 && lane == 0 && p.tc_desc != nullptr) {
+                // where the combine finds this pair's pieces: CTAs first ..
+                // first + pieces - 1 (the owners of its first and last unit); a
+                // pair that continues past this CTA is its cut pair (at most
+                // one: the range's last piece).  (Written here, a piece ahead of
+                // the softmax warps: the count takes a 64-bit division.)
+                const int pieces = sched_pieces(p, it, w);
+                const long long pair = (long long)it.b * p.Hkv * p.nchunks + it.g;
+                p.tc_desc[pair] = make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
+                if (!it.whole)
+                    p.tc_cut[blockIdx.x] =
+                        make_int4((int)pair, (int)blockIdx.x, pieces, it.first ? 0 : 1);
+            }
             // stores the appended row into block `blk` (every head chunk its
             // own identical copy), ordered before this warp's later copies
             auto store_row = [&](int blk) {
@@ -738,26 +754,11 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             return (pc.ntiles > 0 && tok < pc.t1) ? __ldg(p.bt + (long long)pc.b * p.maxb + tok / B)
                                                   : -1;
         };
-        // (this CTA's cut pair, if any, is recorded below; none so far)
-        if (warp == C::SM_WARP0 && lane == 0 && p.tc_cut != nullptr)
-            p.tc_cut[blockIdx.x] = make_int4(-1, 0, 0, 0);
         UItem it;
         bool have = umma_walk_next<B, G>(p, w, it);
         int blk0 = have ? first_block(it) : -1;
         while (!stop && have) {
             const long long head0 = (long long)it.b * p.H + it.hbase + h0;
-            if (it.u == 0 && warp == C::SM_WARP0 && lane == 0 && p.tc_desc != nullptr) {
-                // where the combine finds this pair's pieces: CTAs first ..
-                // first + pieces - 1 (the owners of its first and last unit);
-                // a pair that continues past this CTA is its cut pair (at most
-                // one: the range's last piece)
-                const int pieces = sched_pieces(p, it, w);
-                const long long pair = (long long)it.b * p.Hkv * p.nchunks + it.g;
-                p.tc_desc[pair] = make_int4((int)blockIdx.x, pieces, it.first ? 0 : 1, 0);
-                if (!it.whole)
-                    p.tc_cut[blockIdx.x] =
-                        make_int4((int)pair, (int)blockIdx.x, pieces, it.first ? 0 : 1);
-            }
             if (it.ntiles == 0) {  // empty context: output 0 (always a whole piece)
 #pragma unroll
                 for (int g = 0; g < HG; ++g) p.out[(head0 + g) * 128 + r] = 0.f;
