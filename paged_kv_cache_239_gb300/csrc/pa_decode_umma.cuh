@@ -745,6 +745,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         // at a named barrier the others have abandoned.
         bool failed = false;
         float lp[HG];  // this thread's share of the softmax denominators
+        auto swait = [&](uint32_t bar, uint32_t parity) {
+            return umma_wait(bar, parity, abort_all, p.status);
+        };
         UWalk w;
         umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
         // the block id of this thread's token in a piece's first tile, loaded
@@ -781,8 +784,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 const int stage = kt % C::SV;  // V stage
                 const int blk = blk_next;
                 blk_next = tok_block(i + 1);
-                const bool ok = umma_wait(bar0 + 8 * (C::S_FULL + (kt & 1)), (kt >> 1) & 1,
-                                          abort_all, p.status);
+                const bool ok = swait(bar0 + 8 * (C::S_FULL + (kt & 1)), (kt >> 1) & 1);
                 failed = failed || !ok;
                 __syncwarp();
                 tc_fence_after();
@@ -810,7 +812,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                         need |= x[g + e] > mv[e] + 8.f;
                     }
                 }
-                bool pv_waited = false;
+                bool rescale = false;
                 if (part_bar_or(part, need | failed)) {
                     // raise the running max to this tile's max (per head); the
                     // barrier that publishes the warps' maxima also decides
@@ -835,27 +837,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     part_bar(part);
 #pragma unroll
                     for (int g = 0; g < HG; ++g) lp[g] *= a_sh[h0 + g];
-                    if (i > 0) {
-                        // O (this piece's earlier tiles) scaled by the same factors
-                        if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)),
-                                       ((kt - 1) >> 1) & 1, abort_all, p.status))
-                            failed = true;
-                        pv_waited = true;
-                        __syncwarp();
-                        tc_fence_after();
-#pragma unroll
-                        for (int part = 0; part < 2; ++part) {   // hi heads, lo heads
-                            uint32_t v[HG];
-                            const uint32_t col = trow + C::O_COL + part * G + h0;
-                            tmem_ld_cols<HG>(col, v);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int j = 0; j < HG; ++j)
-                                v[j] = __float_as_uint(__uint_as_float(v[j]) * a_sh[h0 + j]);
-                            tmem_st_cols<HG>(col, v);
-                        }
-                        tmem_wait_st();
-                    }
+                    // O (this piece's earlier tiles) is scaled by the same
+                    // factors once P is written (the scores are dead there)
+                    rescale = i > 0;
                 }
                 // p = 2^(x - m) for this thread's token and heads (a head whose
                 // max is still -inf has only -inf scores here: p = 0)
@@ -871,16 +855,15 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                         x[g + e] = pv;
                     }
                 }
-                // the one P buffer is free once the previous tile's P V is done
-                if (!pv_waited && kt > 0 &&
-                    !umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1,
-                               abort_all, p.status))
+                // the one P buffer (and O) is free once the previous tile's P V
+                // is done
+                if (kt > 0 &&
+                    !swait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1))
                     failed = true;
                 // V of this tile must have landed before its invalid rows are
                 // zeroed (only the rows' own threads need it, but all wait so
                 // that the tile's stage is in place before P is published)
-                if (!umma_wait(bar0 + 8 * (C::V_FULL + stage), (kt / C::SV) & 1, abort_all,
-                               p.status))
+                if (!swait(bar0 + 8 * (C::V_FULL + stage), (kt / C::SV) & 1))
                     failed = true;
                 if (!valid && h0 == 0) {
                     // rows past the context (or of a bad block) hold stale or
@@ -913,6 +896,23 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                                               sw128(r, (nl & 63) >> 3)) =
                         make_uint4(lo[0], lo[1], lo[2], lo[3]);
                 }
+                if (rescale) {
+                    __syncwarp();
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 2 * HG; c += 8) {   // hi heads, then lo heads
+                        uint32_t v[8];
+                        const int hc = c % HG;
+                        const uint32_t col = trow + C::O_COL + (c / HG) * G + h0 + hc;
+                        tmem_ld_cols<8>(col, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) * a_sh[h0 + hc + j]);
+                        tmem_st_cols<8>(col, v);
+                    }
+                    tmem_wait_st();
+                }
                 // one arrival per warp, after all its lanes' writes
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -931,8 +931,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 const float v = warp_scatter_reduce<HG, false>(lp, lane);
                 if ((lane & (32 / HG - 1)) == 0) red[qd * G + h0 + lane / (32 / HG)] = v;
             }
-            if (!umma_wait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1,
-                           abort_all, p.status))
+            if (!swait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1))
                 failed = true;
             if (part_bar_or(part, failed)) {
                 stop = true;
