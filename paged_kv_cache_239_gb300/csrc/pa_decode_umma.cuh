@@ -45,6 +45,7 @@
 // wait for their copies and MMAs in flight, and TMEM is freed.
 #pragma once
 
+#include <cfloat>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -801,7 +802,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 // (the running maxima are read from shared memory where they
                 // are used: no thread of the part changes them before every
                 // thread has passed this tile's vote, and registers are short)
-                bool need = (i == 0);
+                float dmax = -INFINITY;  // largest score - running max (NaN-free)
 #pragma unroll
                 for (int g = 0; g < HG; g += 4) {
                     const float4 m4 = *reinterpret_cast<const float4*>(m_sh + h0 + g);
@@ -809,9 +810,10 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         x[g + e] = valid ? x[g + e] * p.qscale : -INFINITY;
-                        need |= x[g + e] > mv[e] + 8.f;
+                        dmax = fmaxf(dmax, x[g + e] - mv[e]);
                     }
                 }
+                const bool need = i == 0 || dmax > 8.f;
                 bool rescale = false;
                 if (part_bar_or(part, need | failed)) {
                     // raise the running max to this tile's max (per head); the
@@ -832,7 +834,10 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                         const float old = (i == 0) ? -INFINITY : m_sh[h];
                         const float mn = fmaxf(old, mt);
                         a_sh[h] = (old == -INFINITY) ? 0.f : exp2f(old - mn);
-                        m_sh[h] = mn;
+                        // (a head with no valid score yet keeps the finite
+                        // floor -FLT_MAX: its scores minus the max are then
+                        // -inf, and 2^-inf = 0, with no special case below)
+                        m_sh[h] = fmaxf(mn, -FLT_MAX);
                     }
                     part_bar(part);
 #pragma unroll
@@ -842,15 +847,14 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     rescale = i > 0;
                 }
                 // p = 2^(x - m) for this thread's token and heads (a head whose
-                // max is still -inf has only -inf scores here: p = 0)
+                // max is still the floor has only -inf scores here: p = 0)
 #pragma unroll
                 for (int g = 0; g < HG; g += 4) {
                     const float4 m4 = *reinterpret_cast<const float4*>(m_sh + h0 + g);
                     const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float mm = mv[e] == -INFINITY ? 0.f : mv[e];
-                        const float pv = ex2_approx(x[g + e] - mm);
+                        const float pv = ex2_approx(x[g + e] - mv[e]);
                         lp[g + e] += pv;
                         x[g + e] = pv;
                     }
@@ -962,7 +966,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                             ((long long)blockIdx.x * 2 + (it.first ? 0 : 1)) * G + h0 + g;
                         p.part_o[slot * 128 + r] = o;
                         if (r == 0) {
-                            p.part_ml[slot * 2 + 0] = m_sh[h0 + g];
+                            const float m = m_sh[h0 + g];
+                            p.part_ml[slot * 2 + 0] = m == -FLT_MAX ? -INFINITY : m;
                             p.part_ml[slot * 2 + 1] = L;
                         }
                     }
