@@ -789,18 +789,24 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 failed = failed || !ok;
                 __syncwarp();
                 tc_fence_after();
+                const int tok = it.t0 + i * C::TT + r;
+                const bool valid = tok < it.t1 && blk >= 0 && blk < p.num_blocks;
+                // this thread's scaled scores (-inf for a token past the
+                // context or in a bad block), read from the tile's S buffer
+                // (which stays in place until every warp has written P)
                 float x[HG];
-                {
+                auto load_scores = [&]() {
                     uint32_t v[HG];
                     tmem_ld_cols<HG>(trow + (kt & 1) * G + h0, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < HG; ++j) x[j] = __uint_as_float(v[j]);
-                }
-                const int tok = it.t0 + i * C::TT + r;
-                const bool valid = tok < it.t1 && blk >= 0 && blk < p.num_blocks;
-                // (the running maxima are read from shared memory where they
-                // are used: no thread of the part changes them before every
+                    for (int j = 0; j < HG; ++j)
+                        x[j] = valid ? __uint_as_float(v[j]) * p.qscale : -INFINITY;
+                };
+                load_scores();
+                // x becomes score - running max, the exponent of p unless the
+                // max is raised (the running maxima are read from shared
+                // memory: no thread of the part changes them before every
                 // thread has passed this tile's vote, and registers are short)
                 float dmax = -INFINITY;  // largest score - running max (NaN-free)
 #pragma unroll
@@ -809,8 +815,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        x[g + e] = valid ? x[g + e] * p.qscale : -INFINITY;
-                        dmax = fmaxf(dmax, x[g + e] - mv[e]);
+                        x[g + e] -= mv[e];
+                        dmax = fmaxf(dmax, x[g + e]);
                     }
                 }
                 const bool need = i == 0 || dmax > 8.f;
@@ -818,7 +824,9 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 if (part_bar_or(part, need | failed)) {
                     // raise the running max to this tile's max (per head); the
                     // barrier that publishes the warps' maxima also decides
-                    // whether the part stops
+                    // whether the part stops.  The scores are read again (x
+                    // holds them minus the old max, which may be the floor).
+                    load_scores();
                     {
                         const float v = warp_scatter_reduce<HG, true>(x, lane);
                         if ((lane & (32 / HG - 1)) == 0) red[qd * G + h0 + lane / (32 / HG)] = v;
@@ -842,22 +850,25 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     part_bar(part);
 #pragma unroll
                     for (int g = 0; g < HG; ++g) lp[g] *= a_sh[h0 + g];
+#pragma unroll
+                    for (int g = 0; g < HG; g += 4) {
+                        const float4 m4 = *reinterpret_cast<const float4*>(m_sh + h0 + g);
+                        x[g] -= m4.x;
+                        x[g + 1] -= m4.y;
+                        x[g + 2] -= m4.z;
+                        x[g + 3] -= m4.w;
+                    }
                     // O (this piece's earlier tiles) is scaled by the same
                     // factors once P is written (the scores are dead there)
                     rescale = i > 0;
                 }
-                // p = 2^(x - m) for this thread's token and heads (a head whose
-                // max is still the floor has only -inf scores here: p = 0)
+                // p = 2^(score - m) for this thread's token and heads (a head
+                // whose max is still the floor has only -inf scores: p = 0)
 #pragma unroll
-                for (int g = 0; g < HG; g += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4*>(m_sh + h0 + g);
-                    const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float pv = ex2_approx(x[g + e] - mv[e]);
-                        lp[g + e] += pv;
-                        x[g + e] = pv;
-                    }
+                for (int g = 0; g < HG; ++g) {
+                    const float pv = ex2_approx(x[g]);
+                    lp[g] += pv;
+                    x[g] = pv;
                 }
                 // the one P buffer (and O) is free once the previous tile's P V
                 // is done
