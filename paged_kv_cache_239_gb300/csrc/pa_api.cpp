@@ -75,10 +75,13 @@ int num_sms_current(int* out) {
 // that about 12 partitions fall on each SM: enough CTAs of similar size that
 // ragged lengths even out.  Bounds: at most 64 blocks and 1 MiB per CTA (more
 // only adds partials and idle tail), at least 32 KiB (less is all ramp-up).
-// The pick is rounded down to a multiple of 8 blocks (two per warp of a CTA).
-// GB300 sweeps: large-batch 64 blocks (fastest; picks 64), long-context 32
-// (fastest; the unrounded 35 was 2.5% slower; picks 32), MHA batch 64 12-16
-// (picks 16), mini-infer shape 4-8 (picks 8).
+// The pick is rounded up to a multiple of 8 blocks (two per warp of a CTA), so
+// that a context a little longer than the estimate does not leave a sliver of
+// a second partition.  GB300 sweeps (graph-timed calls): large-batch 64 blocks
+// (fastest; picks 64); long context 24-48 within 0.5 %, 40 fastest (picks
+// 40); MHA batch 64 at lengths up to 1024: 16 / 20 / 24 / 28 blocks 72.8 /
+// 71.3 / 71.1 / 75.2 us per call (picks 24; rounding down picked 16);
+// mini-infer shape 4-8 (picks 8).
 int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sms, int G) {
     const long long blk_bytes = 2LL * g.B * g.D * g.elt;
     const long long est_total = (long long)batch * g.Hkv * maxb * blk_bytes / 2;
@@ -92,7 +95,7 @@ int auto_partition_blocks(const pa::PoolGeom& g, int batch, int maxb, int num_sm
     if (G >= 16) pb = hi;
     if (pb > hi) pb = hi;
     if (pb < lo) pb = lo;
-    if (pb > 8) pb -= pb % 8;
+    if (pb > 8) pb = (pb + 7) / 8 * 8;
     if (pb > maxb) pb = maxb;
     if (pb < 1) pb = 1;
     return (int)pb;
