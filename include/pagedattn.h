@@ -315,6 +315,11 @@ PA_API int pa_write_kv(pa_pool* pool, int layer, const void* k, const void* v,
  *                 ceil(n / B) do not affect the result (a kernel may load
  *                 them with the rest of its row; pad with -1).
  *   context_lens  device int32 [batch], 0 <= n <= max_blocks_per_seq * B.
+ *   A table entry outside [0, num_blocks) among the first ceil(n / B) sets
+ *   PA_STATUS_BAD_BLOCK_ID and that block's tokens get no weight (no valid
+ *   token left: a zero vector); a length outside the range above sets
+ *   PA_STATUS_BAD_LENGTH and the sequence is decoded as n = 0.  Neither is an
+ *   error return: the kernels run before the lengths and tables are read.
  *   block_size, num_kv_heads, head_dim must equal the pool's; num_heads must be
  *   a multiple of num_kv_heads.
  *   workspace     device scratch of at least pa_decode_workspace_size() bytes,

@@ -345,6 +345,65 @@ def test_bad_length_is_flagged(cuda_device):
     assert torch.all(out[1] == 0)
 
 
+def _without_blocks(wl, tables, bad):
+    """The tables with the blocks listed in bad[b] (logical indices) removed
+    and the lengths shortened by their tokens: the attention the kernels give
+    when those blocks' ids are out of range (their tokens get no weight)."""
+    lens = wl.context_lens.copy()
+    out = np.full_like(tables, -1)
+    for b in range(wl.batch):
+        n = int(lens[b])
+        keep = [j for j in range(-(-n // wl.block_size)) if j not in bad.get(b, ())]
+        lost = sum(min(wl.block_size, n - j * wl.block_size) for j in bad.get(b, ()))
+        out[b, :len(keep)] = tables[b, keep]
+        lens[b] = n - lost
+    return out, lens
+
+
+@pytest.mark.parametrize("H,Hkv", [(32, 1), (32, 8)])
+def test_tokens_of_bad_blocks_get_no_weight(cuda_device, H, Hkv):
+    """A table entry outside [0, num_blocks) is flagged, and every kernel gives
+    its block's tokens no weight: the result is the attention over the other
+    tokens (the oracle on the same tables with those blocks removed), and a
+    sequence with no valid token left gives a zero vector.  The cases: the
+    whole first 128-token tile of a context, one block inside it, two whole
+    tiles and a ragged last block, and every block."""
+    lens = [600, 300, 1000, 130]
+    wl = W.custom("badw", "bf16", 1, H, Hkv, 128, 16, lens, seed=31, spare_blocks=4)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    try:
+        tables = wl.block_tables.copy()
+        bad = {0: tuple(range(8)), 1: (5,), 2: tuple(range(8, 24)) + (62,),
+               3: tuple(range(-(-130 // 16)))}
+        for b, js in bad.items():
+            for k, j in enumerate(js):
+                tables[b, j] = (-1 - k) if k % 2 else wl.num_blocks + 3 * k
+        ref_tables, ref_lens = _without_blocks(wl, wl.block_tables, bad)
+        assert ref_lens[3] == 0
+        ref = oracle_decode(wl, pool, q, 0, tables=ref_tables, lens=ref_lens)
+        bt = torch.from_numpy(tables).to(cuda_device)
+        ln = torch.from_numpy(wl.context_lens).to(cuda_device)
+        kinds = [B.PA_DECODE_AUTO, B.PA_DECODE_TENSOR_CORES]
+        if H // Hkv <= 8:  # (the CUDA-core kernel's groups)
+            kinds.append(B.PA_DECODE_CUDA_CORES)
+        if B.pa_decode_kernel_choice(gp.h, H) == B.PA_DECODE_TCGEN05:
+            kinds.append(B.PA_DECODE_TCGEN05)
+        torch.cuda.synchronize()
+        B.pa_get_status()
+        for kind in kinds:
+            B.pa_pool_set_decode_kernel(gp.h, kind)
+            for pb in (0, 1, 3, wl.max_blocks):
+                out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln, partition_blocks=pb).cpu()
+                assert B.pa_get_status() == B.PA_STATUS_BAD_BLOCK_ID, (kind, pb)
+                assert torch.isfinite(out).all(), (kind, pb)
+                assert max_abs_err(out, ref) <= TOL["bf16"], (kind, pb)
+                assert torch.all(out[3] == 0), (kind, pb)
+    finally:
+        gp.close()
+
+
 def test_decode_on_side_stream_matches(cuda_device):
     wl = W.custom("stream", "bf16", 2, 16, 4, 128, 32, [100, 250, 3, 64], seed=13)
     pool = W.make_pool(wl)
