@@ -93,15 +93,49 @@ cudaError_t launch_combine(const DecodeParams& p, int D, int B, cudaStream_t s) 
     return cudaErrorNotSupported;
 }
 
+// CTAs of pa_combine_tc_kernel<128, W> resident on the device at once (per
+// device, looked up once).
+template <int W>
+static cudaError_t combine_tc_wave(long long* wave) {
+    static std::mutex mu;
+    static long long cached[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cached[dev]) {
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_combine_tc_kernel<128, W>,
+                                                          256, 0);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        cached[dev] = (long long)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+    }
+    *wave = cached[dev];
+    return cudaSuccess;
+}
+
 template <int W>
 static cudaError_t launch_combine_tc_w(const DecodeParams& p, long long groups, int direct,
                                        cudaStream_t s) {
+    constexpr int HPC = 8 / W;
     const int chunk = p.gsize / p.nchunks;
-    const long long grid = groups * (chunk / (8 / W));
-    if (grid <= 0) return cudaSuccess;
+    if (groups <= 0 || chunk <= 0) return cudaSuccess;
+    // heads per warp: one, unless a CTA per 8 / W heads would take more than
+    // one wave of CTAs (the second wave starts only as the first one ends)
+    long long wave = 0;
+    cudaError_t e = combine_tc_wave<W>(&wave);
+    if (e != cudaSuccess) return e;
+    const int max_rounds = (chunk + HPC - 1) / HPC;
+    int rounds = 1;
+    while (rounds < max_rounds && groups * ((chunk + HPC * rounds - 1) / (HPC * rounds)) > wave)
+        ++rounds;
+    const long long grid = groups * ((chunk + HPC * rounds - 1) / (HPC * rounds));
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     return launch_pdl(pa_combine_tc_kernel<128, W>, dim3((unsigned)grid), dim3(256), 0, s, p,
-                      direct);
+                      direct, rounds);
 }
 
 cudaError_t launch_combine_tc(const DecodeParams& p, int D, bool direct, int pieces_hint,

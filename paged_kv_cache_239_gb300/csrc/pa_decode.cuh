@@ -619,16 +619,19 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, i
 }
 
 // Merges the pieces of the (sequence, head group) pairs the tcgen05 kernel
-// cut at its CTAs' range ends.  CTA group k (chunk / (8 / W) CTAs, one per 8 /
-// W heads of the chunk) serves pair k (direct: fewer pairs than decode CTAs,
-// so most are cut) or the pair tc_cut[k] whose first piece decode CTA k holds
-// (pair -1: none), which carries the pair's descriptor {first CTA, pieces,
-// slot of the first piece} itself (direct: the pair's descriptor).  Piece c
-// sits at slot ((first + c nchunks) * 2 + (c == 0 ? slot0 : 0)) * chunk +
-// head in chunk: piece c came from CTA first + c nchunks (the CTAs of one head
-// chunk are every nchunks-th), and only the first piece can be a CTA's second.
+// cut at its CTAs' range ends.  CTA group k (ceil(chunk / (rounds * 8 / W))
+// CTAs, each serving rounds * 8 / W heads of the chunk, 8 / W at a time) serves
+// pair k (direct: fewer pairs than decode CTAs, so most are cut) or the pair
+// tc_cut[k] whose first piece decode CTA k holds (pair -1: none), which carries
+// the pair's descriptor {first CTA, pieces, slot of the first piece} itself
+// (direct: the pair's descriptor).  Piece c sits at slot ((first + c nchunks) *
+// 2 + (c == 0 ? slot0 : 0)) * chunk + head in chunk: piece c came from CTA
+// first + c nchunks (the CTAs of one head chunk are every nchunks-th), and only
+// the first piece can be a CTA's second.  (rounds > 1 when one head per warp
+// would not fit the SMs in one wave of CTAs.)
 template <int D, int W>
-__global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p, int direct) {
+__global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p, int direct,
+                                                            int rounds) {
     pdl_trigger();
     pdl_wait();
     constexpr int HPC = 8 / W;
@@ -636,9 +639,10 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
     const int hl = warp / W;
     const int w = warp % W;
     const int chunk = p.gsize / p.nchunks;
-    const int cpp = chunk / HPC;  // CTAs per pair
+    const int per_cta = HPC * rounds;                  // heads of the chunk per CTA
+    const int cpp = (chunk + per_cta - 1) / per_cta;   // CTAs per pair
     const long long k = blockIdx.x / cpp;
-    const int hh = (int)(blockIdx.x % cpp) * HPC + hl;  // head within the chunk
+    const int h_first = (int)(blockIdx.x % cpp) * per_cta;
     const long long npairs = (long long)p.batch * p.Hkv * p.nchunks;
     long long pair = k;
     int4 d = make_int4(0, 0, 0, 0);
@@ -650,7 +654,7 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
         d = make_int4(rec.y, rec.z, rec.w, 0);
     }
     int nparts = 0, first = 0, slot0 = 0;
-    long long gh = 0;
+    long long gh0 = 0;  // the chunk's first head in the output
     if (pair >= 0 && pair < npairs) {
         first = d.x;
         nparts = d.y;
@@ -663,16 +667,62 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
             nparts = 0;
         const long long gpairs = (long long)p.Hkv * p.nchunks;
         const int g = (int)(pair % gpairs);
-        gh = (pair / gpairs) * p.H + (long long)(g / p.nchunks) * p.gsize +
-             (long long)(g % p.nchunks) * chunk + hh;
+        gh0 = (pair / gpairs) * p.H + (long long)(g / p.nchunks) * p.gsize +
+              (long long)(g % p.nchunks) * chunk;
     }
-    combine_head<D, W>(
-        p, gh, nparts,
-        [&](int c) -> long long {
-            return ((long long)first + (long long)c * p.nchunks) * 2 * chunk +
-                   (long long)(c == 0 ? slot0 : 0) * chunk + hh;
-        },
-        hl, w);
+    auto slot_of = [&](int hh, int c) -> long long {
+        return ((long long)first + (long long)c * p.nchunks) * 2 * chunk +
+               (long long)(c == 0 ? slot0 : 0) * chunk + hh;
+    };
+    if constexpr (W == 1 && D == 128) {
+        if (rounds <= 2 && nparts <= 2) {
+            // the common case (a pair cut once, one or two heads per warp):
+            // every load of the warp's heads first, then the merges, so the
+            // heads share one round trip (uniform per CTA: no barrier here)
+            const int lane = threadIdx.x & 31;
+            float mv[2][2], lv[2][2];
+            float4 ov[2][2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int hh = h_first + r * HPC + hl;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    mv[r][c] = -INFINITY;
+                    lv[r][c] = 0.f;
+                    ov[r][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (r < rounds && hh < chunk && nparts == 2) {
+                        const long long sl = slot_of(hh, c);
+                        mv[r][c] = __ldg(p.part_ml + 2 * sl);
+                        lv[r][c] = __ldg(p.part_ml + 2 * sl + 1);
+                        ov[r][c] = __ldg(reinterpret_cast<const float4*>(p.part_o + sl * D) + lane);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int hh = h_first + r * HPC + hl;
+                if (r < rounds && hh < chunk && nparts == 2) {
+                    const float M = fmaxf(mv[r][0], mv[r][1]);
+                    const float w0 = mv[r][0] == -INFINITY ? 0.f : exp2f(mv[r][0] - M);
+                    const float w1 = mv[r][1] == -INFINITY ? 0.f : exp2f(mv[r][1] - M);
+                    const float L = w0 * lv[r][0] + w1 * lv[r][1];
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    float4 o;
+                    o.x = (w0 * ov[r][0].x + w1 * ov[r][1].x) * inv;
+                    o.y = (w0 * ov[r][0].y + w1 * ov[r][1].y) * inv;
+                    o.z = (w0 * ov[r][0].z + w1 * ov[r][1].z) * inv;
+                    o.w = (w0 * ov[r][0].w + w1 * ov[r][1].w) * inv;
+                    reinterpret_cast<float4*>(p.out + (gh0 + hh) * D)[lane] = o;
+                }
+            }
+            return;
+        }
+    }
+    for (int r = 0; r < rounds; ++r) {  // (uniform: combine_head synchronises the CTA)
+        const int hh = h_first + r * HPC + hl;  // head within the chunk
+        combine_head<D, W>(
+            p, gh0 + hh, hh < chunk ? nparts : 0, [&](int c) { return slot_of(hh, c); }, hl, w);
+    }
 }
 
 }  // namespace pa
