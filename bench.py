@@ -932,8 +932,9 @@ def run_loop(args, local_rank: int, _result=None) -> None:
 def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev,
                     _result=None):
     """The same loop with the free stack on the device: each step is
-    pa_device_alloc_blocks + pa_write_kv_and_decode + a length increment, and a
-    whole run of `nsteps` steps is one CUDA graph replay (no host round trip)."""
+    pa_device_alloc_blocks_step (the allocation and the next lengths) +
+    pa_write_kv_and_decode, and a whole run of `nsteps` steps is one CUDA graph
+    replay (no host round trip)."""
     B.pa_pool_seed_free_stack(h, order)
     for _ in used:
         B.pa_alloc_block(h)
@@ -942,7 +943,8 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
     stack0 = stack.clone()
     bt0 = torch.from_numpy(wl.block_tables.copy()).to(dev)
     lens0 = torch.from_numpy(wl.context_lens.copy()).to(dev)
-    bt, lens, lens1 = bt0.clone(), lens0.clone(), lens0.clone()
+    bt = bt0.clone()
+    lens_ab = (lens0.clone(), lens0.clone())  # this step's positions / next lengths, in turn
     out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
     maxlen_blocks = wl.max_blocks
     pb = B.pa_decode_partition_blocks(h, wl.batch, wl.num_heads, maxlen_blocks)
@@ -955,19 +957,20 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
             for t in range(nsteps):
-                B.pa_device_alloc_blocks(h, stack, bt, wl.max_blocks, lens, wl.batch, stream=s)
-                torch.add(lens, 1, out=lens1)
-                B.pa_write_kv_and_decode(out, qs[t], h, 0, ks[t], vs[t], lens, bt, wl.max_blocks,
-                                         lens1, wl.batch, wl.block_size, wl.num_heads,
+                cur, nxt = lens_ab[t % 2], lens_ab[(t + 1) % 2]
+                # allocation and the next lengths (positions + 1) in one launch
+                B.pa_device_alloc_blocks_step(h, stack, bt, wl.max_blocks, cur, nxt, wl.batch,
+                                              stream=s)
+                B.pa_write_kv_and_decode(out, qs[t], h, 0, ks[t], vs[t], cur, bt, wl.max_blocks,
+                                         nxt, wl.batch, wl.block_size, wl.num_heads,
                                          wl.num_kv_heads, wl.head_dim, wl.scale, pb, ws, need,
                                          stream=s)
-                lens.copy_(lens1)
     torch.cuda.current_stream(dev).wait_stream(s)
 
     def reset():
         stack.copy_(stack0)
         bt.copy_(bt0)
-        lens.copy_(lens0)
+        lens_ab[0].copy_(lens0)
 
     for _ in range(max(1, args.warmup)):
         reset()
@@ -998,8 +1001,8 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
            "frac_of_nominal_hbm_peak": gbs / NOMINAL_HBM_GBS,
            "ms_per_step": ms / (runs * nsteps), "partition_blocks": pb,
            "decode_kernel": kernel_name(B, B.pa_decode_kernel_choice(h, wl.num_heads)),
-           "timing": "CUDA events around one graph replay per run (device allocation, fused "
-                     "append+decode, length update)", "clocks": clocks.summary()}
+           "timing": "CUDA events around one graph replay per run (device allocation with "
+                     "the length update, fused append+decode)", "clocks": clocks.summary()}
     B.pa_device_stack_download(h, stack)
     B.pa_pool_destroy(h)
     if _result is not None:

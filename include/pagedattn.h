@@ -262,6 +262,21 @@ PA_API int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tab
                                   pa_stream_t stream);
 
 /*
+ * pa_device_alloc_blocks, and in the same launch next_lens[b] = positions[b] + 1
+ * for every b: the context length once the token at positions[b] is appended,
+ * i.e. the context_lens of the step's pa_write_kv_and_decode and the positions
+ * of the next step.  A decode loop alternates two length arrays (this step's
+ * next_lens is the next step's positions) and needs no kernel of its own to
+ * advance them.  next_lens: device int32 [batch], 4-byte aligned, must not
+ * overlap positions (PA_ERR_INVALID_ARG).
+ * Cites: as pa_device_alloc_blocks; "kv-cache" skill, section 2 (each
+ * generated token grows its sequence's context by one).
+ */
+PA_API int pa_device_alloc_blocks_step(pa_pool* pool, void* dev_stack, int* block_tables,
+                                       int max_blocks_per_seq, const int* positions,
+                                       int* next_lens, int batch, pa_stream_t stream);
+
+/*
  * For every sequence b with finished[b] != 0, in increasing b, push the ids of
  * its ceil(context_lens[b] / block_size) blocks in table order (as repeated
  * pa_free_block calls) and set those table entries to -1.  Out-of-range ids are

@@ -91,6 +91,7 @@ _SIGNATURES = {
     "pa_device_stack_upload": ([_P, _P, _P], _I),
     "pa_device_stack_download": ([_P, _P, _P], _I),
     "pa_device_alloc_blocks": ([_P, _P, _P, _I, _P, _I, _P], _I),
+    "pa_device_alloc_blocks_step": ([_P, _P, _P, _I, _P, _P, _I, _P], _I),
     "pa_device_free_blocks": ([_P, _P, _P, _I, _P, _P, _I, _P], _I),
     "pa_decode_attention": ([_P, _P, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P], _I),
     "pa_decode_attention_partitioned": (
@@ -272,6 +273,14 @@ def pa_device_alloc_blocks(pool: int, dev_stack, block_tables, max_blocks_per_se
     _check(lib().pa_device_alloc_blocks(pool, _ptr(dev_stack), _ptr(block_tables),
                                         max_blocks_per_seq, _ptr(positions), batch,
                                         _stream(stream)), "pa_device_alloc_blocks")
+
+
+def pa_device_alloc_blocks_step(pool: int, dev_stack, block_tables, max_blocks_per_seq: int,
+                                positions, next_lens, batch: int, stream=None) -> None:
+    _check(lib().pa_device_alloc_blocks_step(pool, _ptr(dev_stack), _ptr(block_tables),
+                                             max_blocks_per_seq, _ptr(positions),
+                                             _ptr(next_lens), batch, _stream(stream)),
+           "pa_device_alloc_blocks_step")
 
 
 def pa_device_free_blocks(pool: int, dev_stack, block_tables, max_blocks_per_seq: int,

@@ -49,8 +49,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int& tot
 }
 
 __global__ void __launch_bounds__(kScanThreads)
-pa_device_alloc_kernel(int* stack, int* bt, int maxb, const int* positions, int batch, int B,
-                       unsigned* status) {
+pa_device_alloc_kernel(int* stack, int* bt, int maxb, const int* positions, int* next_lens,
+                       int batch, int B, unsigned* status) {
     pdl_trigger();
     pdl_wait();
     __shared__ int s_warp[32];
@@ -64,6 +64,7 @@ pa_device_alloc_kernel(int* stack, int* bt, int maxb, const int* positions, int 
         int need = 0, pos = 0;
         if (b < batch) {
             pos = positions[b];
+            if (next_lens != nullptr) next_lens[b] = pos + 1;
             if (pos < 0 || pos / B >= maxb) {
                 atomicOr(status, kStatusBadLength);
             } else if (pos % B == 0) {
@@ -141,11 +142,12 @@ pa_device_free_kernel(int* stack, int* bt, int maxb, const int* lens, const uint
 
 }  // namespace
 
-cudaError_t launch_device_alloc(int* stack, int* bt, int maxb, const int* positions, int batch,
-                                int B, unsigned* status, cudaStream_t s) {
+cudaError_t launch_device_alloc(int* stack, int* bt, int maxb, const int* positions,
+                                int* next_lens, int batch, int B, unsigned* status,
+                                cudaStream_t s) {
     if (batch <= 0) return cudaSuccess;
     return launch_pdl(pa_device_alloc_kernel, dim3(1), dim3(kScanThreads), 0, s, stack, bt, maxb,
-                      positions, batch, B, status);
+                      positions, next_lens, batch, B, status);
 }
 
 cudaError_t launch_device_free(int* stack, int* bt, int maxb, const int* lens,

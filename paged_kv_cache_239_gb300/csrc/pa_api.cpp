@@ -530,9 +530,9 @@ int pa_device_stack_download(pa_pool* pool, const void* dev_stack, pa_stream_t s
     return PA_OK;
 }
 
-int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
-                           int max_blocks_per_seq, const int* positions, int batch,
-                           pa_stream_t stream) {
+static int device_alloc(const char* who, pa_pool* pool, void* dev_stack, int* block_tables,
+                        int max_blocks_per_seq, const int* positions, int* next_lens, int batch,
+                        pa_stream_t stream) {
     if (int rc = check_pool(pool)) return rc;
     if (batch < 0 || max_blocks_per_seq <= 0)
         return fail(PA_ERR_INVALID_ARG, "batch (%d) / max_blocks_per_seq (%d) out of range", batch,
@@ -541,14 +541,38 @@ int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
     if (!dev_stack || !block_tables || !positions || !aligned(dev_stack, 4) ||
         !aligned(block_tables, 4) || !aligned(positions, 4))
         return fail(PA_ERR_INVALID_ARG, "dev_stack, block_tables, positions: non-NULL, 4-byte aligned");
+    if (next_lens) {
+        if (!aligned(next_lens, 4))
+            return fail(PA_ERR_INVALID_ARG, "next_lens: 4-byte aligned");
+        const char* a = reinterpret_cast<const char*>(positions);
+        const char* n = reinterpret_cast<const char*>(next_lens);
+        const size_t bytes = (size_t)batch * sizeof(int);
+        if (n < a + bytes && a < n + bytes)
+            return fail(PA_ERR_INVALID_ARG, "next_lens overlaps positions");
+    }
     unsigned* status = nullptr;
     cudaError_t e = pa::status_word(&status);
     if (e != cudaSuccess) return cuda_fail(e, "status word lookup");
     e = pa::launch_device_alloc(static_cast<int*>(dev_stack), block_tables, max_blocks_per_seq,
-                                positions, batch, pool->g.B, status,
+                                positions, next_lens, batch, pool->g.B, status,
                                 reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "pa_device_alloc_blocks launch");
+    if (e != cudaSuccess) return cuda_fail(e, who);
     return PA_OK;
+}
+
+int pa_device_alloc_blocks(pa_pool* pool, void* dev_stack, int* block_tables,
+                           int max_blocks_per_seq, const int* positions, int batch,
+                           pa_stream_t stream) {
+    return device_alloc("pa_device_alloc_blocks launch", pool, dev_stack, block_tables,
+                        max_blocks_per_seq, positions, nullptr, batch, stream);
+}
+
+int pa_device_alloc_blocks_step(pa_pool* pool, void* dev_stack, int* block_tables,
+                                int max_blocks_per_seq, const int* positions, int* next_lens,
+                                int batch, pa_stream_t stream) {
+    if (!next_lens) return fail(PA_ERR_INVALID_ARG, "next_lens is NULL");
+    return device_alloc("pa_device_alloc_blocks_step launch", pool, dev_stack, block_tables,
+                        max_blocks_per_seq, positions, next_lens, batch, stream);
 }
 
 int pa_device_free_blocks(pa_pool* pool, void* dev_stack, int* block_tables,

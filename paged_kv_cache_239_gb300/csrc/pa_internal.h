@@ -140,8 +140,9 @@ cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s);
 cudaError_t launch_write_kv(const WriteParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_kv(const GatherParams& p, int num_sms, cudaStream_t s);
 
-cudaError_t launch_device_alloc(int* stack, int* bt, int maxb, const int* positions, int batch,
-                                int B, unsigned* status, cudaStream_t s);
+cudaError_t launch_device_alloc(int* stack, int* bt, int maxb, const int* positions,
+                                int* next_lens, int batch, int B, unsigned* status,
+                                cudaStream_t s);
 cudaError_t launch_device_free(int* stack, int* bt, int maxb, const int* lens,
                                const uint8_t* finished, int batch, int B, long long num_blocks,
                                unsigned* status, cudaStream_t s);

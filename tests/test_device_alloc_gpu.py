@@ -109,10 +109,13 @@ def test_device_free_matches_host_frees(cuda_device):
         B.pa_pool_destroy(h)
 
 
-def test_device_loop_in_one_graph_matches_oracle(cuda_device):
+@pytest.mark.parametrize("advance", ["torch", "step_call"])
+def test_device_loop_in_one_graph_matches_oracle(cuda_device, advance):
     """Workload-5-shaped loop (MHA, block 32) with every step on the device:
     pa_device_alloc_blocks -> pa_write_kv_and_decode -> lengths += 1, the
-    whole run captured as one CUDA graph; against the host allocator + oracle."""
+    whole run captured as one CUDA graph; against the host allocator + oracle.
+    The lengths advance either by torch kernels or inside the allocation
+    launch (pa_device_alloc_blocks_step, two length arrays taking turns)."""
     import oracle
     from paged_kv_cache_239_gb300 import workloads as W
     from gpu_helpers import max_abs_err
@@ -153,12 +156,20 @@ def test_device_loop_in_one_graph_matches_oracle(cuda_device):
         with torch.cuda.stream(s):
             with torch.cuda.graph(g, stream=s):
                 for t in range(steps):
-                    B.pa_device_alloc_blocks(h, stack, bt, wl.max_blocks, lens, wl.batch, stream=s)
-                    torch.add(lens, 1, out=lens1)
-                    B.pa_write_kv_and_decode(outs[t], qd[t], h, 0, kd[t], vd[t], lens, bt,
-                                             wl.max_blocks, lens1, wl.batch, 32, 16, 16, 128,
+                    if advance == "torch":
+                        cur, nxt = lens, lens1
+                        B.pa_device_alloc_blocks(h, stack, bt, wl.max_blocks, cur, wl.batch,
+                                                 stream=s)
+                        torch.add(cur, 1, out=nxt)
+                    else:
+                        cur, nxt = (lens, lens1) if t % 2 == 0 else (lens1, lens)
+                        B.pa_device_alloc_blocks_step(h, stack, bt, wl.max_blocks, cur, nxt,
+                                                      wl.batch, stream=s)
+                    B.pa_write_kv_and_decode(outs[t], qd[t], h, 0, kd[t], vd[t], cur, bt,
+                                             wl.max_blocks, nxt, wl.batch, 32, 16, 16, 128,
                                              wl.scale, pb, ws, need, stream=s)
-                    lens.copy_(lens1)
+                    if advance == "torch":
+                        lens.copy_(lens1)
         torch.cuda.current_stream().wait_stream(s)
         g.replay()
         torch.cuda.synchronize()
@@ -177,8 +188,43 @@ def test_device_loop_in_one_graph_matches_oracle(cuda_device):
                                             wl.scale)
                 assert max_abs_err(outs[t], r) <= 2e-3, t
         assert np.array_equal(bt.cpu().numpy(), tables)
-        assert np.array_equal(lens.cpu().numpy(), ln)
+        final = lens if (advance == "torch" or steps % 2 == 0) else lens1
+        assert np.array_equal(final.cpu().numpy(), ln)
         assert np.array_equal(W.as_oracle_array(pool_d), host)
+        assert B.pa_get_status() == 0
+        assert _download_stack(h, stack) == [ref.allocate_block() for _ in range(ref.num_free())]
+    finally:
+        B.pa_pool_destroy(h)
+
+
+def test_alloc_step_writes_next_lengths_and_refuses_overlap(cuda_device):
+    """pa_device_alloc_blocks_step allocates exactly as pa_device_alloc_blocks
+    and writes positions + 1; next_lens overlapping positions is refused before
+    any launch."""
+    nb, Bs, maxb = 12, 16, 4
+    pool = torch.zeros((nb, 2, 1, 1, Bs, 64), dtype=torch.bfloat16, device=cuda_device)
+    h = B.pa_pool_create(pool, nb, 1, 1, Bs, 64, pool.dtype)
+    try:
+        order = [int(x) for x in np.random.default_rng(3).permutation(nb)]
+        B.pa_pool_seed_free_stack(h, order)
+        stack = torch.empty(nb + 1, dtype=torch.int32, device=cuda_device)
+        B.pa_device_stack_upload(h, stack)
+        bt = torch.full((5, maxb), -1, dtype=torch.int32, device=cuda_device)
+        pos = torch.tensor([0, 16, 5, 63, 32], dtype=torch.int32, device=cuda_device)
+        nxt = torch.full((5,), -7, dtype=torch.int32, device=cuda_device)
+        with pytest.raises(B.PagedAttnError) as e:
+            B.pa_device_alloc_blocks_step(h, stack, bt, maxb, pos, pos, 5)
+        assert e.value.code == B.PA_ERR_INVALID_ARG
+        B.pa_device_alloc_blocks_step(h, stack, bt, maxb, pos, nxt, 5)
+        torch.cuda.synchronize()
+        assert nxt.cpu().tolist() == [1, 17, 6, 64, 33]
+        ref = FreeBlockStack(nb)
+        ref.seed(order)
+        want = np.full((5, maxb), -1, dtype=np.int32)
+        for b, p_ in enumerate([0, 16, 5, 63, 32]):
+            if p_ % Bs == 0:
+                want[b, p_ // Bs] = ref.allocate_block()
+        assert np.array_equal(bt.cpu().numpy(), want)
         assert B.pa_get_status() == 0
         assert _download_stack(h, stack) == [ref.allocate_block() for _ in range(ref.num_free())]
     finally:
