@@ -70,6 +70,14 @@ class BlockPool:
         B.pa_device_alloc_blocks(self.handle, stack, block_tables, block_tables.shape[1],
                                  positions, positions.shape[0], stream)
 
+    def device_allocate_blocks_step(self, stack: torch.Tensor, block_tables: torch.Tensor,
+                                    positions: torch.Tensor, next_lens: torch.Tensor,
+                                    stream=None) -> None:
+        """device_allocate_blocks, and next_lens = positions + 1 in the same
+        launch (the context lengths once this step's tokens are appended)."""
+        B.pa_device_alloc_blocks_step(self.handle, stack, block_tables, block_tables.shape[1],
+                                      positions, next_lens, positions.shape[0], stream)
+
     def device_free_blocks(self, stack: torch.Tensor, block_tables: torch.Tensor,
                            context_lens: torch.Tensor, finished: torch.Tensor,
                            stream=None) -> None:
