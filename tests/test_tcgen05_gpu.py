@@ -127,6 +127,33 @@ def test_many_more_items_than_sms(cuda_device):
         gp.close()
 
 
+@pytest.mark.parametrize("batch,H", [(200, 64), (160, 128)])
+def test_combine_with_several_heads_per_warp(cuda_device, batch, H):
+    """More (sequence, head group) pairs than decode CTAs, 64-head chunks: the
+    combine then serves one record per decode CTA with 64 heads each, more
+    CTAs than fit the SMs at once with one head per warp, so each warp merges
+    two heads (and the pairs cut once take the loads-first path)."""
+    rng = np.random.default_rng(batch + H)
+    lens = [int(x) for x in rng.integers(0, 1200, size=batch)]
+    lens[:4] = [0, 1, 127, 129]
+    wl = W.custom("tcrounds", "bf16", 1, H, 1, 128, 16, lens, seed=batch * 7 + H,
+                  interleave=True)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    try:
+        assert B.pa_decode_kernel_choice(gp.h, H) == B.PA_DECODE_TCGEN05
+        bt, ln = device_tables(wl, cuda_device)
+        ref = oracle_decode(wl, pool, q, 0)
+        _status_clear()
+        out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln)
+        assert torch.isfinite(out).all()
+        assert max_abs_err(out, ref) <= TOL
+        assert B.pa_get_status() == 0
+    finally:
+        gp.close()
+
+
 def _poison_unused_rows(pool, wl):
     """NaN in every K/V row no sequence's context covers (free blocks and the
     rows past n in each last block)."""
