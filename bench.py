@@ -932,9 +932,9 @@ def run_loop(args, local_rank: int, _result=None) -> None:
 def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps, dev,
                     _result=None):
     """The same loop with the free stack on the device: each step is
-    pa_device_alloc_blocks_step (the allocation and the next lengths) +
-    pa_write_kv_and_decode, and a whole run of `nsteps` steps is one CUDA graph
-    replay (no host round trip)."""
+    pa_device_alloc_blocks_step (the allocation and the next lengths, run a
+    step ahead on a second stream) + pa_write_kv_and_decode, and a whole run of
+    `nsteps` steps is one CUDA graph replay (no host round trip)."""
     B.pa_pool_seed_free_stack(h, order)
     for _ in used:
         B.pa_alloc_block(h)
@@ -944,7 +944,9 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
     bt0 = torch.from_numpy(wl.block_tables.copy()).to(dev)
     lens0 = torch.from_numpy(wl.context_lens.copy()).to(dev)
     bt = bt0.clone()
-    lens_ab = (lens0.clone(), lens0.clone())  # this step's positions / next lengths, in turn
+    # three length arrays in turn: step t's positions, its lengths (= step t +
+    # 1's positions), and the one step t + 1's allocation writes meanwhile
+    bufs = (lens0.clone(), lens0.clone(), lens0.clone())
     out = torch.empty((wl.batch, wl.num_heads, wl.head_dim), dtype=torch.float32, device=dev)
     maxlen_blocks = wl.max_blocks
     pb = B.pa_decode_partition_blocks(h, wl.batch, wl.num_heads, maxlen_blocks)
@@ -953,24 +955,42 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
     B.pa_get_status()
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream(dev)
+    side = torch.cuda.Stream(dev)
     s.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
+            side.wait_stream(s)
+            ev_alloc = [torch.cuda.Event() for _ in range(nsteps)]
+            ev_dec = [torch.cuda.Event() for _ in range(nsteps)]
+
+            def alloc(t):
+                # step t's blocks and lengths (positions + 1) in one launch, on
+                # a second stream a step ahead of the decodes; it waits for the
+                # decode that last read the array it writes
+                with torch.cuda.stream(side):
+                    if t >= 2:
+                        side.wait_event(ev_dec[t - 2])
+                    B.pa_device_alloc_blocks_step(h, stack, bt, wl.max_blocks, bufs[t % 3],
+                                                  bufs[(t + 1) % 3], wl.batch, stream=side)
+                    ev_alloc[t].record(side)
+
+            alloc(0)
             for t in range(nsteps):
-                cur, nxt = lens_ab[t % 2], lens_ab[(t + 1) % 2]
-                # allocation and the next lengths (positions + 1) in one launch
-                B.pa_device_alloc_blocks_step(h, stack, bt, wl.max_blocks, cur, nxt, wl.batch,
-                                              stream=s)
-                B.pa_write_kv_and_decode(out, qs[t], h, 0, ks[t], vs[t], cur, bt, wl.max_blocks,
-                                         nxt, wl.batch, wl.block_size, wl.num_heads,
-                                         wl.num_kv_heads, wl.head_dim, wl.scale, pb, ws, need,
-                                         stream=s)
+                if t + 1 < nsteps:
+                    alloc(t + 1)
+                s.wait_event(ev_alloc[t])
+                B.pa_write_kv_and_decode(out, qs[t], h, 0, ks[t], vs[t], bufs[t % 3], bt,
+                                         wl.max_blocks, bufs[(t + 1) % 3], wl.batch,
+                                         wl.block_size, wl.num_heads, wl.num_kv_heads,
+                                         wl.head_dim, wl.scale, pb, ws, need, stream=s)
+                ev_dec[t].record(s)
+            s.wait_stream(side)
     torch.cuda.current_stream(dev).wait_stream(s)
 
     def reset():
         stack.copy_(stack0)
         bt.copy_(bt0)
-        lens_ab[0].copy_(lens0)
+        bufs[0].copy_(lens0)
 
     for _ in range(max(1, args.warmup)):
         reset()
@@ -1002,7 +1022,8 @@ def run_loop_device(args, B, torch, wl, pool, ks, vs, qs, h, used, order, nsteps
            "ms_per_step": ms / (runs * nsteps), "partition_blocks": pb,
            "decode_kernel": kernel_name(B, B.pa_decode_kernel_choice(h, wl.num_heads)),
            "timing": "CUDA events around one graph replay per run (device allocation with "
-                     "the length update, fused append+decode)", "clocks": clocks.summary()}
+                     "the length update a step ahead on a second stream, fused append+decode)",
+           "clocks": clocks.summary()}
     B.pa_device_stack_download(h, stack)
     B.pa_pool_destroy(h)
     if _result is not None:

@@ -16,6 +16,14 @@ def _pool(dev, nb, Bs=16):
     return t, B.pa_pool_create(t, nb, 1, 1, Bs, 64, t.dtype)
 
 
+class _null:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
 def _download_stack(h, stack):
     B.pa_device_stack_download(h, stack)
     order = []
@@ -109,13 +117,16 @@ def test_device_free_matches_host_frees(cuda_device):
         B.pa_pool_destroy(h)
 
 
-@pytest.mark.parametrize("advance", ["torch", "step_call"])
+@pytest.mark.parametrize("advance", ["torch", "step_call", "step_call_ahead"])
 def test_device_loop_in_one_graph_matches_oracle(cuda_device, advance):
     """Workload-5-shaped loop (MHA, block 32) with every step on the device:
     pa_device_alloc_blocks -> pa_write_kv_and_decode -> lengths += 1, the
     whole run captured as one CUDA graph; against the host allocator + oracle.
     The lengths advance either by torch kernels or inside the allocation
-    launch (pa_device_alloc_blocks_step, two length arrays taking turns)."""
+    launch (pa_device_alloc_blocks_step, two length arrays taking turns), or
+    that launch runs a step ahead on a second stream while the previous step
+    decodes (three length arrays; it waits for the decode that last read the
+    array it writes)."""
     import oracle
     from paged_kv_cache_239_gb300 import workloads as W
     from gpu_helpers import max_abs_err
@@ -153,9 +164,39 @@ def test_device_loop_in_one_graph_matches_oracle(cuda_device, advance):
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
+        lens2 = torch.empty_like(lens)
+        if advance == "step_call_ahead":
+            side = torch.cuda.Stream()
+            bufs = (lens, lens1, lens2)
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    side.wait_stream(s)
+                    ev_alloc = [torch.cuda.Event() for _ in range(steps)]
+                    ev_dec = [torch.cuda.Event() for _ in range(steps)]
+
+                    def alloc(t):
+                        with torch.cuda.stream(side):
+                            if t >= 2:
+                                side.wait_event(ev_dec[t - 2])
+                            B.pa_device_alloc_blocks_step(h, stack, bt, wl.max_blocks,
+                                                          bufs[t % 3], bufs[(t + 1) % 3],
+                                                          wl.batch, stream=side)
+                            ev_alloc[t].record(side)
+
+                    alloc(0)
+                    for t in range(steps):
+                        if t + 1 < steps:
+                            alloc(t + 1)
+                        s.wait_event(ev_alloc[t])
+                        B.pa_write_kv_and_decode(outs[t], qd[t], h, 0, kd[t], vd[t],
+                                                 bufs[t % 3], bt, wl.max_blocks,
+                                                 bufs[(t + 1) % 3], wl.batch, 32, 16, 16, 128,
+                                                 wl.scale, pb, ws, need, stream=s)
+                        ev_dec[t].record(s)
+                    s.wait_stream(side)
         with torch.cuda.stream(s):
-            with torch.cuda.graph(g, stream=s):
-                for t in range(steps):
+            with torch.cuda.graph(g, stream=s) if advance != "step_call_ahead" else _null():
+                for t in range(steps if advance != "step_call_ahead" else 0):
                     if advance == "torch":
                         cur, nxt = lens, lens1
                         B.pa_device_alloc_blocks(h, stack, bt, wl.max_blocks, cur, wl.batch,
@@ -188,7 +229,10 @@ def test_device_loop_in_one_graph_matches_oracle(cuda_device, advance):
                                             wl.scale)
                 assert max_abs_err(outs[t], r) <= 2e-3, t
         assert np.array_equal(bt.cpu().numpy(), tables)
-        final = lens if (advance == "torch" or steps % 2 == 0) else lens1
+        if advance == "step_call_ahead":
+            final = (lens, lens1, lens2)[steps % 3]
+        else:
+            final = lens if (advance == "torch" or steps % 2 == 0) else lens1
         assert np.array_equal(final.cpu().numpy(), ln)
         assert np.array_equal(W.as_oracle_array(pool_d), host)
         assert B.pa_get_status() == 0
