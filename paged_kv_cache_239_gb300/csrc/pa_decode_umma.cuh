@@ -1,5 +1,5 @@
 // pa_decode_umma.cuh -- paged decode attention for bf16 pools with large GQA
-// groups (16, 32 or 64 query heads per CTA) on the 5th-generation tensor cores:
+// groups (16, 32, 48 or 64 query heads per CTA) on the 5th-generation tensor cores:
 // tcgen05.mma with the accumulators in tensor memory (TMEM).
 //
 // Computes the same thing as the other decode kernels: for sequence b and query
@@ -216,12 +216,12 @@ struct UmmaCfg {
     // Separate K and V rings: a K stage is free once S = K Q^T has read it, a V
     // stage only after P V; so K runs ahead and the V ring covers the long
     // chain (copy, S, softmax, P V).
-    static constexpr int SK = G >= 64 ? 2 : 3;      // K stages
+    static constexpr int SK = G >= 48 ? 2 : 3;      // K stages
     static constexpr int SV = 3;                    // V stages
     // P of a tile: [64-column block][token][128 B] rows of hi heads | lo heads
-    // | zeros, in one buffer: the softmax of tile i + 1 overlaps P V of tile i
-    // and waits for it only before writing P.
-    static constexpr int PW = 2 * G < 64 ? 64 : 2 * G;
+    // | zeros up to a whole block, in one buffer: the softmax of tile i + 1
+    // overlaps P V of tile i and waits for it only before writing P.
+    static constexpr int PW = (2 * G + 63) / 64 * 64;
     static constexpr int P_BYTES = (PW / 64) * HALF;
     static constexpr int Q_BYTES = 2 * G * 128;     // q of one piece, two 64-column halves
                                                     // (two buffers: the next piece's q
@@ -239,10 +239,10 @@ struct UmmaCfg {
     static constexpr int CTRL_BYTES = SCHED_OFF + 48;
     static constexpr int TMEM_SLOT_OFF = 224, ABORT_OFF = 228;
     static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
-    // warps: 0 K producer (+ q), 1 MMA, 2 V producer, 3 .. 10 softmax (4 lane
-    // quarters x 2 head parts: more than one warp per scheduler, so the
-    // dependent latencies of the per-token work overlap)
-    static constexpr int NPART = G >= 64 ? 4 : 2;   // head parts
+    // warps: 0 K producer (+ q), 1 MMA, 2 V producer, 3 .. softmax (4 lane
+    // quarters x 2, 3 or 4 head parts: more than one warp per scheduler, so
+    // the dependent latencies of the per-token work overlap)
+    static constexpr int NPART = G == 48 ? 3 : (G >= 64 ? 4 : 2);   // head parts
     static constexpr int HG = G / NPART;            // heads per softmax warp
     static constexpr int SM_WARP0 = 3;
     static constexpr int NSW = 4 * NPART;           // softmax warps
@@ -258,7 +258,7 @@ struct UmmaCfg {
     // phases ahead of a waiter (parity waits would alias); every other
     // barrier's next phase needs the waiter's own progress.
 
-    static_assert(G == 16 || G == 32 || G == 64, "head chunk of 16, 32 or 64");
+    static_assert(G == 16 || G == 32 || G == 48 || G == 64, "head chunk of 16, 32, 48 or 64");
     static_assert(B == 16 || B == 32, "block size 16 or 32");
     static_assert(NBAR * 8 <= TMEM_SLOT_OFF, "barriers");
     static_assert(2 * G + PW <= TMEM_COLS, "TMEM columns");
@@ -734,10 +734,12 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
         unsigned char* pbuf = smem + C::OFF_P;
         if (C::PW > 2 * G && part == 0) {
-            // the P buffer's zero columns (heads past the group) are written once
+            // the P buffer's zero columns (past the hi and lo heads, up to a
+            // whole 64-column block) are written once
 #pragma unroll
-            for (int j = (2 * G) / 8; j < 8; ++j)
-                *reinterpret_cast<uint4*>(pbuf + sw128(r, j)) = make_uint4(0, 0, 0, 0);
+            for (int c8 = (2 * G) / 8; c8 < C::PW / 8; ++c8)
+                *reinterpret_cast<uint4*>(pbuf + (c8 / 8) * C::HALF + sw128(r, c8 % 8)) =
+                    make_uint4(0, 0, 0, 0);
         }
         int kt = 0;
         bool stop = false;
