@@ -762,7 +762,7 @@ def run_extra_workloads(args, B, torch, W, dev):
                             "K/V per layer below L2; consecutive layers read disjoint slices"))
     res.append(measure_step(B, torch, W, dev, W.named(4), "long_context_bf16",
                             "one layer: every call re-reads the same 1.35 GB (10x L2)"))
-    for H, Hkv in ((32, 2), (32, 1), (64, 1)):
+    for H, Hkv in ((32, 2), (32, 1), (48, 1), (64, 1), (128, 1)):
         wl = W.named(3)
         wl.num_heads, wl.num_kv_heads, wl.num_layers = H, Hkv, 16 if Hkv == 1 else 8
         res.append(measure_step(B, torch, W, dev, wl,
