@@ -127,12 +127,13 @@ def test_many_more_items_than_sms(cuda_device):
         gp.close()
 
 
-@pytest.mark.parametrize("batch,H", [(200, 64), (160, 128)])
+@pytest.mark.parametrize("batch,H", [(200, 64), (160, 128), (200, 96)])
 def test_combine_with_several_heads_per_warp(cuda_device, batch, H):
-    """More (sequence, head group) pairs than decode CTAs, 64-head chunks: the
-    combine then serves one record per decode CTA with 64 heads each, more
-    CTAs than fit the SMs at once with one head per warp, so each warp merges
-    two heads (and the pairs cut once take the loads-first path)."""
+    """More (sequence, head group) pairs than decode CTAs, 64- or 48-head
+    chunks: the combine then serves one record per decode CTA with 64 or 48
+    heads each, more CTAs than fit the SMs at once with one head per warp, so
+    each warp merges two heads (and the pairs cut once take the loads-first
+    path)."""
     rng = np.random.default_rng(batch + H)
     lens = [int(x) for x in rng.integers(0, 1200, size=batch)]
     lens[:4] = [0, 1, 127, 129]
