@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["pa_api.cpp", "pa_aux.cu", "pa_decode_bf16.cu", "pa_decode_f32.cu",
            "pa_decode_noalloc.cu", "pa_alloc.cu", "pa_decode_mma.cu",
-           "pa_decode_umma.cu"]
+           "pa_decode_mma_wide.cu", "pa_decode_umma.cu"]
 
 
 def _nvcc() -> str:

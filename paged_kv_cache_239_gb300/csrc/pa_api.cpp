@@ -147,6 +147,7 @@ struct DecodeShape {
     int tc_grid;  // tcgen05 kernel: persistent grid
     size_t ws_bytes;
     bool combine;  // a second kernel merges split contexts
+    bool wide;     // mma.sync kernel in wide CTAs, one per (sequence, KV head, chunk)
 };
 
 // The kernel the pool's choice selects for group G, or a PA_ERR_UNSUPPORTED
@@ -188,6 +189,15 @@ int pick_kernel(const pa_pool* pool, int G, Kernel* k) {
             *k = umma_ok ? Kernel::Tcgen05 : mma_ok ? Kernel::MmaSync : Kernel::CudaCores;
             return PA_OK;
     }
+}
+
+// Whether the mma.sync kernel's wide CTAs (one per sequence, KV head and head
+// chunk, holding the whole context) suit a call: see decode_mma_wide_fits.
+bool wide_fits(const pa_pool* pool, int G, int batch, int maxb, int sms) {
+    const int chunk = pa::decode_mma_chunk(G);
+    if (chunk == 0) return false;
+    return pa::decode_mma_wide_fits(pool->g.D, G, maxb, (long long)batch * pool->g.Hkv * (G / chunk),
+                                    sms);
 }
 
 int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb,
@@ -232,17 +242,21 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         out->combine = grid > 1;
         return PA_OK;
     }
+    const int chunk = kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G) : G;
+    const long long nchunks = G / chunk;
     int pb = partition_blocks;
+    bool wide = false;
     if (pb == 0) {
         int sms = 0;
         int rc = num_sms_current(&sms);
         if (rc != PA_OK) return rc;
-        pb = auto_partition_blocks(pool->g, batch, maxb, sms, G);
+        // Whole contexts in wide CTAs when those fit one wave and each warp
+        // streams only a few blocks: no partials and no combine launch.
+        wide = kernel == Kernel::MmaSync && wide_fits(pool, G, batch, maxb, sms);
+        pb = wide ? maxb : auto_partition_blocks(pool->g, batch, maxb, sms, G);
     }
     if (pb > maxb) pb = maxb;
     const int Cmax = (maxb + pb - 1) / pb;
-    const int chunk = kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G) : G;
-    const long long nchunks = G / chunk;
     if ((long long)batch * pool->g.Hkv * nchunks * Cmax > INT_MAX)
         return fail(PA_ERR_INVALID_ARG, "grid of %lld CTAs is too large",
                     (long long)batch * pool->g.Hkv * nchunks * Cmax);
@@ -254,6 +268,7 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
     out->tc_grid = 0;
     out->ws_bytes = workspace_bytes_for(batch, num_heads, Cmax, pool->g.D);
     out->combine = Cmax > 1;
+    out->wide = wide;
     return PA_OK;
 }
 
@@ -733,6 +748,12 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     p.gsize = sh.G;
     p.nchunks = sh.G / sh.chunk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (!sh.wide && sh.kernel == Kernel::MmaSync && sh.Cmax == 1) {
+        // an explicit partition that covers the table: wide CTAs where they fit
+        int sms = 0;
+        if (int rc = num_sms_current(&sms)) return rc;
+        sh.wide = wide_fits(pool, sh.G, batch, max_blocks_per_seq, sms);
+    }
     if (sh.kernel != Kernel::CudaCores) {
         {
             std::lock_guard<std::mutex> lock(pool->mu);
@@ -747,7 +768,8 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
         p.tma_slot_layer = pool->tma_slots[1];
         p.tma_slot_head = pool->tma_slots[2];
         e = sh.kernel == Kernel::Tcgen05 ? pa::launch_decode_umma(p, pool->tmaps, g.B, sh.G, s)
-                                         : pa::launch_decode_mma(p, pool->tmaps, g.D, g.B, sh.G, s);
+            : sh.wide ? pa::launch_decode_mma_wide(p, pool->tmaps, g.D, g.B, sh.G, s)
+                      : pa::launch_decode_mma(p, pool->tmaps, g.D, g.B, sh.G, s);
     } else {
         e = g.dtype == 1 ? pa::launch_decode_bf16(p, g.D, g.B, sh.G, s)
                          : pa::launch_decode_f32(p, g.D, g.B, sh.G, s);

@@ -20,48 +20,6 @@ constexpr int kMmaWarps = 4;
 template <int D>
 constexpr int kMmaStages = D == 64 ? 4 : 2;
 
-template <int D, int B, int G>
-cudaError_t launch_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream_t stream) {
-    using Cfg = MmaCfg<D, B, G, kMmaWarps, kMmaStages<D>>;
-    auto kern = pa_decode_mma_kernel<D, B, G, kMmaWarps, kMmaStages<D>>;
-    static std::mutex mu;
-    static unsigned long long done_mask = 0;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        const unsigned long long bit = 1ull << (dev & 63);
-        if (!(done_mask & bit)) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     Cfg::SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-            done_mask |= bit;
-        }
-    }
-    const long long grid = (long long)p.batch * p.Hkv * p.nchunks * p.Cmax;
-    if (grid <= 0) return cudaSuccess;
-    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    return launch_pdl(kern, dim3((unsigned)grid), dim3(kMmaWarps * 32), Cfg::SMEM_BYTES, stream, p,
-                      tm[0], tm[1]);
-}
-
-template <int D, int B>
-cudaError_t launch_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaStream_t s) {
-    switch (G) {
-        case 1: return launch_inst<D, B, 1>(p, tm, s);
-        case 2: return launch_inst<D, B, 2>(p, tm, s);
-        case 3: return launch_inst<D, B, 3>(p, tm, s);
-        case 4: return launch_inst<D, B, 4>(p, tm, s);
-        case 5: return launch_inst<D, B, 5>(p, tm, s);
-        case 6: return launch_inst<D, B, 6>(p, tm, s);
-        case 7: return launch_inst<D, B, 7>(p, tm, s);
-        case 8: return launch_inst<D, B, 8>(p, tm, s);
-        case 16: return launch_inst<D, B, 16>(p, tm, s);
-        default: return cudaErrorNotSupported;
-    }
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -102,11 +60,11 @@ cudaError_t launch_decode_mma(const DecodeParams& p_in, const void* tmaps, int D
     p.gsize = Gtot;
     p.nchunks = Gtot / G;
     if (D == 64) {
-        if (B == 16) return launch_g<64, 16>(p, tm, G, s);
-        if (B == 32) return launch_g<64, 32>(p, tm, G, s);
+        if (B == 16) return launch_mma_g<64, 16, kMmaWarps, kMmaStages<64>>(p, tm, G, s);
+        if (B == 32) return launch_mma_g<64, 32, kMmaWarps, kMmaStages<64>>(p, tm, G, s);
     } else if (D == 128) {
-        if (B == 16) return launch_g<128, 16>(p, tm, G, s);
-        if (B == 32) return launch_g<128, 32>(p, tm, G, s);
+        if (B == 16) return launch_mma_g<128, 16, kMmaWarps, kMmaStages<128>>(p, tm, G, s);
+        if (B == 32) return launch_mma_g<128, 32, kMmaWarps, kMmaStages<128>>(p, tm, G, s);
     }
     return cudaErrorNotSupported;
 }

@@ -28,6 +28,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "pa_device.cuh"
 #include "pa_fused_append.cuh"
 #include "pa_internal.h"
@@ -449,6 +451,52 @@ __global__ void __launch_bounds__(NW * 32)
                 p.part_ml[slot * 2 + 1] = Lsum;
             }
         }
+    }
+}
+
+// Host: sets the kernel's shared-memory limit once per device, then launches
+// one CTA per (sequence, KV head, head chunk, partition) with programmatic
+// serialisation.
+template <int D, int B, int G, int NW, int S>
+cudaError_t launch_mma_inst(const DecodeParams& p, const CUtensorMap* tm, cudaStream_t stream) {
+    using Cfg = MmaCfg<D, B, G, NW, S>;
+    auto kern = pa_decode_mma_kernel<D, B, G, NW, S>;
+    static std::mutex mu;
+    static unsigned long long done_mask = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const unsigned long long bit = 1ull << (dev & 63);
+        if (!(done_mask & bit)) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            done_mask |= bit;
+        }
+    }
+    const long long grid = (long long)p.batch * p.Hkv * p.nchunks * p.Cmax;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(NW * 32), Cfg::SMEM_BYTES, stream, p,
+                      tm[0], tm[1]);
+}
+
+// The instantiation for head chunk G (the chunk sizes decode_mma_chunk gives).
+template <int D, int B, int NW, int S>
+cudaError_t launch_mma_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_mma_inst<D, B, 1, NW, S>(p, tm, s);
+        case 2: return launch_mma_inst<D, B, 2, NW, S>(p, tm, s);
+        case 3: return launch_mma_inst<D, B, 3, NW, S>(p, tm, s);
+        case 4: return launch_mma_inst<D, B, 4, NW, S>(p, tm, s);
+        case 5: return launch_mma_inst<D, B, 5, NW, S>(p, tm, s);
+        case 6: return launch_mma_inst<D, B, 6, NW, S>(p, tm, s);
+        case 7: return launch_mma_inst<D, B, 7, NW, S>(p, tm, s);
+        case 8: return launch_mma_inst<D, B, 8, NW, S>(p, tm, s);
+        case 16: return launch_mma_inst<D, B, 16, NW, S>(p, tm, s);
+        default: return cudaErrorNotSupported;
     }
 }
 

@@ -115,6 +115,13 @@ bool decode_mma_supported(int D, int B, int G);
 int decode_mma_chunk(int G);
 cudaError_t launch_decode_mma(const DecodeParams& p, const void* tmaps, int D, int B, int G,
                               cudaStream_t s);
+// The same kernel in wide CTAs (many warps, one partition per context: p.Cmax
+// must be 1).  decode_mma_wide_fits: whether a call with group G and `ctas`
+// (sequence, KV head, chunk) CTAs over tables of maxb blocks suits it (a third
+// to all of one wave, a few blocks per warp).
+bool decode_mma_wide_fits(int D, int G, int maxb, long long ctas, int num_sms);
+cudaError_t launch_decode_mma_wide(const DecodeParams& p, const void* tmaps, int D, int B, int G,
+                                   cudaStream_t s);
 // Encodes the K and V tensor maps of a bf16 pool (5-D, box 64 x 16, 128-byte
 // swizzle) into tmaps[0..1]; slots receives the outer-dimension order.
 cudaError_t encode_pool_tmaps(const PoolGeom& g, void* tmaps, int* slot_blk, int* slot_layer,

@@ -86,7 +86,7 @@ def test_noalloc_sequence_of_differently_cut_calls(cuda_device):
     larger leftovers."""
     steps = [  # (H, Hkv, lens, partition_blocks)
         (32, 8, [30000, 26000, 5000, 1], 1),        # mma.sync, one block per partition
-        (32, 8, [700, 1, 0, 300, 129], 0),           # mma.sync, heuristic partitions
+        (32, 8, [3000, 1, 0, 300, 129], 0),          # mma.sync, heuristic partitions
         (64, 1, [4000, 9000, 1, 700, 0, 2048], 0),   # tcgen05, cut at CTA shares
         (32, 8, [4000, 2, 1500], 2),                 # mma.sync again, after tcgen05
     ]
