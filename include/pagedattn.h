@@ -397,7 +397,13 @@ PA_API int pa_write_kv_and_decode(float* out, const void* q, pa_pool* pool, int 
                                   pa_stream_t stream);
 
 /* The partition size (in blocks) that pa_decode_attention picks for these
- * sizes on the current device.  Queries the device's SM count.
+ * sizes on the current device.  Queries the device's SM count.  On the
+ * mma.sync kernel it is the whole table (max_blocks_per_seq: no workspace, no
+ * combine) when the call's (sequence, KV head, head chunk) CTAs number between
+ * a third of the SMs and all of them and the table holds at most 64 blocks
+ * (head_dim 64) or 48 (head_dim 128): each context then runs in one wide CTA
+ * of 16 (8) warps.  A partition covering the table that is passed explicitly
+ * runs the same way under the same conditions.
  * Cites: no counterpart on the pages (see pa_decode_attention_partitioned). */
 PA_API int pa_decode_partition_blocks(const pa_pool* pool, int batch, int num_heads,
                                int max_blocks_per_seq, int* partition_blocks);
