@@ -103,6 +103,11 @@ __global__ void __launch_bounds__(NW * 32)
     const int* bt_row = p.bt + (long long)b * p.maxb;
     const int k_first = c * p.PB + warp + lane * NW;
     const int id_first = k_first < p.maxb ? __ldg(bt_row + k_first) : -1;
+    // The fused append's position and new rows do not depend on the length
+    // either: all four loads are in flight together.
+    const bool fused = p.new_k != nullptr;
+    const int pos = fused ? __ldg(p.positions + b) : 0;
+    const uint4 new_row = fused ? load_new_row<D * 2>(p, b, kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
 
     int n = __ldg(p.lens + b);
     if (n < 0 || n > p.maxb * B) {
@@ -151,26 +156,35 @@ __global__ void __launch_bounds__(NW * 32)
     // of that partition stores the (identical) row itself.  The store is made
     // by the warp that copies that block, just before the copy, so its latency
     // hides behind the warp's earlier blocks and no other warp waits.
-    int app_k = -1, app_blk = -1, app_pos = 0;
-    if (p.new_k != nullptr) {
-        const int pos = __ldg(p.positions + b);
+    int app_k = -1, app_blk = -1;
+    if (fused) {
         if (pos < 0 || pos / B >= p.maxb) {
             if (c == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0)
                 atomicOr(p.status, kStatusBadLength);
         } else if (c == (pos < n ? (pos / B) / p.PB : 0)) {
             const int jb = pos / B;
-            const int blk = __ldg(bt_row + jb);
-            if (blk < 0 || blk >= p.num_blocks) {
-                if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
-            } else if (pos < n) {
+            if (pos < n) {
                 if (warp == (jb - pb0) % NW) {
-                    app_k = (jb - pb0) / NW;
-                    app_blk = blk;
-                    app_pos = pos;
+                    // the block is this warp's k-th: among its prefetched ids
+                    // when k < 32
+                    const int k = (jb - pb0) / NW;
+                    int blk = __shfl_sync(kFullMask, id_first, k & 31);
+                    if (k >= 32) blk = __ldg(bt_row + jb);
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        if (lane == 0) atomicOr(p.status, kStatusBadBlock);
+                    } else {
+                        app_k = k;
+                        app_blk = blk;
+                    }
                 }
             } else if (warp == 0) {
                 // past the decoded context: no copy of this call needs the row
-                warp_store_new_row<D * 2, 2>(p, b, kvh, blk, pos, B, lane);
+                const int blk = __ldg(bt_row + jb);
+                if (blk < 0 || blk >= p.num_blocks) {
+                    if (lane == 0) atomicOr(p.status, kStatusBadBlock);
+                } else {
+                    store_new_row<D * 2, 2>(p, kvh, blk, pos, B, lane, new_row);
+                }
             }
         }
     }
@@ -192,7 +206,7 @@ __global__ void __launch_bounds__(NW * 32)
         const int row0 = sub * C::R;
         const int rows = min(C::R, n - (jb * B + row0));
         const int stage = u % S;
-        if (k == app_k && sub == 0) warp_store_new_row<D * 2, 2>(p, b, kvh, app_blk, app_pos, B, lane);
+        if (k == app_k && sub == 0) store_new_row<D * 2, 2>(p, kvh, app_blk, pos, B, lane, new_row);
         if (lane == 0) {
             const uint32_t bar = bars + 8 * stage;
             if (blk >= 0 && blk < p.num_blocks) {
