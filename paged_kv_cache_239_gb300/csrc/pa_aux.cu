@@ -170,12 +170,12 @@ __global__ void __launch_bounds__(256) pa_write_kv_kernel(const WriteParams p) {
         r /= p.Hkv;
         const int kv = (int)(r % 2);
         const int b = (int)(r / 2);
-        const int pos = __ldg(p.positions + b);
+        const int pos = ld_dep(p.positions + b);
         if (pos < 0 || pos / p.B >= p.maxb) {
             if (ci == 0 && kvh == 0 && kv == 0) atomicOr(p.status, kStatusBadLength);
             continue;
         }
-        const int blk = __ldg(p.bt + (long long)b * p.maxb + pos / p.B);
+        const int blk = ld_dep(p.bt + (long long)b * p.maxb + pos / p.B);
         if (blk < 0 || blk >= p.num_blocks) {
             if (ci == 0 && kvh == 0 && kv == 0) atomicOr(p.status, kStatusBadBlock);
             continue;
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(256) pa_write_kv_kernel(const WriteParams p) {
                                    ((long long)b * p.Hkv + kvh) * p.row_bytes + ci * 16;
         unsigned char* dst = static_cast<unsigned char*>(kv ? p.v_base : p.k_base) +
                              off * p.elt + ci * 16;
-        *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
+        *reinterpret_cast<uint4*>(dst) = ld_dep(reinterpret_cast<const uint4*>(src));
     }
 }
 
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(256) pa_gather_kv_kernel(const GatherParams p)
         r /= p.Hkv;
         const int t = (int)(r % p.max_len);
         const int b = (int)(r / p.max_len);
-        int n = __ldg(p.lens + b);
+        int n = ld_dep(p.lens + b);
         if (n < 0 || n > p.max_len || n > p.maxb * p.B) {
             if (t == 0 && kvh == 0 && kv == 0 && ci == 0) atomicOr(p.status, kStatusBadLength);
             n = 0;
@@ -228,14 +228,14 @@ __global__ void __launch_bounds__(256) pa_gather_kv_kernel(const GatherParams p)
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         bool valid = t < n;
         if (valid) {
-            const int blk = __ldg(p.bt + (long long)b * p.maxb + t / p.B);
+            const int blk = ld_dep(p.bt + (long long)b * p.maxb + t / p.B);
             if (blk < 0 || blk >= p.num_blocks) {
                 if (kvh == 0 && kv == 0 && ci == 0) atomicOr(p.status, kStatusBadBlock);
             } else {
                 const long long off = (long long)blk * p.s_blk + p.tile_off +
                                       (long long)kvh * p.s_head +
                                       (long long)(t % p.B) * (p.row_bytes / p.elt);
-                val = __ldg(reinterpret_cast<const uint4*>(
+                val = ld_dep(reinterpret_cast<const uint4*>(
                     static_cast<const unsigned char*>(kv ? p.v_base : p.k_base) + off * p.elt +
                     ci * 16));
             }
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(256) pa_gather_kv_tiled(const GatherParams p) 
     const int b = blockIdx.y;
     const int t0 = j * p.B;
     const int rows_here = min(p.B, p.max_len - t0);
-    int n = __ldg(p.lens + b);
+    int n = ld_dep(p.lens + b);
     if (n < 0 || n > p.max_len || n > p.maxb * p.B) {
         if (j == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
         n = 0;
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(256) pa_gather_kv_tiled(const GatherParams p) 
     int valid = min(max(n - t0, 0), rows_here);
     int blk = -1;
     if (valid > 0) {
-        blk = __ldg(p.bt + (long long)b * p.maxb + j);
+        blk = ld_dep(p.bt + (long long)b * p.maxb + j);
         if (blk < 0 || blk >= p.num_blocks) {
             if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
             valid = 0;
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(256) pa_gather_kv_tiled(const GatherParams p) 
                 for (int u = 0; u < 4; ++u) {
                     v[u] = make_uint4(0u, 0u, 0u, 0u);
                     if (live && h0 + u < p.Hkv)
-                        v[u] = __ldg(reinterpret_cast<const uint4*>(sbase + (h0 + u) * head_bytes));
+                        v[u] = ld_dep(reinterpret_cast<const uint4*>(sbase + (h0 + u) * head_bytes));
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u)

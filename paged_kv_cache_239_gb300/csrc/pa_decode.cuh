@@ -176,9 +176,9 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     // overlaps the length's instead of waiting for it.
     const int* bt_row = p.bt + (long long)b * p.maxb;
     const int k_first = c * p.PB + warp + lane * NW;
-    const int id_first = k_first < p.maxb ? __ldg(bt_row + k_first) : -1;
+    const int id_first = k_first < p.maxb ? ld_dep(bt_row + k_first) : -1;
 
-    int n = __ldg(p.lens + b);
+    int n = ld_dep(p.lens + b);
     if (n < 0 || n > p.maxb * B) {
         if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
         n = 0;
@@ -224,12 +224,12 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     //      the store, just before the copy (see pa_decode_mma_kernel). ----
     int app_k = -1, app_blk = -1, app_pos = 0;
     if (p.new_k != nullptr) {
-        const int pos = __ldg(p.positions + b);
+        const int pos = ld_dep(p.positions + b);
         if (pos < 0 || pos / B >= p.maxb) {
             if (c == 0 && kvh == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
         } else if (c == (pos < n ? (pos / B) / p.PB : 0)) {
             const int jb = pos / B;
-            const int blk = __ldg(bt_row + jb);
+            const int blk = ld_dep(bt_row + jb);
             if (blk < 0 || blk >= p.num_blocks) {
                 if (threadIdx.x == 0) atomicOr(p.status, kStatusBadBlock);
             } else if (pos < n) {
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
         if (k >= kbase + 32) {
             kbase += 32;
             const int kk = kbase + lane;
-            myid = (kk < nk) ? __ldg(bt_row + pb0 + warp + kk * NW) : -1;
+            myid = (kk < nk) ? ld_dep(bt_row + pb0 + warp + kk * NW) : -1;
         }
         const int blk = __shfl_sync(kFullMask, myid, k - kbase);
         const int jb = pb0 + warp + k * NW;
@@ -524,18 +524,18 @@ __device__ __forceinline__ void combine_head(const DecodeParams& p, long long gh
                 for (int i = 0; i < PL; ++i) ov[u][i] = 0.f;
                 if (c < nparts) {
                     const long long sl = slot_of(c);
-                    mv[u] = __ldg(p.part_ml + 2 * sl);
-                    lv[u] = __ldg(p.part_ml + 2 * sl + 1);
+                    mv[u] = ld_dep(p.part_ml + 2 * sl);
+                    lv[u] = ld_dep(p.part_ml + 2 * sl + 1);
                     const float* oc = p.part_o + sl * D + lane * PL;
                     if constexpr (PL == 4) {
-                        const float4 v = __ldg(reinterpret_cast<const float4*>(oc));
+                        const float4 v = ld_dep(reinterpret_cast<const float4*>(oc));
                         ov[u][0] = v.x;
                         ov[u][1] = v.y;
                         ov[u][2] = v.z;
                         ov[u][3] = v.w;
                     } else {
 #pragma unroll
-                        for (int i = 0; i < PL; ++i) ov[u][i] = __ldg(oc + i);
+                        for (int i = 0; i < PL; ++i) ov[u][i] = ld_dep(oc + i);
                     }
                 }
             }
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(256) pa_combine_kernel(const DecodeParams p, i
     const long long gh = (long long)blockIdx.x * HPC + hl;  // b * H + h
     int nparts = 0;
     if (gh < (long long)p.batch * p.H) {
-        int n = __ldg(p.lens + gh / p.H);
+        int n = ld_dep(p.lens + gh / p.H);
         if (n < 0 || n > p.maxb * B) n = 0;
         const int nblk = (n + B - 1) / B;
         nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
@@ -692,9 +692,9 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
                     ov[r][c] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (r < rounds && hh < chunk && nparts == 2) {
                         const long long sl = slot_of(hh, c);
-                        mv[r][c] = __ldg(p.part_ml + 2 * sl);
-                        lv[r][c] = __ldg(p.part_ml + 2 * sl + 1);
-                        ov[r][c] = __ldg(reinterpret_cast<const float4*>(p.part_o + sl * D) + lane);
+                        mv[r][c] = ld_dep(p.part_ml + 2 * sl);
+                        lv[r][c] = ld_dep(p.part_ml + 2 * sl + 1);
+                        ov[r][c] = ld_dep(reinterpret_cast<const float4*>(p.part_o + sl * D) + lane);
                     }
                 }
             }

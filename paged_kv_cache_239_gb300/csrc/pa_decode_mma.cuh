@@ -72,7 +72,6 @@ __global__ void __launch_bounds__(NW * 32)
     pa_decode_mma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                          const __grid_constant__ CUtensorMap tmv) {
     pdl_trigger();
-    pdl_wait();
     using C = MmaCfg<D, B, G, NW, S>;
     extern __shared__ unsigned char smem_raw[];
 
@@ -97,30 +96,10 @@ __global__ void __launch_bounds__(NW * 32)
     const int b = idx / p.Hkv;
     const int hbase = kvh * p.gsize + hc * G;  // first query head of this CTA in the sequence
 
-    // The first 32 block ids of this warp's share of the partition depend only
-    // on the partition index (the table row holds maxb entries): their load
-    // overlaps the length's instead of waiting for it.
-    const int* bt_row = p.bt + (long long)b * p.maxb;
-    const int k_first = c * p.PB + warp + lane * NW;
-    const int id_first = k_first < p.maxb ? __ldg(bt_row + k_first) : -1;
-    // The fused append's position and new rows do not depend on the length
-    // either: all four loads are in flight together.
-    const bool fused = p.new_k != nullptr;
-    const int pos = fused ? __ldg(p.positions + b) : 0;
-    const uint4 new_row = fused ? load_new_row<D * 2>(p, b, kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
-
-    int n = __ldg(p.lens + b);
-    if (n < 0 || n > p.maxb * B) {
-        if (c == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
-        n = 0;
-    }
-    const int nblk = (n + B - 1) / B;
-    const int nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
-    if (c >= nparts) return;
-    const int pb0 = c * p.PB;
-    const int pb1 = min(nblk, pb0 + p.PB);
-
     // 1024-byte aligned stage area (swizzle atoms), then per-warp metadata.
+    // The barriers and the tensor maps read nothing the previous kernel
+    // writes: they are set up before the programmatic-launch wait, while that
+    // kernel drains.
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
     unsigned char* smem = smem_raw + (base_addr - raw_addr);
@@ -140,6 +119,30 @@ __global__ void __launch_bounds__(NW * 32)
         }
     }
     __syncwarp();
+    pdl_wait();
+
+    // The first 32 block ids of this warp's share of the partition depend only
+    // on the partition index (the table row holds maxb entries): their load
+    // overlaps the length's instead of waiting for it.
+    const int* bt_row = p.bt + (long long)b * p.maxb;
+    const int k_first = c * p.PB + warp + lane * NW;
+    const int id_first = k_first < p.maxb ? ld_dep(bt_row + k_first) : -1;
+    // The fused append's position and new rows do not depend on the length
+    // either: all four loads are in flight together.
+    const bool fused = p.new_k != nullptr;
+    const int pos = fused ? ld_dep(p.positions + b) : 0;
+    const uint4 new_row = fused ? load_new_row<D * 2>(p, b, kvh, lane) : make_uint4(0u, 0u, 0u, 0u);
+
+    int n = ld_dep(p.lens + b);
+    if (n < 0 || n > p.maxb * B) {
+        if (c == 0 && kvh == 0 && hc == 0 && threadIdx.x == 0) atomicOr(p.status, kStatusBadLength);
+        n = 0;
+    }
+    const int nblk = (n + B - 1) / B;
+    const int nparts = nblk > 0 ? (nblk + p.PB - 1) / p.PB : 1;
+    if (c >= nparts) return;
+    const int pb0 = c * p.PB;
+    const int pb1 = min(nblk, pb0 + p.PB);
 
     const int span = pb1 - pb0;
     const int nk = span > warp ? (span - warp + NW - 1) / NW : 0;
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(NW * 32)
                     // when k < 32
                     const int k = (jb - pb0) / NW;
                     int blk = __shfl_sync(kFullMask, id_first, k & 31);
-                    if (k >= 32) blk = __ldg(bt_row + jb);
+                    if (k >= 32) blk = ld_dep(bt_row + jb);
                     if (blk < 0 || blk >= p.num_blocks) {
                         if (lane == 0) atomicOr(p.status, kStatusBadBlock);
                     } else {
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(NW * 32)
                 }
             } else if (warp == 0) {
                 // past the decoded context: no copy of this call needs the row
-                const int blk = __ldg(bt_row + jb);
+                const int blk = ld_dep(bt_row + jb);
                 if (blk < 0 || blk >= p.num_blocks) {
                     if (lane == 0) atomicOr(p.status, kStatusBadBlock);
                 } else {
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(NW * 32)
         if (k >= kbase + 32) {
             kbase += 32;
             const int kk = kbase + lane;
-            myid = (kk < nk) ? __ldg(bt_row + pb0 + warp + kk * NW) : -1;
+            myid = (kk < nk) ? ld_dep(bt_row + pb0 + warp + kk * NW) : -1;
         }
         const int blk = __shfl_sync(kFullMask, myid, k - kbase);
         const int jb = pb0 + warp + k * NW;

@@ -448,15 +448,15 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         auto box_block = [&](const UItem& pc, int i) {
             const int tok = pc.t0 + i * C::TT + 16 * lane;
             return (i < pc.ntiles && lane < C::NBOX && tok < pc.t1)
-                       ? __ldg(p.bt + (long long)pc.b * p.maxb + tok / B)
+                       ? ld_dep(p.bt + (long long)pc.b * p.maxb + tok / B)
                        : 0;
         };
         // the appended row of a piece's (sequence, KV head): its position and
         // (lanes < 16) one 16-byte chunk of its 256 bytes
-        auto row_pos = [&](const UItem& pc) { return append ? __ldg(p.positions + pc.b) : -1; };
+        auto row_pos = [&](const UItem& pc) { return append ? ld_dep(p.positions + pc.b) : -1; };
         auto row_val = [&](const UItem& pc) {
             return (append && lane < 16)
-                       ? __ldg(reinterpret_cast<const uint4*>(
+                       ? ld_dep(reinterpret_cast<const uint4*>(
                                    new_rows + ((long long)pc.b * p.Hkv + pc.kvh) * 256) +
                                lane)
                        : make_uint4(0, 0, 0, 0);
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 } else if (pos < it.n) {
                     if (pos >= it.t0 && pos < it.t1) store_tile = (pos - it.t0) / C::TT;
                 } else if (it.u == 0) {
-                    store_row(__ldg(p.bt + (long long)it.b * p.maxb + pos / B));
+                    store_row(ld_dep(p.bt + (long long)it.b * p.maxb + pos / B));
                 }
             }
 
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         // one piece ahead (later tiles' ids are loaded a tile ahead)
         auto first_block = [&](const UItem& pc) {
             const int tok = pc.t0 + r;
-            return (pc.ntiles > 0 && tok < pc.t1) ? __ldg(p.bt + (long long)pc.b * p.maxb + tok / B)
+            return (pc.ntiles > 0 && tok < pc.t1) ? ld_dep(p.bt + (long long)pc.b * p.maxb + tok / B)
                                                   : -1;
         };
         UItem it;
@@ -780,7 +780,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             const int* bt_row = p.bt + (long long)it.b * p.maxb;
             auto tok_block = [&](int i) {
                 const int tok = it.t0 + i * C::TT + r;
-                return (i < it.ntiles && tok < it.t1) ? __ldg(bt_row + tok / B) : -1;
+                return (i < it.ntiles && tok < it.t1) ? ld_dep(bt_row + tok / B) : -1;
             };
             int blk_next = blk0;
             for (int i = 0; i < it.ntiles; ++i, ++kt) {

@@ -28,6 +28,20 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Loads of data that another kernel writes -- block tables, lengths,
+// positions, new rows, pool rows, partials.  With programmatic launch the
+// previous kernel may still be running when this one starts, so such a load
+// must stay after pdl_wait().  A read-only load (__ldg, ld.global.nc) promises
+// that nothing writes the data while the kernel runs, and the compiler may
+// schedule it ahead of the wait (GB300: once the decode set up its barriers
+// before the wait, its read-only loads returned wrong results in a graph of
+// device allocation and decode steps).  These are plain loads: the wait's
+// memory clobber keeps them after it, and they still use L1.
+template <typename T>
+__device__ __forceinline__ T ld_dep(const T* p) {
+    return *p;
+}
+
 // Host: launch `kern` with the programmatic-serialisation attribute.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,

@@ -24,7 +24,7 @@ __device__ __forceinline__ void warp_store_new_row(const DecodeParams& p, int b,
     for (int i = lane; i < 2 * CPR; i += 32) {
         const int kv = i / CPR;
         const int ci = i % CPR;
-        const uint4 val = __ldg(reinterpret_cast<const uint4*>(
+        const uint4 val = ld_dep(reinterpret_cast<const uint4*>(
             static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src + ci * 16));
         unsigned char* dst = static_cast<unsigned char*>(const_cast<void*>(kv ? p.v_base : p.k_base)) +
                              row * ELT;
@@ -46,7 +46,7 @@ __device__ __forceinline__ uint4 load_new_row(const DecodeParams& p, int b, int 
     if (lane < 2 * CPR) {
         const int kv = lane / CPR;
         const long long src = ((long long)b * p.Hkv + kvh) * ROW_BYTES + (lane % CPR) * 16;
-        val = __ldg(reinterpret_cast<const uint4*>(
+        val = ld_dep(reinterpret_cast<const uint4*>(
             static_cast<const unsigned char*>(kv ? p.new_v : p.new_k) + src));
     }
     return val;

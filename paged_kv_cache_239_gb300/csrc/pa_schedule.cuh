@@ -50,7 +50,7 @@ __device__ __forceinline__ void sched_pair_units(const DecodeParams& p, int b0, 
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int b = b0 + 8 * lane + k;
-        nv[k] = b < p.batch ? __ldg(p.lens + b) : 0;
+        nv[k] = b < p.batch ? ld_dep(p.lens + b) : 0;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k)
@@ -151,7 +151,7 @@ __device__ __forceinline__ void sched_walk_seq(const DecodeParams& p, SWalk& w, 
     w.bad = n_raw < 0 || n_raw > maxtok;
     w.n = w.bad ? 0 : n_raw;
     w.c = sched_units<TU>(w.n, maxtok);
-    w.n_next = w.b + 1 < p.batch ? __ldg(p.lens + w.b + 1) : 0;
+    w.n_next = w.b + 1 < p.batch ? ld_dep(p.lens + w.b + 1) : 0;
 }
 
 template <int B, int TU>
@@ -166,7 +166,7 @@ __device__ __forceinline__ void sched_walk_begin(const DecodeParams& p,
     w.g = s32[1];
     w.o = s32[2];
     w.emitted = false;
-    if (w.left > 0) sched_walk_seq<B, TU>(p, w, __ldg(p.lens + w.b));
+    if (w.left > 0) sched_walk_seq<B, TU>(p, w, ld_dep(p.lens + w.b));
 }
 
 template <int B, int TU, int OV, int G>
