@@ -48,6 +48,10 @@ struct MmaCfg {
     static constexpr int KS = D / 16;              // k-steps of S = K Q^T
     static constexpr int MT = D / 16;              // m-tiles of O^T = V^T P
     static constexpr int NT = (G + 7) / 8;         // 8-head mma tiles of the group
+    // A warp's O in the merge area: one row of D floats per head, rows D + 4
+    // apart, so that the four lanes of an mma group (heads 2cq, D columns
+    // apart) write to different banks.
+    static constexpr int ACC_LD = D + 4;
     static constexpr int WARP_STAGE_BYTES = S * STAGE_BYTES;
     static constexpr int META_BYTES = 64;          // per warp: nvalid[S], mbarriers[S]
     static constexpr int SMEM_BYTES = NW * WARP_STAGE_BYTES + NW * META_BYTES + 1024;
@@ -56,7 +60,7 @@ struct MmaCfg {
     static_assert(B % R == 0, "block size must be a multiple of 16");
     static_assert(G >= 1 && G <= 16, "GQA group of at most 16 query heads");
     static_assert(S * 12 <= META_BYTES, "meta");
-    static_assert((2 * G + G * D) * 4 <= WARP_STAGE_BYTES, "merge area must fit in the stages");
+    static_assert((2 * G + G * ACC_LD) * 4 <= WARP_STAGE_BYTES, "merge area must fit in the stages");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(NW * 32)
     __syncwarp();
     float* w_m = reinterpret_cast<float*>(wbase);
     float* w_l = w_m + G;
-    float* w_acc = w_l + G;  // [G][D]
+    float* w_acc = w_l + G;  // [G][ACC_LD]
 #pragma unroll
     for (int nt = 0; nt < C::NT; ++nt) {
         const int h0 = 8 * nt + 2 * cq;
@@ -429,12 +433,12 @@ __global__ void __launch_bounds__(NW * 32)
         for (int mt = 0; mt < C::MT; ++mt) {
             const int d = 16 * mt + g;
             if (h0_ok[nt]) {
-                w_acc[h0 * D + d] = o[nt][mt][0];
-                w_acc[h0 * D + d + 8] = o[nt][mt][2];
+                w_acc[h0 * C::ACC_LD + d] = o[nt][mt][0];
+                w_acc[h0 * C::ACC_LD + d + 8] = o[nt][mt][2];
             }
             if (h1_ok[nt]) {
-                w_acc[(h0 + 1) * D + d] = o[nt][mt][1];
-                w_acc[(h0 + 1) * D + d + 8] = o[nt][mt][3];
+                w_acc[(h0 + 1) * C::ACC_LD + d] = o[nt][mt][1];
+                w_acc[(h0 + 1) * C::ACC_LD + d + 8] = o[nt][mt][3];
             }
         }
     }
@@ -456,7 +460,7 @@ __global__ void __launch_bounds__(NW * 32)
             const float mw = wm[h];
             const float wt = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
             Lsum += wt * wm[G + h];
-            O += wt * wm[2 * G + h * D + d];
+            O += wt * wm[2 * G + h * C::ACC_LD + d];
         }
         if (nparts == 1) {
             p.out[(head0 + h) * D + d] = Lsum > 0.f ? O / Lsum : 0.f;
