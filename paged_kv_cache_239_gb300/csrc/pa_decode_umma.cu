@@ -47,6 +47,7 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaSt
         case 32: return launch_inst<B, 32>(p, tm, s);
         case 48: return launch_inst<B, 48>(p, tm, s);
         case 64: return launch_inst<B, 64>(p, tm, s);
+        case 128: return launch_inst<B, 128>(p, tm, s);
         default: return cudaErrorNotSupported;
     }
 }
@@ -55,6 +56,7 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaSt
 
 int decode_umma_chunk(int G) {
     if (G <= 0 || G % 16 != 0) return 0;
+    if (G % 128 == 0) return 128;
     if (G % 64 == 0) return 64;
     if (G % 48 == 0) return 48;
     if (G % 32 == 0) return 32;

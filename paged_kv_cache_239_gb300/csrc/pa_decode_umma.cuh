@@ -91,6 +91,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t 
         : "memory");
 }
 
+// D (TMEM) = A . B (+ D), A read from tensor memory (M rows on the lanes, two
+// 16-bit K elements per 32-bit column, the first in the low half), B from
+// shared memory.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // The mbarrier receives one arrival once every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -204,11 +216,34 @@ __device__ __forceinline__ bool part_bar_or(int part, bool v) {
     return r != 0;
 }
 
+// HM softmax: named barriers over the four warps of one TMEM lane quarter (the
+// four token parts of the same 32 heads): id 1 + 2 * quarter plain, 2 + 2 *
+// quarter with an OR reduction (the ids of the head parts' barriers above,
+// which an HM kernel does not use).
+__device__ __forceinline__ void quarter_bar(int qd) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + 2 * qd) : "memory");
+}
+__device__ __forceinline__ bool quarter_bar_or(int qd, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(2 + 2 * qd)
+        : "memory");
+    return r != 0;
+}
+
 // ------------------------------------------------------------------ config --
 
 template <int B_, int G_>
 struct UmmaCfg {
     static constexpr int D = 128, B = B_, G = G_;
+    // 128-head chunks put the heads on the rows of the accumulators (HM):
+    // S[128 heads x 128 tok] = Q K^T and O[128 heads x 128 d] += P V, with P
+    // written to tensor memory and read from there as the A operand -- no P
+    // buffer in shared memory, and one row of S and O per softmax thread.
+    static constexpr bool HM = G == 128;
     static constexpr int TT = 128;                  // tokens per tile (M of S = K Q^T)
     static constexpr int NBOX = TT / 16;            // 16-row boxes per 64-column half
     static constexpr int HALF = TT * 128;           // one 64-column half of a tile (bytes)
@@ -220,19 +255,29 @@ struct UmmaCfg {
     static constexpr int SV = 3;                    // V stages
     // P of a tile: [64-column block][token][128 B] rows of hi heads | lo heads
     // | zeros up to a whole block, in one buffer: the softmax of tile i + 1
-    // overlaps P V of tile i and waits for it only before writing P.
-    static constexpr int PW = (2 * G + 63) / 64 * 64;
+    // overlaps P V of tile i and waits for it only before writing P.  (HM: in
+    // tensor memory instead.)
+    static constexpr int PW = HM ? 0 : (2 * G + 63) / 64 * 64;
     static constexpr int P_BYTES = (PW / 64) * HALF;
     static constexpr int Q_BYTES = 2 * G * 128;     // q of one piece, two 64-column halves
-                                                    // (two buffers: the next piece's q
-                                                    // lands while this piece's S runs)
-    static constexpr int O_COL = 2 * G;             // TMEM: S0 [0, G), S1 [G, 2G), O^T after
-    static constexpr int TMEM_COLS = (2 * G + PW) <= 32 ? 32 : (2 * G + PW) <= 64 ? 64
-                                   : (2 * G + PW) <= 128 ? 128 : (2 * G + PW) <= 256 ? 256 : 512;
+    // q buffers: two (the next piece's q lands while this piece's S runs); HM
+    // one, for the third V stage (the next q is loaded once this piece's last
+    // S is done, while its last tiles' softmax and P V still run)
+    static constexpr int NQ = HM ? 1 : 2;
+    // TMEM: S0 [0, G), S1 [G, 2G), O^T after; HM: S0 [0, 128), S1 [128, 256),
+    // P [256, 384) (hi, tokens packed in pairs, then lo), O [384, 512).  (P in
+    // the tile's own S buffer, which the next S but one overwrites behind this
+    // tile's P V, measured the same on GB300: 78.2 against 78.3 us per call.)
+    static constexpr int S_COLS = HM ? TT : G;
+    static constexpr int P_COL = 256;
+    static constexpr int O_COL = HM ? 384 : 2 * G;
+    static constexpr int TMEM_USED = HM ? 512 : 2 * G + PW;
+    static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64
+                                   : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
     static constexpr int OFF_V = SK * TILE;
     static constexpr int OFF_P = OFF_V + SV * TILE;
     static constexpr int OFF_Q = OFF_P + P_BYTES;
-    static constexpr int OFF_CTRL = OFF_Q + 2 * Q_BYTES;
+    static constexpr int OFF_CTRL = OFF_Q + NQ * Q_BYTES;
     // ctrl: mbarriers [0, 224) | TMEM address | abort flag | m[G] | alpha[G] |
     // red[4][G] | this CTA's schedule (48 bytes)
     static constexpr int SCHED_OFF = 256 + 6 * G * 4;
@@ -241,9 +286,11 @@ struct UmmaCfg {
     static constexpr int SMEM_BYTES = OFF_CTRL + CTRL_BYTES + 1024;
     // warps: 0 K producer (+ q), 1 MMA, 2 V producer, 3 .. softmax (4 lane
     // quarters x 2, 3 or 4 head parts: more than one warp per scheduler, so
-    // the dependent latencies of the per-token work overlap)
-    static constexpr int NPART = G == 48 ? 3 : (G >= 64 ? 4 : 2);   // head parts
-    static constexpr int HG = G / NPART;            // heads per softmax warp
+    // the dependent latencies of the per-token work overlap; HM: 4 lane
+    // quarters of heads x 4 parts of the tile's tokens)
+    static constexpr int NPART = G == 48 ? 3 : (G >= 64 ? 4 : 2);   // head (HM: token) parts
+    static constexpr int HG = HM ? 8 : G / NPART;   // heads per softmax warp (not HM)
+    static constexpr int TP = TT / NPART;           // HM: tokens per softmax warp
     static constexpr int SM_WARP0 = 3;
     static constexpr int NSW = 4 * NPART;           // softmax warps
     static constexpr int NSM = NSW * 32;            // softmax threads
@@ -258,11 +305,13 @@ struct UmmaCfg {
     // phases ahead of a waiter (parity waits would alias); every other
     // barrier's next phase needs the waiter's own progress.
 
-    static_assert(G == 16 || G == 32 || G == 48 || G == 64, "head chunk of 16, 32, 48 or 64");
+    static_assert(G == 16 || G == 32 || G == 48 || G == 64 || G == 128,
+                  "head chunk of 16, 32, 48, 64 or 128");
     static_assert(B == 16 || B == 32, "block size 16 or 32");
     static_assert(NBAR * 8 <= TMEM_SLOT_OFF, "barriers");
-    static_assert(2 * G + PW <= TMEM_COLS, "TMEM columns");
+    static_assert(TMEM_USED <= TMEM_COLS, "TMEM columns");
     static_assert(HG == 8 || HG % 16 == 0, "TMEM loads of 8 or 16k columns");
+    static_assert(!HM || TP == 32, "HM: 32 tokens per softmax warp");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -562,19 +611,19 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 if (!is_v && i == 0) {
                     // q of the piece's G heads -> K-major swizzled tile
                     // [half][G][128 B] by two tensor-map copies, once its first
-                    // K copy is on its way (buffer qi & 1: free once the last S
-                    // of piece qi - 2 is done)
-                    if (qi >= 2 &&
-                        !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + (qi & 1)),
-                                                         ((qi >> 1) - 1) & 1, abort_all,
+                    // K copy is on its way (buffer qi % NQ: free once the last S
+                    // of piece qi - NQ is done)
+                    if (qi >= C::NQ &&
+                        !__all_sync(kFullMask, umma_wait(bar0 + 8 * (C::Q_EMPTY + qi % C::NQ),
+                                                         ((qi / C::NQ) - 1) & 1, abort_all,
                                                          p.status))) {
                         aborted = true;
                         ++kt;  // (tile 0's copy is in flight: the exit path waits for it)
                         break;
                     }
                     if (lane == 0) {
-                        const uint32_t qbuf = sbase + C::OFF_Q + (qi & 1) * C::Q_BYTES;
-                        const uint32_t qbar = bar0 + 8 * (C::Q_FULL + (qi & 1));
+                        const uint32_t qbuf = sbase + C::OFF_Q + (qi % C::NQ) * C::Q_BYTES;
+                        const uint32_t qbar = bar0 + 8 * (C::Q_FULL + qi % C::NQ);
                         const int qrow = it.b * p.H + it.hbase;
                         mbar_arrive_expect_tx(qbar, (uint32_t)C::Q_BYTES);
                         tma_load_2d(qbuf, &tmq, qbar, 0, qrow);
@@ -595,8 +644,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             // copies still in flight land before the CTA can exit
             for (int k = kt > NS ? kt - NS : 0; k < kt; ++k)
                 (void)mbar_wait_bounded(full0 + 8 * (k % NS), (k / NS) & 1);
-            for (int k = q_last > 0 ? q_last - 1 : 0; !is_v && k <= q_last; ++k)
-                (void)mbar_wait_bounded(bar0 + 8 * (C::Q_FULL + (k & 1)), (k >> 1) & 1);
+            for (int k = q_last >= C::NQ - 1 ? q_last - (C::NQ - 1) : 0; !is_v && k <= q_last; ++k)
+                (void)mbar_wait_bounded(bar0 + 8 * (C::Q_FULL + k % C::NQ), (k / C::NQ) & 1);
         }
     } else if (warp == 1) {
         // ============================================ MMA issuer (warp 1, lane 0)
@@ -612,8 +661,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             // Descriptors: each buffer's base is encoded once; a K-step adds its
             // byte offset / 16 to the start-address field (no carry: shared
             // addresses stay below 256 KB).
-            constexpr uint32_t IDQ = umma_idesc_bf16(128, G, 0, 0);
-            constexpr uint32_t IDP = umma_idesc_bf16(128, C::PW, 1, 1);
+            constexpr uint32_t IDQ = umma_idesc_bf16(128, C::HM ? C::TT : G, 0, 0);
+            constexpr uint32_t IDP = umma_idesc_bf16(128, C::HM ? 128 : C::PW, 1, 1);
             const uint64_t dP0 = umma_desc_sw128(sbase + C::OFF_P, C::HALF, 1024);
             const uint64_t dV0 = umma_desc_sw128(sbase + C::OFF_V, C::HALF, 1024);
             const uint64_t dK0 = umma_desc_sw128(sbase, 0, 1024);
@@ -635,11 +684,25 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     const int vs = kt_pv % C::SV;
                     const bool first = (first_bits >> (kt_pv & 1)) & 1u;
                     const uint64_t a0 = dV0 + (uint64_t)((vs * C::TILE) >> 4);
+                    if constexpr (C::HM) {
+                        // O[128 heads x 128 d] += P_hi V, then += P_lo V: A = P in
+                        // TMEM (a K-step of 16 tokens is 8 columns), B = V
+                        // (MN-major, the same descriptor as V^T as A below)
+                        constexpr uint32_t IDV = umma_idesc_bf16(128, 128, 0, 1);
+                        constexpr int KS = C::TT / 16;
 #pragma unroll
-                    for (int k = 0; k < C::TT / 16; ++k)
-                        umma_bf16(tmem + C::O_COL, a0 + (uint64_t)(k * (2048 >> 4)),
-                                  dP0 + (uint64_t)(k * (2048 >> 4)), IDP,
-                                  (k > 0 || !first) ? 1u : 0u);
+                        for (int k = 0; k < 2 * KS; ++k)
+                            umma_bf16_ts(tmem + C::O_COL,
+                                         tmem + C::P_COL + (k / KS) * 64 + (k % KS) * 8,
+                                         a0 + (uint64_t)((k % KS) * (2048 >> 4)), IDV,
+                                         (k > 0 || !first) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < C::TT / 16; ++k)
+                            umma_bf16(tmem + C::O_COL, a0 + (uint64_t)(k * (2048 >> 4)),
+                                      dP0 + (uint64_t)(k * (2048 >> 4)), IDP,
+                                      (k > 0 || !first) ? 1u : 0u);
+                    }
                     umma_commit(bar0 + 8 * (C::PV_DONE + (kt_pv & 1)));
                     umma_commit(bar0 + 8 * (C::V_EMPTY + vs));
                     ++kt_pv;
@@ -660,27 +723,32 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                         done_q = true;
                     } else {
                         if (!q_ready)
-                            q_ready = mbar_test(bar0 + 8 * (C::Q_FULL + (qi & 1)), (qi >> 1) & 1);
+                            q_ready = mbar_test(bar0 + 8 * (C::Q_FULL + qi % C::NQ), (qi / C::NQ) & 1);
                         const int ks = kt_q % C::SK;
                         if (q_ready &&
                             mbar_test(bar0 + 8 * (C::K_FULL + ks), (kt_q / C::SK) & 1)) {
                             tc_fence_after();
                             const uint64_t a0 = dK0 + (uint64_t)((ks * C::TILE) >> 4);
-                            const uint64_t b0 = dQ0 + (uint64_t)(((qi & 1) * C::Q_BYTES) >> 4);
+                            const uint64_t b0 = dQ0 + (uint64_t)(((qi % C::NQ) * C::Q_BYTES) >> 4);
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
                                 const int h = k >> 2, kk = k & 3;
-                                umma_bf16(tmem + (kt_q & 1) * G,
-                                          a0 + (uint64_t)((h * C::HALF + kk * 32) >> 4),
-                                          b0 + (uint64_t)((h * (G * 128) + kk * 32) >> 4), IDQ,
-                                          k > 0 ? 1u : 0u);
+                                const uint64_t kdesc = a0 + (uint64_t)((h * C::HALF + kk * 32) >> 4);
+                                const uint64_t qdesc =
+                                    b0 + (uint64_t)((h * (G * 128) + kk * 32) >> 4);
+                                if constexpr (C::HM)   // S[128 heads x 128 tok] = Q K^T
+                                    umma_bf16(tmem + (kt_q & 1) * C::S_COLS, qdesc, kdesc, IDQ,
+                                              k > 0 ? 1u : 0u);
+                                else                   // S[128 tok x G] = K Q^T
+                                    umma_bf16(tmem + (kt_q & 1) * C::S_COLS, kdesc, qdesc, IDQ,
+                                              k > 0 ? 1u : 0u);
                             }
                             umma_commit(bar0 + 8 * (C::S_FULL + (kt_q & 1)));
                             umma_commit(bar0 + 8 * (C::K_EMPTY + ks));
                             first_bits = (first_bits & ~(1u << (kt_q & 1))) |
                                          ((i_q == 0 ? 1u : 0u) << (kt_q & 1));
                             ++i_q;
-                            if (--tiles_left == 0) umma_commit(bar0 + 8 * (C::Q_EMPTY + (qi & 1)));
+                            if (--tiles_left == 0) umma_commit(bar0 + 8 * (C::Q_EMPTY + qi % C::NQ));
                             ++kt_q;
                             progressed = true;
                         }
@@ -696,7 +764,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 // its K) while it may run ahead, else the pending P V's P
                 if (!done_q && tiles_left > 0 && kt_q < kt_pv + 2) {
                     if (!q_ready)
-                        (void)mbar_try_wait_for(bar0 + 8 * (C::Q_FULL + (qi & 1)), (qi >> 1) & 1,
+                        (void)mbar_try_wait_for(bar0 + 8 * (C::Q_FULL + qi % C::NQ), (qi / C::NQ) & 1,
                                                 200);
                     else
                         (void)mbar_try_wait_for(bar0 + 8 * (C::K_FULL + kt_q % C::SK),
@@ -719,6 +787,222 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
             (void)mbar_wait_bounded(bar0 + 8 * C::FINAL, 0);
         }
         __syncwarp();
+    } else if constexpr (C::HM) {
+        // ========== softmax, heads on the rows (128-head chunks): warp w reads
+        // TMEM lane quarter w % 4 (heads 32 * (w % 4) + lane) and the tile's
+        // tokens [32 * part, 32 * part + 32) of S; O's head-dim columns are
+        // split the same way.  A thread holds one head's running max (the four
+        // parts of a quarter agree on it at the quarter's barrier) and its
+        // part's share of the sum.
+        const int part = (warp - C::SM_WARP0) >> 2;
+        const int qd = warp & 3;
+        const int hrow = qd * 32 + lane;       // head within the chunk (TMEM lane)
+        const int c0 = part * C::TP;           // the part's first token / head-dim column
+        const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+        int kt = 0;
+        bool stop = false;
+        bool failed = false;   // (as below: the threads stop together at a barrier)
+        auto swait = [&](uint32_t bar, uint32_t parity) {
+            return umma_wait(bar, parity, abort_all, p.status);
+        };
+        // block ids of the part's 32 tokens in tile i of a piece (two boxes of
+        // 16 tokens; one block when B = 32), -1 past the piece; loaded a tile
+        // ahead
+        auto part_blocks = [&](const UItem& pc, int i, int& b0, int& b1) {
+            const int tok = pc.t0 + i * C::TT + c0;
+            const int* row = p.bt + (long long)pc.b * p.maxb;
+            b0 = (i < pc.ntiles && tok < pc.t1) ? ld_dep(row + tok / B) : -1;
+            if constexpr (B == 16)
+                b1 = (i < pc.ntiles && tok + 16 < pc.t1) ? ld_dep(row + (tok + 16) / B) : -1;
+            else
+                b1 = b0;
+        };
+        UWalk w;
+        umma_walk_begin<B>(p, ctrl + C::SCHED_OFF, w);
+        UItem it;
+        bool have = umma_walk_next<B, G>(p, w, it);
+        int nb0 = -1, nb1 = -1;
+        if (have) part_blocks(it, 0, nb0, nb1);
+        while (!stop && have) {
+            if (it.ntiles == 0) {  // empty context: output 0 (always a whole piece)
+                const long long head0 = (long long)it.b * p.H + it.hbase;
+                float4* o4 = reinterpret_cast<float4*>(p.out + (head0 + hrow) * 128 + c0);
+#pragma unroll
+                for (int j = 0; j < C::TP / 4; ++j) o4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                have = umma_walk_next<B, G>(p, w, it);
+                if (have) part_blocks(it, 0, nb0, nb1);
+                continue;
+            }
+            float m_run = -INFINITY;   // this head's running max (the floor -FLT_MAX
+            float l_run = 0.f;         // once a tile has passed), this part's sum
+            for (int i = 0; i < it.ntiles; ++i, ++kt) {
+                const int stage = kt % C::SV;  // V stage
+                const int b0 = nb0, b1 = nb1;
+                part_blocks(it, i + 1, nb0, nb1);
+                // the part's valid tokens: before the piece's end, in a good block
+                uint32_t vm;
+                {
+                    const int nv = it.t1 - (it.t0 + i * C::TT + c0);
+                    vm = nv >= 32 ? 0xffffffffu : (nv > 0 ? (1u << nv) - 1u : 0u);
+                    if (b0 < 0 || b0 >= p.num_blocks) vm &= 0xffff0000u;
+                    if (b1 < 0 || b1 >= p.num_blocks) vm &= 0x0000ffffu;
+                }
+                const bool ok = swait(bar0 + 8 * (C::S_FULL + (kt & 1)), (kt >> 1) & 1);
+                failed = failed || !ok;
+                __syncwarp();
+                tc_fence_after();
+                float x[C::TP];
+                {
+                    uint32_t v[C::TP];
+                    tmem_ld_cols<C::TP>(trow + (kt & 1) * C::S_COLS + c0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < C::TP; ++j)
+                        x[j] = ((vm >> j) & 1u) ? __uint_as_float(v[j]) * p.qscale : -INFINITY;
+                }
+                float mloc = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < C::TP; ++j) mloc = fmaxf(mloc, x[j]);
+                // the running max is raised (to the tile's max over the four
+                // parts) only when a score exceeds it by more than 2^8; every
+                // part of the head takes the same decision from the same values
+                float alpha = 1.f;
+                bool raised = false;
+                if (quarter_bar_or(qd, i == 0 || mloc - m_run > 8.f || failed)) {
+                    red[part * G + hrow] = mloc;
+                    if (quarter_bar_or(qd, failed)) {
+                        stop = true;
+                        break;
+                    }
+                    const float mt = fmaxf(fmaxf(red[hrow], red[G + hrow]),
+                                           fmaxf(red[2 * G + hrow], red[3 * G + hrow]));
+                    if (i == 0 || mt - m_run > 8.f) {
+                        // (a head with no valid score yet keeps the finite floor
+                        // -FLT_MAX: its scores minus the max are -inf, p = 0)
+                        const float mn = fmaxf(fmaxf(m_run, mt), -FLT_MAX);
+                        alpha = (i == 0) ? 0.f : exp2f(m_run - mn);
+                        m_run = mn;
+                        raised = i > 0;
+                    }
+                }
+                float lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < C::TP; ++j) {
+                    const float pv = ex2_approx(x[j] - m_run);
+                    lsum += pv;
+                    x[j] = pv;
+                }
+                l_run = l_run * alpha + lsum;
+                // the P columns and O are free once the previous tile's P V is
+                // done
+                if (kt > 0 &&
+                    !swait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1))
+                    failed = true;
+                // V of this tile must have landed before its invalid rows are
+                // zeroed (0 * a stale value must stay 0); warp (part, quarter)
+                // takes the part's rows 8 * quarter .. + 8, each row's 16 chunks
+                // over four lanes
+                if (!swait(bar0 + 8 * (C::V_FULL + stage), (kt / C::SV) & 1)) failed = true;
+                {
+                    const int rr = 8 * qd + (lane >> 2);
+                    if (!((vm >> rr) & 1u)) {
+                        unsigned char* vrow = smem + C::OFF_V + stage * C::TILE + (c0 + rr) * 128;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int ch = (lane & 3) * 4 + k;   // half ch / 8, chunk ch % 8
+                            *reinterpret_cast<uint4*>(vrow + (ch >> 3) * C::HALF + (ch & 7) * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                // P of the part's tokens as bf16 hi, then lo, two tokens per
+                // column (the first in the low half): columns P_COL + 16 * part
+                // and P_COL + 64 + 16 * part (in two halves of 16 tokens: fewer
+                // registers live at once)
+                const uint32_t sbuf = trow + C::P_COL;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float a = x[16 * hf + 2 * c], b = x[16 * hf + 2 * c + 1];
+                        hi[c] = pack_bf16x2(a, b);
+                        const float ha = __uint_as_float(hi[c] << 16);
+                        const float hb = __uint_as_float(hi[c] & 0xffff0000u);
+                        lo[c] = pack_bf16x2(a - ha, b - hb);
+                    }
+                    tmem_st8(sbuf + c0 / 2 + 8 * hf, hi);
+                    tmem_st8(sbuf + 64 + c0 / 2 + 8 * hf, lo);
+                }
+                if (raised) {
+                    // O (this piece's earlier tiles) by the same factor: the
+                    // part's 32 of the row's 128 head-dim columns
+                    tc_fence_after();
+                    uint32_t v[C::TP];
+                    tmem_ld_cols<C::TP>(trow + C::O_COL + c0, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < C::TP; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                    tmem_st_cols<C::TP>(trow + C::O_COL + c0, v);
+                }
+                tmem_wait_st();
+                // one arrival per warp, after all its lanes' writes
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar0 + 8 * (C::P_FULL + (kt & 1)));
+            }
+            if (stop) break;
+
+            // ---- piece epilogue: the four parts' sums, the O row, output ----
+            if (!swait(bar0 + 8 * (C::PV_DONE + ((kt - 1) & 1)), ((kt - 1) >> 1) & 1))
+                failed = true;
+            // (every part has read the last tile's maxima before the sums
+            // replace them)
+            if (quarter_bar_or(qd, failed)) {
+                stop = true;
+                break;
+            }
+            red[part * G + hrow] = l_run;
+            quarter_bar(qd);
+            const float L = (red[hrow] + red[G + hrow]) + (red[2 * G + hrow] + red[3 * G + hrow]);
+            __syncwarp();
+            tc_fence_after();
+            {
+                uint32_t v[C::TP];
+                tmem_ld_cols<C::TP>(trow + C::O_COL + c0, v);
+                tmem_wait_ld();
+                if (it.whole) {
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    const long long head0 = (long long)it.b * p.H + it.hbase;
+                    float4* o4 = reinterpret_cast<float4*>(p.out + (head0 + hrow) * 128 + c0);
+#pragma unroll
+                    for (int j = 0; j < C::TP / 4; ++j)
+                        o4[j] = make_float4(__uint_as_float(v[4 * j]) * inv,
+                                            __uint_as_float(v[4 * j + 1]) * inv,
+                                            __uint_as_float(v[4 * j + 2]) * inv,
+                                            __uint_as_float(v[4 * j + 3]) * inv);
+                } else {
+                    const long long slot =
+                        ((long long)blockIdx.x * 2 + (it.first ? 0 : 1)) * G + hrow;
+                    float4* o4 = reinterpret_cast<float4*>(p.part_o + slot * 128 + c0);
+#pragma unroll
+                    for (int j = 0; j < C::TP / 4; ++j)
+                        o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]),
+                                            __uint_as_float(v[4 * j + 3]));
+                    if (part == 0) {
+                        p.part_ml[slot * 2 + 0] = m_run == -FLT_MAX ? -INFINITY : m_run;
+                        p.part_ml[slot * 2 + 1] = L;
+                    }
+                }
+            }
+            tc_fence_before();
+            // the next piece, and its first tile's block ids
+            have = umma_walk_next<B, G>(p, w, it);
+            if (have) part_blocks(it, 0, nb0, nb1);
+        }
     } else {
         // ====================== softmax (warps SM_WARP0 .. SM_WARP0 + NSW - 1)
         // Warp w works on TMEM lane quarter w % 4 (token / head-dim rows

@@ -25,7 +25,8 @@ def _status_clear():
 
 
 @pytest.mark.parametrize("Hkv,H,Bs", [(1, 16, 16), (2, 32, 16), (1, 64, 32), (2, 128, 16),
-                                       (1, 48, 16), (1, 96, 32), (1, 128, 16), (1, 192, 32)])
+                                       (1, 48, 16), (1, 96, 32), (1, 128, 16), (1, 192, 32),
+                                       (1, 128, 32), (2, 256, 16), (1, 256, 32)])
 def test_groups_match_oracle_every_partition(cuda_device, Hkv, H, Bs):
     wl = W.custom("tc", "bf16", 2, H, Hkv, 128, Bs, LENS, seed=H + Bs, spare_blocks=3,
                   interleave=True)
@@ -68,7 +69,8 @@ def test_tcgen05_refuses_other_shapes(cuda_device):
             gp.close()
 
 
-@pytest.mark.parametrize("H,Bs,pb", [(32, 16, 0), (64, 32, 4), (16, 16, 1)])
+@pytest.mark.parametrize("H,Bs,pb", [(32, 16, 0), (64, 32, 4), (16, 16, 1), (128, 16, 0),
+                                     (128, 32, 0)])
 def test_fused_append_matches_oracle(cuda_device, H, Bs, pb):
     wl = W.custom("tcapp", "bf16", 2, H, 1, 128, Bs, [0, 1, Bs - 1, Bs, 127, 128, 300, 511],
                   seed=11 + H, spare_blocks=4, interleave=True, steps=1)
@@ -172,7 +174,8 @@ def _poison_unused_rows(pool, wl):
     return t
 
 
-@pytest.mark.parametrize("H,Hkv,D,kind", [(32, 1, 128, "TCGEN05"), (16, 2, 128, "TENSOR_CORES"),
+@pytest.mark.parametrize("H,Hkv,D,kind", [(32, 1, 128, "TCGEN05"), (128, 1, 128, "TCGEN05"),
+                                         (16, 2, 128, "TENSOR_CORES"),
                                          (8, 2, 64, "TENSOR_CORES"), (8, 2, 64, "CUDA_CORES")])
 def test_values_past_the_context_are_never_used(cuda_device, H, Hkv, D, kind):
     wl = W.custom("nan", "bf16", 1, H, Hkv, D, 16, [1, 7, 16, 100, 129, 250], seed=91,
@@ -257,7 +260,8 @@ def test_graph_replays_match(cuda_device):
 @pytest.mark.parametrize("lens,H,Hkv", [
     ([20000], 64, 1),                 # one context cut into a piece per CTA
     ([1], 64, 1),                     # one unit: a single CTA has work
-    ([5000, 0, 3, 9000, 0], 128, 1),  # two 64-head chunks, empty contexts
+    ([5000, 0, 3, 9000, 0], 128, 1),  # one 128-head chunk (heads on the rows), empty contexts
+    ([5000, 0, 3, 9000, 0], 192, 1),  # three 64-head chunks, empty contexts
     ([700, 1500, 0, 129, 2047], 48, 1),   # three 16-head chunks
     ([33000, 17, 128], 32, 2),        # long + short, two KV heads
 ])
