@@ -150,8 +150,9 @@ PA_API int pa_pool_destroy(pa_pool* pool);
  * (num_heads / num_kv_heads) 1-8, 16 or any multiple of 8 on the mma.sync
  * tensor-core kernel (bf16 pools; groups above 16 run as 16- or 8-head chunks
  * whose CTAs share each K/V tile through L2), any multiple of 16 on the
- * tcgen05 kernel (bf16 pools, head_dim 128; chunks of 64, 48, 32 or 16 heads),
- * 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
+ * tcgen05 kernel (bf16 pools, head_dim 128; chunks of 128, 64, 48, 32 or 16
+ * heads), 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes:
+ * PA_ERR_UNSUPPORTED.
  *
  * Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
  * for bf16 pools with head_dim 128 the tcgen05 kernel for groups that are

@@ -1,6 +1,6 @@
 // pa_decode_umma.cuh -- paged decode attention for bf16 pools with large GQA
-// groups (16, 32, 48 or 64 query heads per CTA) on the 5th-generation tensor cores:
-// tcgen05.mma with the accumulators in tensor memory (TMEM).
+// groups (16, 32, 48, 64 or 128 query heads per CTA) on the 5th-generation
+// tensor cores: tcgen05.mma with the accumulators in tensor memory (TMEM).
 //
 // Computes the same thing as the other decode kernels: for sequence b and query
 // head h, out = softmax_t(scale * q . K_t) V_t over the tokens reached through
@@ -41,6 +41,11 @@
 //    (|P - hi - lo| <= 2^-16 P) into the one P buffer once the previous P V
 //    has read it, and at the end of a piece read O^T (thread = head-dim
 //    element), add the hi and lo halves and store the output or the partial.
+// 128-head chunks (HM) swap the roles of the operands: S[128 heads x 128 tok]
+// = Q K^T and O[128 heads x 128 d] += P_hi V + P_lo V with P written to TMEM
+// by the softmax warps and read from there as the A operand; a softmax thread
+// then owns one head's row (16 warps: 4 lane quarters of heads x 4 quarters of
+// the tile's tokens, which agree on the running max at a named barrier).
 // Every wait is bounded (PA_STATUS_TIMEOUT); the roles then stop together,
 // wait for their copies and MMAs in flight, and TMEM is freed.
 #pragma once
