@@ -147,9 +147,10 @@ PA_API int pa_pool_create_strided(pa_pool** out, const pa_pool_layout* layout, i
 PA_API int pa_pool_destroy(pa_pool* pool);
 
 /* Built shapes: head_dim 64 or 128, block_size 16 or 32; GQA group
- * (num_heads / num_kv_heads) 1-8, 16 or any multiple of 8 on the mma.sync
- * tensor-core kernel (bf16 pools; groups above 16 run as 16- or 8-head chunks
- * whose CTAs share each K/V tile through L2), any multiple of 16 on the
+ * (num_heads / num_kv_heads) of any size on the mma.sync tensor-core kernel
+ * (bf16 pools; groups above 8 run as 16- or 8-head chunks whose CTAs share
+ * each K/V tile through L2, the last chunk holding the rest of a group that
+ * is no multiple of 8), any multiple of 16 on the
  * tcgen05 kernel (bf16 pools, head_dim 128; chunks of 128, 64, 48, 32 or 16
  * heads), 1, 2, 4 or 8 on the CUDA-core kernel.  Other shapes:
  * PA_ERR_UNSUPPORTED.

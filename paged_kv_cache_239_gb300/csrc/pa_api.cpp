@@ -163,8 +163,8 @@ int pick_kernel(const pa_pool* pool, int G, Kernel* k) {
     if (!cuda_ok && !mma_ok && !umma_ok)
         return fail(PA_ERR_UNSUPPORTED,
                     "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
-                    "(built: head_dim 64/128, block_size 16/32; group 1-8, 16 or a multiple of 8 "
-                    "for bf16 pools, 1/2/4/8 for fp32 pools)",
+                    "(built: head_dim 64/128, block_size 16/32; any group for bf16 pools, "
+                    "1/2/4/8 for fp32 pools)",
                     g.dtype, g.D, g.B, G);
     switch (pool->decode_kernel) {
         case PA_DECODE_CUDA_CORES:
@@ -196,8 +196,8 @@ int pick_kernel(const pa_pool* pool, int G, Kernel* k) {
 bool wide_fits(const pa_pool* pool, int G, int batch, int maxb, int sms) {
     const int chunk = pa::decode_mma_chunk(G);
     if (chunk == 0) return false;
-    return pa::decode_mma_wide_fits(pool->g.D, G, maxb, (long long)batch * pool->g.Hkv * (G / chunk),
-                                    sms);
+    return pa::decode_mma_wide_fits(pool->g.D, G, maxb,
+                                    (long long)batch * pool->g.Hkv * ((G + chunk - 1) / chunk), sms);
 }
 
 int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb,
@@ -243,7 +243,7 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         return PA_OK;
     }
     const int chunk = kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G) : G;
-    const long long nchunks = G / chunk;
+    const long long nchunks = (G + chunk - 1) / chunk;  // (mma.sync: a ragged last chunk)
     int pb = partition_blocks;
     bool wide = false;
     if (pb == 0) {
@@ -746,7 +746,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     p.tc_desc = tc_desc;
     p.tc_cut = tc_cut;
     p.gsize = sh.G;
-    p.nchunks = sh.G / sh.chunk;
+    p.nchunks = (sh.G + sh.chunk - 1) / sh.chunk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!sh.wide && sh.kernel == Kernel::MmaSync && sh.Cmax == 1) {
         // an explicit partition that covers the table: wide CTAs where they fit

@@ -40,7 +40,7 @@ int decode_mma_chunk(int G) {
     if (G >= 1 && G <= 8) return G;
     if (G == 16) return 16;
     if (G > 16 && G % 16 == 0) return 16;
-    if (G > 16 && G % 8 == 0) return 8;
+    if (G > 8) return 8;  // (the last chunk holds G % 8 heads when G is no multiple of 8)
     return 0;
 }
 
@@ -48,6 +48,7 @@ bool decode_mma_supported(int D, int B, int G) {
     if (D != 64 && D != 128) return false;
     if (B != 16 && B != 32) return false;
     // heads past G in the 8-wide mma tiles are masked; larger groups in chunks
+    // (a ragged last chunk masks the heads past the group the same way)
     return decode_mma_chunk(G) > 0;
 }
 
@@ -58,7 +59,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p_in, const void* tmaps, int D
     if (G == 0) return cudaErrorNotSupported;
     DecodeParams p = p_in;
     p.gsize = Gtot;
-    p.nchunks = Gtot / G;
+    p.nchunks = (Gtot + G - 1) / G;
     if (D == 64) {
         if (B == 16) return launch_mma_g<64, 16, kMmaWarps, kMmaStages<64>>(p, tm, G, s);
         if (B == 32) return launch_mma_g<64, 32, kMmaWarps, kMmaStages<64>>(p, tm, G, s);

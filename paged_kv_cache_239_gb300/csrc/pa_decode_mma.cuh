@@ -99,6 +99,9 @@ __global__ void __launch_bounds__(NW * 32)
     const int kvh = idx % p.Hkv;
     const int b = idx / p.Hkv;
     const int hbase = kvh * p.gsize + hc * G;  // first query head of this CTA in the sequence
+    // this chunk's heads: G, fewer in the last chunk of a group that is not a
+    // multiple of G (heads past them are masked like those past a small group)
+    const int gact = min(G, p.gsize - hc * G);
 
     // 1024-byte aligned stage area (swizzle atoms), then per-warp metadata.
     // The barriers and the tensor maps read nothing the previous kernel
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(NW * 32)
             reinterpret_cast<const unsigned short*>(p.q) + ((long long)b * p.H + hbase + hq) * D;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
-            if (hq < G) {
+            if (hq < gact) {
                 qb[nt][ks][0] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * cq);
                 qb[nt][ks][1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * cq);
             } else {
@@ -275,8 +278,8 @@ __global__ void __launch_bounds__(NW * 32)
         m1[nt] = -INFINITY;
         l0[nt] = 0.f;
         l1[nt] = 0.f;
-        h0_ok[nt] = 8 * nt + 2 * cq < G;
-        h1_ok[nt] = 8 * nt + 2 * cq + 1 < G;
+        h0_ok[nt] = 8 * nt + 2 * cq < gact;
+        h1_ok[nt] = 8 * nt + 2 * cq + 1 < gact;
     }
 
     int u_issue = 0;
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(NW * 32)
 
     // ---- merge the NW warps (log-sum-exp) and write ----
     const long long head0 = (long long)b * p.H + hbase;
-    for (int t = threadIdx.x; t < G * D; t += NW * 32) {
+    for (int t = threadIdx.x; t < gact * D; t += NW * 32) {
         const int h = t / D;
         const int d = t % D;
         float M = -INFINITY;

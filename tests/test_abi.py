@@ -156,7 +156,10 @@ def test_decode_host_checks(pa_lib):
 
         for bad, code in [(dict(layer=2), 1), (dict(B=32), 1), (dict(Hkv=1), 1), (dict(D=128), 1),
                           (dict(H=5), 1), (dict(maxb=0), 1), (dict(pb=-1), 1),
-                          (dict(scale=float("nan")), 1), (dict(H=18), 5), (dict(H=34), 5),
+                          (dict(scale=float("nan")), 1),
+                          # groups of 9 and 17 are served (8-head chunks, the last
+                          # ragged): the call fails only for want of a workspace
+                          (dict(H=18), 6), (dict(H=34), 6),
                           (dict(ws=None, wsb=0), 6), (dict(ws=F + 64, wsb=1 << 30), 6),
                           (dict(ws=F, wsb=16), 6)]:
             with pytest.raises(pa_lib.PagedAttnError) as e:
@@ -164,6 +167,14 @@ def test_decode_host_checks(pa_lib):
             assert e.value.code == code, (bad, e.value)
         # batch 0 is a no-op that needs no device
         call(batch=0)
+        # an fp32 pool runs only on the CUDA-core kernel: groups 1, 2, 4, 8
+        h32 = _pool(pa_lib, nb=8, L=2, Hkv=2, B=16, D=64, dtype=0)
+        try:
+            with pytest.raises(pa_lib.PagedAttnError) as e:
+                call(pool=h32, H=6)
+            assert e.value.code == pa_lib.PA_ERR_UNSUPPORTED
+        finally:
+            pa_lib.pa_pool_destroy(h32)
         with pytest.raises(pa_lib.PagedAttnError) as e:
             call(out=F + 4, ws=F, wsb=1 << 20)
         assert e.value.code == pa_lib.PA_ERR_INVALID_ARG
@@ -241,6 +252,9 @@ def test_decode_kernel_choice_query(pa_lib):
         (1, 128, 1, 16, L.PA_DECODE_TCGEN05),        # bf16, head_dim 128, group 16
         (2, 128, 1, 128, L.PA_DECODE_TCGEN05),       # group 64
         (1, 128, 1, 24, L.PA_DECODE_TENSOR_CORES),   # group 24: not a multiple of 16
+        (1, 128, 1, 71, L.PA_DECODE_TENSOR_CORES),   # group 71: 8-head chunks, the last of 7
+        (8, 128, 1, 232, L.PA_DECODE_TENSOR_CORES),  # group 29
+        (1, 128, 1, 128, L.PA_DECODE_TCGEN05),       # group 128: one chunk, heads on the rows
         (1, 64, 1, 32, L.PA_DECODE_TENSOR_CORES),    # head_dim 64: no tcgen05
         (2, 64, 0, 8, L.PA_DECODE_CUDA_CORES),       # fp32
     ]

@@ -555,3 +555,32 @@ def test_large_groups_in_head_chunks(cuda_device, Hkv, H, D, Bs):
     assert max_abs_err(out, ref1) <= 2e-3
     assert np.array_equal(W.as_oracle_array(gp.t), host)
     _check_status()
+
+
+@pytest.mark.parametrize("H,Hkv,D,Bs", [(71, 1, 128, 16), (232, 8, 128, 16), (12, 2, 64, 32),
+                                        (20, 1, 64, 16), (11, 1, 128, 32)])
+def test_groups_of_any_size_match_oracle(cuda_device, H, Hkv, D, Bs):
+    """Groups that are no multiple of 8 (e.g. 71 query heads on one KV head, or
+    232 on eight: 29 per group) run on the mma.sync kernel as 8-head chunks
+    whose last holds the rest; every head, and no head of the next group, is
+    written ("vllmini", "The CUDA Block Kernel": any num_heads over
+    num_kv_heads).  Lengths around the blocks, every partitioning, the fused
+    append's kernel and the wide CTAs (a whole table)."""
+    lens = [0, 1, Bs - 1, Bs, Bs + 1, 5 * Bs + 3, 300, 40]
+    wl = W.custom("anyg", "bf16", 1, H, Hkv, D, Bs, lens, seed=H * 7 + D + Bs, spare_blocks=3,
+                  interleave=True)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    try:
+        assert B.pa_decode_kernel_choice(gp.h, H) == B.PA_DECODE_TENSOR_CORES
+        bt, ln = device_tables(wl, cuda_device)
+        ref = oracle_decode(wl, pool, q, 0)
+        for pb in (0, 1, 2, wl.max_blocks):
+            out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln, partition_blocks=pb)
+            torch.cuda.synchronize()
+            assert torch.isfinite(out).all(), pb
+            assert max_abs_err(out, ref) <= TOL["bf16"], pb
+        _check_status()
+    finally:
+        gp.close()
