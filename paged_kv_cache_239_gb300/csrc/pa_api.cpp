@@ -220,11 +220,11 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         int sms = 0;
         if (int rc = num_sms_current(&sms)) return rc;
         const int chunk = pa::decode_umma_chunk(G);
-        const long long pairs = (long long)batch * pool->g.Hkv * (G / chunk);
+        const long long pairs = (long long)batch * pool->g.Hkv * ((G + chunk - 1) / chunk);
         if (pairs > INT_MAX)
             return fail(PA_ERR_INVALID_ARG, "%lld (sequence, head group) pairs is too many", pairs);
         // groups served in nc chunks: nc groups of CTAs over the same work
-        const long long nc = G / chunk;
+        const long long nc = (G + chunk - 1) / chunk;
         const long long kv_pairs = (long long)batch * pool->g.Hkv;
         const long long tiles = ((long long)maxb * pool->g.B + 127) / 128;
         const long long units = kv_pairs * (tiles > 1 ? tiles : 1);  // upper bound per group
@@ -705,7 +705,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
         part_o = reinterpret_cast<float*>(ws);
         if (sh.kernel == Kernel::Tcgen05) {
             const size_t S = tc_partial_slots(sh.tc_grid, sh.chunk);
-            const long long pairs = (long long)batch * g.Hkv * (sh.G / sh.chunk);
+            const long long pairs = (long long)batch * g.Hkv * ((sh.G + sh.chunk - 1) / sh.chunk);
             part_ml = reinterpret_cast<float*>(ws + align256(S * g.D * sizeof(float)));
             tc_desc = reinterpret_cast<int4*>(ws + tc_desc_offset(sh.tc_grid, sh.chunk, g.D));
             tc_cut = reinterpret_cast<int4*>(ws + tc_cut_offset(sh.tc_grid, sh.chunk, g.D, pairs));
@@ -747,6 +747,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     p.tc_cut = tc_cut;
     p.gsize = sh.G;
     p.nchunks = (sh.G + sh.chunk - 1) / sh.chunk;
+    p.chunk = sh.chunk;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (!sh.wide && sh.kernel == Kernel::MmaSync && sh.Cmax == 1) {
         // an explicit partition that covers the table: wide CTAs where they fit
@@ -777,7 +778,7 @@ int decode_impl(float* out, const void* q, const pa_pool* pool, int layer,
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     if (sh.combine && sh.kernel == Kernel::Tcgen05) {
         // (fewer pairs than CTAs: most are cut, so every pair gets a CTA group)
-        const long long pairs = (long long)batch * g.Hkv * (sh.G / sh.chunk);
+        const long long pairs = (long long)batch * g.Hkv * ((sh.G + sh.chunk - 1) / sh.chunk);
         e = pa::launch_combine_tc(p, g.D, pairs <= sh.tc_grid, sh.Cmax, s);
         if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     } else if (sh.combine) {

@@ -121,7 +121,7 @@ template <int W>
 static cudaError_t launch_combine_tc_w(const DecodeParams& p, long long groups, int direct,
                                        cudaStream_t s) {
     constexpr int HPC = 8 / W;
-    const int chunk = p.gsize / p.nchunks;
+    const int chunk = p.chunk;
     if (groups <= 0 || chunk <= 0) return cudaSuccess;
     // heads per warp: one, unless a CTA per 8 / W heads would take more than
     // one wave of CTAs (the second wave starts only as the first one ends)

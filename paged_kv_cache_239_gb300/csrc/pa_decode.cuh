@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
     const int warp = threadIdx.x >> 5;
     const int hl = warp / W;
     const int w = warp % W;
-    const int chunk = p.gsize / p.nchunks;
+    const int chunk = p.chunk;                          // heads per chunk (slot width)
     const int per_cta = HPC * rounds;                  // heads of the chunk per CTA
     const int cpp = (chunk + per_cta - 1) / per_cta;   // CTAs per pair
     const long long k = blockIdx.x / cpp;
@@ -654,6 +654,7 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
         d = make_int4(rec.y, rec.z, rec.w, 0);
     }
     int nparts = 0, first = 0, slot0 = 0;
+    int hvalid = 0;     // the chunk's heads (fewer in the last chunk of some groups)
     long long gh0 = 0;  // the chunk's first head in the output
     if (pair >= 0 && pair < npairs) {
         first = d.x;
@@ -669,6 +670,7 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
         const int g = (int)(pair % gpairs);
         gh0 = (pair / gpairs) * p.H + (long long)(g / p.nchunks) * p.gsize +
               (long long)(g % p.nchunks) * chunk;
+        hvalid = min(chunk, p.gsize - (g % p.nchunks) * chunk);
     }
     auto slot_of = [&](int hh, int c) -> long long {
         return ((long long)first + (long long)c * p.nchunks) * 2 * chunk +
@@ -690,7 +692,7 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
                     mv[r][c] = -INFINITY;
                     lv[r][c] = 0.f;
                     ov[r][c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (r < rounds && hh < chunk && nparts == 2) {
+                    if (r < rounds && hh < hvalid && nparts == 2) {
                         const long long sl = slot_of(hh, c);
                         mv[r][c] = ld_dep(p.part_ml + 2 * sl);
                         lv[r][c] = ld_dep(p.part_ml + 2 * sl + 1);
@@ -701,7 +703,7 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int hh = h_first + r * HPC + hl;
-                if (r < rounds && hh < chunk && nparts == 2) {
+                if (r < rounds && hh < hvalid && nparts == 2) {
                     const float M = fmaxf(mv[r][0], mv[r][1]);
                     const float w0 = mv[r][0] == -INFINITY ? 0.f : exp2f(mv[r][0] - M);
                     const float w1 = mv[r][1] == -INFINITY ? 0.f : exp2f(mv[r][1] - M);
@@ -721,7 +723,7 @@ __global__ void __launch_bounds__(256) pa_combine_tc_kernel(const DecodeParams p
     for (int r = 0; r < rounds; ++r) {  // (uniform: combine_head synchronises the CTA)
         const int hh = h_first + r * HPC + hl;  // head within the chunk
         combine_head<D, W>(
-            p, gh0 + hh, hh < chunk ? nparts : 0, [&](int c) { return slot_of(hh, c); }, hl, w);
+            p, gh0 + hh, hh < hvalid ? nparts : 0, [&](int c) { return slot_of(hh, c); }, hl, w);
     }
 }
 

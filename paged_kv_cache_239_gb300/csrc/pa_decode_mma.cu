@@ -60,6 +60,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p_in, const void* tmaps, int D
     DecodeParams p = p_in;
     p.gsize = Gtot;
     p.nchunks = (Gtot + G - 1) / G;
+    p.chunk = G;
     if (D == 64) {
         if (B == 16) return launch_mma_g<64, 16, kMmaWarps, kMmaStages<64>>(p, tm, G, s);
         if (B == 32) return launch_mma_g<64, 32, kMmaWarps, kMmaStages<64>>(p, tm, G, s);

@@ -73,6 +73,7 @@ cudaError_t launch_decode_mma_wide(const DecodeParams& p_in, const void* tmaps, 
     DecodeParams p = p_in;
     p.gsize = Gtot;
     p.nchunks = (Gtot + G - 1) / G;
+    p.chunk = G;
     if (D == 64) {
         if (B == 16) return launch_wide_g<64, 16>(p, tm, G, s);
         if (B == 32) return launch_wide_g<64, 32>(p, tm, G, s);

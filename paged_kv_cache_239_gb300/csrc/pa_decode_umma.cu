@@ -57,6 +57,10 @@ cudaError_t launch_g(const DecodeParams& p, const CUtensorMap* tm, int G, cudaSt
 int decode_umma_chunk(int G) {
     if (G <= 0 || G % 16 != 0) return 0;
     if (G % 128 == 0) return 128;
+    // 80, 96 and 112 heads: one 128-head chunk, the rows past the group
+    // computed and dropped (one K/V pass at the 128-head rate, instead of five,
+    // two or seven sibling chunks)
+    if (G > 64 && G < 128) return 128;
     if (G % 64 == 0) return 64;
     if (G % 48 == 0) return 48;
     if (G % 32 == 0) return 32;
@@ -74,7 +78,8 @@ cudaError_t launch_decode_umma(const DecodeParams& p_in, const void* tmaps, int 
     if (G == 0) return cudaErrorNotSupported;
     DecodeParams p = p_in;
     p.gsize = Gtot;
-    p.nchunks = Gtot / G;
+    p.nchunks = (Gtot + G - 1) / G;
+    p.chunk = G;
     if (B == 16) return launch_g<16>(p, tm, G, s);
     if (B == 32) return launch_g<32>(p, tm, G, s);
     return cudaErrorNotSupported;

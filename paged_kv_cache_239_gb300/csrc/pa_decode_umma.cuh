@@ -829,11 +829,15 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
         int nb0 = -1, nb1 = -1;
         if (have) part_blocks(it, 0, nb0, nb1);
         while (!stop && have) {
+            // this thread's head is one of the chunk's (a group of 80-112 heads
+            // fills 128 rows: the rows past it are computed and not written)
+            const bool own = hrow < p.gsize - it.hc * G;
             if (it.ntiles == 0) {  // empty context: output 0 (always a whole piece)
                 const long long head0 = (long long)it.b * p.H + it.hbase;
                 float4* o4 = reinterpret_cast<float4*>(p.out + (head0 + hrow) * 128 + c0);
 #pragma unroll
-                for (int j = 0; j < C::TP / 4; ++j) o4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < C::TP / 4; ++j)
+                    if (own) o4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                 have = umma_walk_next<B, G>(p, w, it);
                 if (have) part_blocks(it, 0, nb0, nb1);
                 continue;
@@ -978,7 +982,8 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                 uint32_t v[C::TP];
                 tmem_ld_cols<C::TP>(trow + C::O_COL + c0, v);
                 tmem_wait_ld();
-                if (it.whole) {
+                if (!own) {
+                } else if (it.whole) {
                     const float inv = L > 0.f ? 1.f / L : 0.f;
                     const long long head0 = (long long)it.b * p.H + it.hbase;
                     float4* o4 = reinterpret_cast<float4*>(p.out + (head0 + hrow) * 128 + c0);

@@ -56,9 +56,11 @@ struct DecodeParams {
     // tensor-core kernel only: which of the tensor maps' outer dimensions
     // (2, 3, 4) index the physical block, the layer and the kv head
     int tma_slot_blk, tma_slot_layer, tma_slot_head;
-    // tensor-core kernel only: the group (num_heads / Hkv) is served in
-    // `nchunks` chunks of the kernel's compile-time G heads (1 unless G > 16)
-    int gsize, nchunks;
+    // tensor-core kernels only: the group (num_heads / Hkv) is served in
+    // `nchunks` chunks of `chunk` heads (the kernel's compile-time G); the last
+    // chunk holds the rest of a group that is no multiple of it, and the
+    // tcgen05 kernel's partial slots are `chunk` heads wide
+    int gsize, nchunks, chunk;
     // tcgen05 kernel only: its persistent grid, and (with tc_grid > 1) one
     // int4 per (sequence, head group) {first CTA, pieces, slot of the first
     // piece} that tells the combine where the pieces of a split context are;

@@ -26,7 +26,8 @@ def _status_clear():
 
 @pytest.mark.parametrize("Hkv,H,Bs", [(1, 16, 16), (2, 32, 16), (1, 64, 32), (2, 128, 16),
                                        (1, 48, 16), (1, 96, 32), (1, 128, 16), (1, 192, 32),
-                                       (1, 128, 32), (2, 256, 16), (1, 256, 32)])
+                                       (1, 128, 32), (2, 256, 16), (1, 256, 32),
+                                       (1, 80, 16), (2, 224, 32)])
 def test_groups_match_oracle_every_partition(cuda_device, Hkv, H, Bs):
     wl = W.custom("tc", "bf16", 2, H, Hkv, 128, Bs, LENS, seed=H + Bs, spare_blocks=3,
                   interleave=True)
@@ -262,6 +263,7 @@ def test_graph_replays_match(cuda_device):
     ([1], 64, 1),                     # one unit: a single CTA has work
     ([5000, 0, 3, 9000, 0], 128, 1),  # one 128-head chunk (heads on the rows), empty contexts
     ([5000, 0, 3, 9000, 0], 192, 1),  # three 64-head chunks, empty contexts
+    ([700, 1500, 0, 129, 2047], 112, 1),  # 112 heads in one 128-head chunk (16 rows dropped)
     ([700, 1500, 0, 129, 2047], 48, 1),   # three 16-head chunks
     ([33000, 17, 128], 32, 2),        # long + short, two KV heads
 ])
