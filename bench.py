@@ -16,7 +16,7 @@ After the headline line's own measurements, the same run measures the other
 workloads one at a time (graph-timed, each with its clock record) and adds them
 to the line as "workloads": the batched gather on the large-batch pool, the
 mini-infer-shaped 24-layer step, the long-context call, the large-batch lengths
-with 16-, 32- and 64-query-head groups (the tcgen05 kernel), and the append +
+with 16- to 128-query-head groups (the tcgen05 kernel), and the append +
 decode loop with the free stack on the device.  --no-workloads skips them.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
@@ -762,7 +762,7 @@ def run_extra_workloads(args, B, torch, W, dev):
                             "K/V per layer below L2; consecutive layers read disjoint slices"))
     res.append(measure_step(B, torch, W, dev, W.named(4), "long_context_bf16",
                             "one layer: every call re-reads the same 1.35 GB (10x L2)"))
-    for H, Hkv in ((32, 2), (32, 1), (48, 1), (64, 1), (128, 1)):
+    for H, Hkv in ((32, 2), (32, 1), (48, 1), (64, 1), (96, 1), (128, 1)):
         wl = W.named(3)
         wl.num_heads, wl.num_kv_heads, wl.num_layers = H, Hkv, 16 if Hkv == 1 else 8
         res.append(measure_step(B, torch, W, dev, wl,
