@@ -20,7 +20,8 @@
 //  * warp 0 (K producer): block-table walk (entries loaded a tile ahead, a
 //    piece's first ones and its appended row a piece ahead), the fused
 //    append's K row, q of each piece into a swizzled K-major tile (2-D
-//    tensor-map TMA, two buffers), and 5-D tensor-map TMA loads of 128-token
+//    tensor-map TMA, two buffers; one for 128-head chunks), and 5-D
+//    tensor-map TMA loads of 128-token
 //    K tiles (8 boxes of 16 rows per 64-column half, SWIZZLE_128B) into the K
 //    ring;
 //  * warp 2 (V producer): computes the CTA's share at start; the same walk for
@@ -46,6 +47,8 @@
 // by the softmax warps and read from there as the A operand; a softmax thread
 // then owns one head's row (16 warps: 4 lane quarters of heads x 4 quarters of
 // the tile's tokens, which agree on the running max at a named barrier).
+// Groups of 80-112 heads fill one 128-head chunk; the rows past the group are
+// computed and not written.
 // Every wait is bounded (PA_STATUS_TIMEOUT); the roles then stop together,
 // wait for their copies and MMAs in flight, and TMEM is freed.
 #pragma once
