@@ -324,18 +324,22 @@ struct UmmaCfg {
 };
 
 // Work schedule: equal shares of 128-token tiles per persistent CTA (see
-// pa_schedule.cuh), each (sequence, head group) pair charged two extra units
-// for a piece's fixed cost (q, the first tile's maximum, the output, the next
-// copies' latency; GB300, once a piece's inputs were loaded a piece ahead: 2
-// ahead of 3 by 1-2 % at 16 and 32 heads, level at 64, 0 and 1 slower).
-constexpr int kUmmaPieceUnits = 2;
+// pa_schedule.cuh), each (sequence, head group) pair charged extra units for a
+// piece's fixed cost (q, the first tile's maximum, the output, the next
+// copies' latency).  GB300, once a piece's inputs were loaded a piece ahead:
+// two units ahead of three by 1-2 % at 16 and 32 heads, and by 1.5 % at 64
+// (0 and 1 slower); three for 128-head chunks, whose piece epilogue reads a
+// 128 x 256 O^T (128 heads: 74.7 us per call against 76.5 with two and 75.7
+// with four).
+template <int G>
+constexpr int kUmmaPieceUnits = G == 128 ? 3 : 2;
 using UItem = SPiece;
 using UWalk = SWalk;
 
-template <int B>
+template <int B, int G>
 __device__ __forceinline__ void umma_schedule(const DecodeParams& p, unsigned char* sched,
                                               int lane) {
-    sched_compute<B, 128, kUmmaPieceUnits>(p, sched, lane);
+    sched_compute<B, 128, kUmmaPieceUnits<G>>(p, sched, lane);
 }
 template <int B>
 __device__ __forceinline__ void umma_walk_begin(const DecodeParams& p, const unsigned char* sched,
@@ -344,7 +348,7 @@ __device__ __forceinline__ void umma_walk_begin(const DecodeParams& p, const uns
 }
 template <int B, int G>
 __device__ __forceinline__ bool umma_walk_next(const DecodeParams& p, UWalk& w, UItem& it) {
-    return sched_walk_next<B, 128, kUmmaPieceUnits, G>(p, w, it);
+    return sched_walk_next<B, 128, kUmmaPieceUnits<G>, G>(p, w, it);
 }
 
 // Non-blocking test of an mbarrier phase (try_wait may suspend the thread for
@@ -470,7 +474,7 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
     // (nothing above reads what the previous kernel may have written: the
     // set-up overlaps its tail)
     pdl_wait();
-    if (warp == 2) umma_schedule<B>(p, ctrl + C::SCHED_OFF, lane);
+    if (warp == 2) umma_schedule<B, G>(p, ctrl + C::SCHED_OFF, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
