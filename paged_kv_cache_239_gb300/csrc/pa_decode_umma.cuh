@@ -327,10 +327,9 @@ struct UmmaCfg {
 // pa_schedule.cuh), each (sequence, head group) pair charged extra units for a
 // piece's fixed cost (q, the first tile's maximum, the output, the next
 // copies' latency).  GB300, once a piece's inputs were loaded a piece ahead:
-// two units ahead of three by 1-2 % at 16 and 32 heads, and by 1.5 % at 64
-// (0 and 1 slower); three for 128-head chunks, whose piece epilogue reads a
-// 128 x 256 O^T (128 heads: 74.7 us per call against 76.5 with two and 75.7
-// with four).
+// two units ahead of three by 1-2 % at 16, 32 and 48 heads, and by 1.5 % at
+// 64 (0 and 1 slower); three for 128-head chunks (128 heads: 74.7 us per call
+// against 76.5 with two and 75.7 with four).
 template <int G>
 constexpr int kUmmaPieceUnits = G == 128 ? 3 : 2;
 using UItem = SPiece;
