@@ -618,7 +618,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     if not args.no_workloads and world == 1:
         # the other workloads, each measured alone after the headline (the
         # gather on this pool first, then the pool is freed)
-        extra = [measure_gather(B, torch, wl, pool, h, bt, lens, dev, layers=4)]
+        extra = [measure_gather(B, torch, wl, pool, h, bt, lens, dev,
+                                layers=min(4, wl.num_layers))]
         B.pa_pool_destroy(h)
         h = None
         del pool, qs, ks, vs, outs, ws, sets, graph, step_graph
