@@ -83,13 +83,13 @@ def decode_flops(wl) -> int:
 # DRAM bytes (read + write) of one layer's pa_write_kv_and_decode call on this
 # workload, one ncu capture per kernel on the 1-layer pool (--metrics
 # dram__bytes_read.sum,dram__bytes_write.sum, -k one kernel, -c 2):
-# pa_decode_mma_kernel with the fused append 2,231,368,704 read + 6,226,688
-# written, pa_combine_kernel 9,847,808 read + 0 written; see profiles/.  Valid
+# pa_decode_mma_kernel with the fused append 2,231,443,968 read + 6,390,784
+# written, pa_combine_kernel 9,848,064 read + 0 written; see profiles/.  Valid
 # only for the sources they were taken from (the kernels, the shared device
 # code, and the dispatch / partition choice in pa_api.cpp).
 DECODE_TRAFFIC = {
-    "bytes_per_launch": 2231368704 + 6226688 + 9847808,
-    "sources_sha256": "fc8af0715892f26b216b2a3d0007305b8fb97b158d562aff247918315850f5b5",
+    "bytes_per_launch": 2231443968 + 6390784 + 9848064,
+    "sources_sha256": "e8553c7561bc99f0d93bcf519ca31ec7d25ef9f18a7ddd6e270573826241a3c1",
 }
 DECODE_SOURCES = ["pa_decode_mma.cuh", "pa_decode_mma.cu", "pa_decode.cuh", "pa_device.cuh",
                   "pa_internal.h", "pa_api.cpp", "pa_fused_append.cuh"]

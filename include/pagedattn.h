@@ -152,8 +152,9 @@ PA_API int pa_pool_destroy(pa_pool* pool);
  * each K/V tile through L2, the last chunk holding the rest of a group that
  * is no multiple of 8), any multiple of 16 on the
  * tcgen05 kernel (bf16 pools, head_dim 128; chunks of 128, 64, 48, 32 or 16
- * heads, groups of 80, 96 and 112 in one 128-head chunk), 1, 2, 4 or 8 on
- * the CUDA-core kernel.  Other shapes: PA_ERR_UNSUPPORTED.
+ * heads, groups of 80, 96 and 112 in one 128-head chunk), and of any size
+ * on the CUDA-core kernel (every dtype; head chunks of a power of two up to 8,
+ * the heads past the group masked).  Other shapes: PA_ERR_UNSUPPORTED.
  *
  * Which decode kernel a pool's decode calls use.  PA_DECODE_AUTO (default):
  * for bf16 pools with head_dim 128 the tcgen05 kernel for groups that are

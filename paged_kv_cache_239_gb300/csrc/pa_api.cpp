@@ -163,8 +163,7 @@ int pick_kernel(const pa_pool* pool, int G, Kernel* k) {
     if (!cuda_ok && !mma_ok && !umma_ok)
         return fail(PA_ERR_UNSUPPORTED,
                     "no decode kernel for dtype=%d head_dim=%d block_size=%d group=%d "
-                    "(built: head_dim 64/128, block_size 16/32; any group for bf16 pools, "
-                    "1/2/4/8 for fp32 pools)",
+                    "(built: head_dim 64/128, block_size 16/32, any group)",
                     g.dtype, g.D, g.B, G);
     switch (pool->decode_kernel) {
         case PA_DECODE_CUDA_CORES:
@@ -242,7 +241,8 @@ int resolve_decode_shape(const pa_pool* pool, int batch, int num_heads, int maxb
         out->combine = grid > 1;
         return PA_OK;
     }
-    const int chunk = kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G) : G;
+    const int chunk =
+        kernel == Kernel::MmaSync ? pa::decode_mma_chunk(G) : pa::decode_cc_chunk(G);
     const long long nchunks = (G + chunk - 1) / chunk;  // (mma.sync: a ragged last chunk)
     int pb = partition_blocks;
     bool wide = false;
@@ -281,7 +281,7 @@ bool decode_supported(int dtype, int D, int B, int G) {
     if (dtype != 0 && dtype != 1) return false;
     if (D != 64 && D != 128) return false;
     if (B != 16 && B != 32) return false;
-    return G == 1 || G == 2 || G == 4 || G == 8;
+    return decode_cc_chunk(G) > 0;  // (any group: chunks of a power of two)
 }
 }  // namespace pa
 

@@ -163,13 +163,20 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     const int rg = lane / C::LR;  // row group
     const int jl = lane % C::LR;  // position within the row
 
-    // ---- CTA coordinates: KV head fastest, then sequence, partition slowest ----
+    // ---- CTA coordinates: head chunk fastest, then KV head, then sequence,
+    //      partition slowest.  A group that is no power of two up to 8 runs
+    //      in chunks of G heads (the next power of two, or 8), the heads past
+    //      the group masked: zero q, nothing written. ----
     int idx = blockIdx.x;
+    const int hc = idx % p.nchunks;
+    idx /= p.nchunks;
     const int nbh = p.batch * p.Hkv;
     const int c = idx / nbh;
     idx %= nbh;
     const int kvh = idx % p.Hkv;
     const int b = idx / p.Hkv;
+    const int hbase = kvh * p.gsize + hc * G;  // first query head of this CTA in the sequence
+    const int gact = min(G, p.gsize - hc * G);
 
     // The first 32 block ids of this warp's share of the partition depend only
     // on the partition index (the table row holds maxb entries): their load
@@ -286,11 +293,11 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     // ---- q of the G heads, this lane's slice, scaled into the log2 domain ----
     float2 qf[G][E2];
     {
-        const T* qb = reinterpret_cast<const T*>(p.q) + ((long long)b * p.H + kvh * G) * D;
+        const T* qb = reinterpret_cast<const T*>(p.q) + ((long long)b * p.H + hbase) * D;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            float2 f[4];
-            load_row_slice<T, C::NV, C::LR>(qb + h * D, jl, f);
+            float2 f[4] = {};
+            if (h < gact) load_row_slice<T, C::NV, C::LR>(qb + h * D, jl, f);
 #pragma unroll
             for (int i = 0; i < E2; ++i)
                 qf[h][i] = make_float2(f[i].x * p.qscale, f[i].y * p.qscale);
@@ -458,8 +465,8 @@ __global__ void __launch_bounds__(NW * 32) pa_decode_kernel(const DecodeParams p
     __syncthreads();
 
     // ---- merge the NW warps (log-sum-exp) and write ----
-    const long long head0 = (long long)b * p.H + kvh * G;
-    for (int t = threadIdx.x; t < G * D; t += NW * 32) {
+    const long long head0 = (long long)b * p.H + hbase;
+    for (int t = threadIdx.x; t < gact * D; t += NW * 32) {
         const int h = t / D;
         const int d = t % D;
         float M = -INFINITY;

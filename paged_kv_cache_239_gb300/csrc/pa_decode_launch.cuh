@@ -43,7 +43,7 @@ cudaError_t launch_decode_inst(const DecodeParams& p, cudaStream_t stream) {
             done_mask |= bit;
         }
     }
-    const long long grid = (long long)p.batch * p.Hkv * p.Cmax;
+    const long long grid = (long long)p.batch * p.Hkv * p.nchunks * p.Cmax;
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(kDecodeWarps * 32), C::SMEM_BYTES, stream,
@@ -62,7 +62,13 @@ cudaError_t launch_decode_g(const DecodeParams& p, int G, cudaStream_t s) {
 }
 
 template <typename T>
-cudaError_t launch_decode_typed(const DecodeParams& p, int D, int B, int G, cudaStream_t s) {
+cudaError_t launch_decode_typed(const DecodeParams& p_in, int D, int B, int Gtot, cudaStream_t s) {
+    const int G = decode_cc_chunk(Gtot);
+    if (G == 0) return cudaErrorNotSupported;
+    DecodeParams p = p_in;
+    p.gsize = Gtot;
+    p.nchunks = (Gtot + G - 1) / G;
+    p.chunk = G;
     if (D == 64) {
         if (B == 16) return launch_decode_g<T, 64, 16>(p, G, s);
         if (B == 32) return launch_decode_g<T, 64, 32>(p, G, s);

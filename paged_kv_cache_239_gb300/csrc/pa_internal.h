@@ -109,6 +109,16 @@ struct GatherParams {
 cudaError_t launch_decode_bf16(const DecodeParams& p, int D, int B, int G, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeParams& p, int D, int B, int G, cudaStream_t s);
 bool decode_supported(int dtype, int D, int B, int G);
+// The CUDA-core kernel's head chunk for group G: G itself for 1, 2, 4, 8;
+// the next power of two below 8, 8 above (the last chunk masks the heads past
+// the group); 0 for G < 1.
+inline int decode_cc_chunk(int G) {
+    if (G < 1) return 0;
+    if (G > 8) return 8;
+    int c = 1;
+    while (c < G) c <<= 1;
+    return c;
+}
 
 // Tensor-core kernel for bf16 pools; `tmaps` points to two CUtensorMap (K, V).
 // Groups of up to 8 or exactly 16 heads run in one CTA per KV head; larger

@@ -167,9 +167,14 @@ def test_decode_host_checks(pa_lib):
             assert e.value.code == code, (bad, e.value)
         # batch 0 is a no-op that needs no device
         call(batch=0)
-        # an fp32 pool runs only on the CUDA-core kernel: groups 1, 2, 4, 8
+        # an fp32 pool runs only on the CUDA-core kernel (any group: a group of
+        # 3 fails only for want of a workspace); the tensor-core kernels refuse it
         h32 = _pool(pa_lib, nb=8, L=2, Hkv=2, B=16, D=64, dtype=0)
         try:
+            with pytest.raises(pa_lib.PagedAttnError) as e:
+                call(pool=h32, H=6)
+            assert e.value.code == pa_lib.PA_ERR_WORKSPACE
+            pa_lib.pa_pool_set_decode_kernel(h32, pa_lib.PA_DECODE_TENSOR_CORES)
             with pytest.raises(pa_lib.PagedAttnError) as e:
                 call(pool=h32, H=6)
             assert e.value.code == pa_lib.PA_ERR_UNSUPPORTED
@@ -262,13 +267,10 @@ def test_decode_kernel_choice_query(pa_lib):
         h = _pool(pa_lib, Hkv=Hkv, D=D, dtype=dtype)
         try:
             assert L.pa_decode_kernel_choice(h, H) == want, (Hkv, D, dtype, H)
+            # the CUDA-core kernel serves every group (power-of-two head chunks,
+            # the heads past the group masked)
             L.pa_pool_set_decode_kernel(h, L.PA_DECODE_CUDA_CORES)
-            if H // Hkv in (1, 2, 4, 8):
-                assert L.pa_decode_kernel_choice(h, H) == L.PA_DECODE_CUDA_CORES
-            else:
-                with pytest.raises(L.PagedAttnError) as e:
-                    L.pa_decode_kernel_choice(h, H)
-                assert e.value.code == L.PA_ERR_UNSUPPORTED
+            assert L.pa_decode_kernel_choice(h, H) == L.PA_DECODE_CUDA_CORES
             L.pa_pool_set_decode_kernel(h, L.PA_DECODE_TCGEN05)
             if want == L.PA_DECODE_TCGEN05:
                 assert L.pa_decode_kernel_choice(h, H) == L.PA_DECODE_TCGEN05

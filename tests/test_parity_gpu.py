@@ -385,9 +385,7 @@ def test_tokens_of_bad_blocks_get_no_weight(cuda_device, H, Hkv):
         ref = oracle_decode(wl, pool, q, 0, tables=ref_tables, lens=ref_lens)
         bt = torch.from_numpy(tables).to(cuda_device)
         ln = torch.from_numpy(wl.context_lens).to(cuda_device)
-        kinds = [B.PA_DECODE_AUTO, B.PA_DECODE_TENSOR_CORES]
-        if H // Hkv <= 8:  # (the CUDA-core kernel's groups)
-            kinds.append(B.PA_DECODE_CUDA_CORES)
+        kinds = [B.PA_DECODE_AUTO, B.PA_DECODE_TENSOR_CORES, B.PA_DECODE_CUDA_CORES]
         if B.pa_decode_kernel_choice(gp.h, H) == B.PA_DECODE_TCGEN05:
             kinds.append(B.PA_DECODE_TCGEN05)
         torch.cuda.synchronize()
@@ -498,7 +496,7 @@ def test_bounded_wait_times_out_into_status(cuda_device):
 @pytest.mark.parametrize("D,Bs", [(128, 16), (64, 32)])
 def test_group_of_16_on_tensor_cores(cuda_device, D, Bs):
     """128 query heads over 8 KV heads style grouping (G = 16): two 8-head mma
-    tiles per KV head; the CUDA-core kernel refuses it."""
+    tiles per KV head; the CUDA-core kernel serves it as two 8-head chunks."""
     wl = W.custom("g16", "bf16", 2, 32, 2, D, Bs, [1, Bs, 5 * Bs + 3, 700, 0], seed=16,
                   spare_blocks=3, interleave=True)
     pool = W.make_pool(wl)
@@ -510,9 +508,9 @@ def test_group_of_16_on_tensor_cores(cuda_device, D, Bs):
         out = gpu_decode(gp, q.to(cuda_device), 1, bt, ln, partition_blocks=pb)
         assert max_abs_err(out, ref) <= 2e-3, pb
     B.pa_pool_set_decode_kernel(gp.h, B.PA_DECODE_CUDA_CORES)
-    with pytest.raises(B.PagedAttnError) as e:
-        gpu_decode(gp, q.to(cuda_device), 1, bt, ln)
-    assert e.value.code == B.PA_ERR_UNSUPPORTED
+    for pb in (0, 1, wl.max_blocks):
+        out = gpu_decode(gp, q.to(cuda_device), 1, bt, ln, partition_blocks=pb)
+        assert max_abs_err(out, ref) <= 2e-3, pb
     _check_status()
 
 
@@ -576,11 +574,40 @@ def test_groups_of_any_size_match_oracle(cuda_device, H, Hkv, D, Bs):
         assert B.pa_decode_kernel_choice(gp.h, H) == B.PA_DECODE_TENSOR_CORES
         bt, ln = device_tables(wl, cuda_device)
         ref = oracle_decode(wl, pool, q, 0)
-        for pb in (0, 1, 2, wl.max_blocks):
+        for kind in (B.PA_DECODE_AUTO, B.PA_DECODE_CUDA_CORES):
+            B.pa_pool_set_decode_kernel(gp.h, kind)
+            for pb in (0, 1, 2, wl.max_blocks):
+                out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln, partition_blocks=pb)
+                torch.cuda.synchronize()
+                assert torch.isfinite(out).all(), (kind, pb)
+                assert max_abs_err(out, ref) <= TOL["bf16"], (kind, pb)
+        _check_status()
+    finally:
+        gp.close()
+
+
+@pytest.mark.parametrize("H,Hkv,D,Bs", [(6, 2, 64, 16), (10, 2, 128, 32), (24, 2, 64, 16),
+                                        (3, 1, 128, 16)])
+def test_fp32_pools_any_group_match_oracle(cuda_device, H, Hkv, D, Bs):
+    """fp32 pools run on the CUDA-core kernel, which serves any group in
+    power-of-two head chunks (3 heads in a 4-head chunk, 5 in an 8-head one,
+    12 as 8 + 4 of two 8-head chunks), the heads past the group masked; within
+    the fp32 tolerance of the oracle at every partitioning."""
+    lens = [0, 1, Bs - 1, Bs, Bs + 1, 4 * Bs + 5, 230]
+    wl = W.custom("f32g", "f32", 1, H, Hkv, D, Bs, lens, seed=H * 11 + D, spare_blocks=2,
+                  interleave=True)
+    pool = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    gp = GpuPool(wl, pool.to(cuda_device))
+    try:
+        assert B.pa_decode_kernel_choice(gp.h, H) == B.PA_DECODE_CUDA_CORES
+        bt, ln = device_tables(wl, cuda_device)
+        ref = oracle_decode(wl, pool, q, 0)
+        for pb in (0, 1, 3, wl.max_blocks):
             out = gpu_decode(gp, q.to(cuda_device), 0, bt, ln, partition_blocks=pb)
             torch.cuda.synchronize()
             assert torch.isfinite(out).all(), pb
-            assert max_abs_err(out, ref) <= TOL["bf16"], pb
+            assert max_abs_err(out, ref) <= TOL["f32"], pb
         _check_status()
     finally:
         gp.close()

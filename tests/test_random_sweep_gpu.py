@@ -93,7 +93,7 @@ def _run_case(cuda_device, i, rng, dtype, D, Bs, Hkv, G, L, lens, layout):
     keep, h = _make_pool_handle(wl, fused, layout, cuda_device)
     try:
         kinds = [B.PA_DECODE_AUTO]
-        if dtype == "bf16" and G in (1, 2, 4, 8):
+        if dtype == "bf16":
             kinds.append(B.PA_DECODE_CUDA_CORES)
         if dtype == "bf16":
             kinds.append(B.PA_DECODE_TENSOR_CORES)
@@ -116,12 +116,6 @@ def _run_case(cuda_device, i, rng, dtype, D, Bs, Hkv, G, L, lens, layout):
             torch.cuda.synchronize()
             err = max_abs_err(out, ref)
             assert err <= TOL[dtype], (i, kind, dtype, D, Bs, Hkv, G, layout, pb, err)
-        if dtype == "bf16" and G not in (1, 2, 4, 8):
-            B.pa_pool_set_decode_kernel(h, B.PA_DECODE_CUDA_CORES)
-            with pytest.raises(B.PagedAttnError) as e:
-                B.pa_decode_attention_partitioned(out, qd, h, layer, bt, wl.max_blocks, ln,
-                                                  wl.batch, Bs, H, Hkv, D, wl.scale, pb, ws, need)
-            assert e.value.code == B.PA_ERR_UNSUPPORTED
         B.pa_pool_set_decode_kernel(h, B.PA_DECODE_AUTO)
         need = B.pa_decode_workspace_size(h, wl.batch, H, wl.max_blocks, pb)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=cuda_device)
