@@ -30,6 +30,27 @@ class GpuPool:
         self.close()
 
 
+def pool_in_layout(wl, fused, layout, dev):
+    """Device tensors holding the fused pool's rows in `layout` -- "fused"
+    [n, 2, L, Hkv, B, D], "separate" K and V caches [n, Hkv, B, D] (one layer),
+    "layer_major" K and V caches [L, n, Hkv, B, D] -- and a handle over them."""
+    tile = wl.block_size * wl.head_dim
+    if layout == "fused":
+        t = fused.to(dev)
+        return (t,), B.pa_pool_create(t, wl.num_blocks, wl.num_layers, wl.num_kv_heads,
+                                      wl.block_size, wl.head_dim, t.dtype)
+    if layout == "separate":
+        kc, vc = fused[:, 0, 0].contiguous().to(dev), fused[:, 1, 0].contiguous().to(dev)
+        sb, sl = wl.num_kv_heads * tile, 0
+    else:
+        kc = fused[:, 0].permute(1, 0, 2, 3, 4).contiguous().to(dev)
+        vc = fused[:, 1].permute(1, 0, 2, 3, 4).contiguous().to(dev)
+        sb, sl = wl.num_kv_heads * tile, wl.num_blocks * wl.num_kv_heads * tile
+    h = B.pa_pool_create_strided(kc, vc, sb, sl, tile, wl.num_blocks, wl.num_layers,
+                                 wl.num_kv_heads, wl.block_size, wl.head_dim, kc.dtype)
+    return (kc, vc), h
+
+
 def device_tables(wl, device):
     bt = torch.from_numpy(np.ascontiguousarray(wl.block_tables)).to(device)
     lens = torch.from_numpy(np.ascontiguousarray(wl.context_lens)).to(device)

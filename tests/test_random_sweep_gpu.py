@@ -11,7 +11,7 @@ import torch
 import oracle
 from paged_kv_cache_239_gb300 import binding as B
 from paged_kv_cache_239_gb300 import workloads as W
-from gpu_helpers import TOL, max_abs_err
+from gpu_helpers import TOL, max_abs_err, pool_in_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -36,25 +36,6 @@ def _case(i):
     if layout == "separate":
         L = 1
     return rng, dtype, D, Bs, Hkv, G, L, lens, layout
-
-
-def _make_pool_handle(wl, fused, layout, dev):
-    """Device tensors holding the fused pool's rows in `layout`, and a handle."""
-    tile = wl.block_size * wl.head_dim
-    if layout == "fused":
-        t = fused.to(dev)
-        return (t,), B.pa_pool_create(t, wl.num_blocks, wl.num_layers, wl.num_kv_heads,
-                                      wl.block_size, wl.head_dim, t.dtype)
-    if layout == "separate":
-        kc, vc = fused[:, 0, 0].contiguous().to(dev), fused[:, 1, 0].contiguous().to(dev)
-        sb, sl = wl.num_kv_heads * tile, 0
-    else:
-        kc = fused[:, 0].permute(1, 0, 2, 3, 4).contiguous().to(dev)
-        vc = fused[:, 1].permute(1, 0, 2, 3, 4).contiguous().to(dev)
-        sb, sl = wl.num_kv_heads * tile, wl.num_blocks * wl.num_kv_heads * tile
-    h = B.pa_pool_create_strided(kc, vc, sb, sl, tile, wl.num_blocks, wl.num_layers,
-                                 wl.num_kv_heads, wl.block_size, wl.head_dim, kc.dtype)
-    return (kc, vc), h
 
 
 def _large_case(i):
@@ -90,7 +71,7 @@ def _run_case(cuda_device, i, rng, dtype, D, Bs, Hkv, G, L, lens, layout):
                   steps=1)
     fused = W.make_pool(wl)
     q = W.make_queries(wl, 1)[0]
-    keep, h = _make_pool_handle(wl, fused, layout, cuda_device)
+    keep, h = pool_in_layout(wl, fused, layout, cuda_device)
     try:
         kinds = [B.PA_DECODE_AUTO]
         if dtype == "bf16":

@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import TOL, GpuPool, device_tables, gpu_decode, max_abs_err, oracle_decode
+from gpu_helpers import (TOL, GpuPool, device_tables, gpu_decode, max_abs_err, oracle_decode,
+                         pool_in_layout)
 from paged_kv_cache_239_gb300 import binding as B
 from paged_kv_cache_239_gb300 import workloads as W
 
@@ -142,3 +143,65 @@ def test_wide_one_wave_boundary(cuda_device):
     assert max_abs_err(out, oracle_decode(wl, pool, q, 0)) <= TOL["bf16"]
     assert B.pa_get_status() == 0
     gp.close()
+
+
+@pytest.mark.parametrize("layout", ["separate", "layer_major"])
+@pytest.mark.parametrize("D,Bs,G", [(64, 16, 8), (128, 32, 16), (128, 16, 5)])
+def test_wide_strided_layouts_match_oracle(cuda_device, layout, D, Bs, G):
+    """Separate K and V caches (one layer) and layer-major caches [L, n, Hkv,
+    B, D]: a wide CTA's tensor maps take the caches' own strides.  The decode,
+    then the fused append -- whose row lands bit-exactly where the oracle puts
+    it in the same layout -- and the decode over the new token."""
+    Hkv = 2
+    H = Hkv * G
+    maxb = wide_max_blocks(D)
+    L = 1 if layout == "separate" else 3
+    wl = W.custom("wide_strided", "bf16", L, H, Hkv, D, Bs, _lens(Bs, maxb - 1, 7 * D + G),
+                  seed=3 * G + D, spare_blocks=3, interleave=True, max_blocks=maxb, steps=1)
+    fused = W.make_pool(wl)
+    q = W.make_queries(wl, 1)[0]
+    (kc, vc), h = pool_in_layout(wl, fused, layout, cuda_device)
+    try:
+        B.pa_pool_set_decode_kernel(h, B.PA_DECODE_TENSOR_CORES)
+        assert B.pa_decode_partition_blocks(h, wl.batch, H, maxb) == maxb
+        assert B.pa_decode_workspace_size(h, wl.batch, H, maxb, 0) == 0
+        layer = L - 1
+        bt, ln = device_tables(wl, cuda_device)
+        qd = q.to(cuda_device)
+        ref = oracle.decode_attention(W.as_oracle_array(q), W.as_oracle_array(fused), layer,
+                                      wl.block_tables, wl.context_lens, H, wl.scale)
+        out = torch.full((wl.batch, H, D), float("nan"), device=cuda_device)
+        B.pa_decode_attention_partitioned(out, qd, h, layer, bt, maxb, ln, wl.batch, Bs, H, Hkv,
+                                          D, wl.scale, 0, None, 0)
+        torch.cuda.synchronize()
+        assert max_abs_err(out, ref) <= TOL["bf16"], layout
+
+        k, v = W.make_new_tokens(wl, 1)
+        tables = wl.block_tables.copy()
+        for b, n in enumerate(wl.context_lens):
+            if n % Bs == 0:
+                tables[b, n // Bs] = wl.free_stack.pop()
+        lens1 = wl.context_lens + 1
+        out = torch.full((wl.batch, H, D), float("nan"), device=cuda_device)
+        B.pa_write_kv_and_decode(out, qd, h, layer, k[0].to(cuda_device), v[0].to(cuda_device),
+                                 torch.from_numpy(wl.context_lens.copy()).to(cuda_device),
+                                 torch.from_numpy(tables).to(cuda_device), maxb,
+                                 torch.from_numpy(lens1).to(cuda_device), wl.batch, Bs, H, Hkv,
+                                 D, wl.scale, 0, None, 0)
+        host = W.as_oracle_array(fused).copy()
+        oracle.write_kv(host, layer, W.as_oracle_array(k[0]), W.as_oracle_array(v[0]), tables,
+                        wl.context_lens)
+        ref1 = oracle.decode_attention(W.as_oracle_array(q), host, layer, tables, lens1, H,
+                                       wl.scale)
+        torch.cuda.synchronize()
+        assert max_abs_err(out, ref1) <= TOL["bf16"], (layout, "fused")
+        if layout == "separate":
+            want_k, want_v = host[:, 0, 0], host[:, 1, 0]
+        else:
+            want_k = np.ascontiguousarray(host[:, 0].transpose(1, 0, 2, 3, 4))
+            want_v = np.ascontiguousarray(host[:, 1].transpose(1, 0, 2, 3, 4))
+        assert np.array_equal(W.as_oracle_array(kc), want_k)
+        assert np.array_equal(W.as_oracle_array(vc), want_v)
+        assert B.pa_get_status() == 0
+    finally:
+        B.pa_pool_destroy(h)
