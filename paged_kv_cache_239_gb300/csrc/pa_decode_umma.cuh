@@ -1184,12 +1184,17 @@ __global__ void __launch_bounds__(UmmaCfg<B, G>::THREADS, 1)
                     failed = true;
                 if (!valid && h0 == 0) {
                     // rows past the context (or of a bad block) hold stale or
-                    // foreign values: zero V so that 0 * V stays 0
+                    // foreign values: zero V so that 0 * V stays 0.  The lanes
+                    // of a shared-memory phase (rows r .. r + 7) start at
+                    // different 16-byte columns, one bank group each; the loop
+                    // stays rolled (unrolled, the eight column offsets were
+                    // hoisted out of the tile loop into registers)
                     unsigned char* vrow = smem + C::OFF_V + stage * C::TILE + r * 128;
-#pragma unroll
+#pragma unroll 1
                     for (int j = 0; j < 8; ++j) {
-                        *reinterpret_cast<uint4*>(vrow + j * 16) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(vrow + C::HALF + j * 16) =
+                        const int col = j ^ (r & 7);
+                        *reinterpret_cast<uint4*>(vrow + col * 16) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vrow + C::HALF + col * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
                 }
