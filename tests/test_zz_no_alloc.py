@@ -9,9 +9,10 @@ given an ordinary workspace, on two calls in a row (the second call must not be
 disturbed by what the first left in the shared array); run a sequence of
 differently cut calls against the one array -- the largest user of scratch
 first, then shorter contexts, a tcgen05 call whose partials, descriptors and
-cut records sit at other offsets, and an mma.sync call after it -- each against
-the fp64 oracle; and check that calls needing more than the fixed array are
-refused before anything is launched, with advice that fits the kernel.
+cut records sit at other offsets, a call in wide CTAs that needs no scratch,
+and an mma.sync call after them -- each against the fp64 oracle; and check
+that calls needing more than the fixed array are refused before anything is
+launched, with advice that fits the kernel.
 This file is named to be collected last."""
 import numpy as np
 import pytest
@@ -88,6 +89,9 @@ def test_noalloc_sequence_of_differently_cut_calls(cuda_device):
         (32, 8, [30000, 26000, 5000, 1], 1),        # mma.sync, one block per partition
         (32, 8, [3000, 1, 0, 300, 129], 0),          # mma.sync, heuristic partitions
         (64, 1, [4000, 9000, 1, 700, 0, 2048], 0),   # tcgen05, cut at CTA shares
+        # wide mma.sync CTAs (8 x 8 KV heads: a third of a wave or more, tables
+        # of 48 blocks): whole contexts, no scratch at all
+        (16, 8, [1536, 1, 0, 700, 33, 1200, 64, 1535], 0),
         (32, 8, [4000, 2, 1500], 2),                 # mma.sync again, after tcgen05
     ]
     sizes = []
@@ -99,7 +103,12 @@ def test_noalloc_sequence_of_differently_cut_calls(cuda_device):
         gp = GpuPool(wl, pool.to(cuda_device))
         bt, ln = device_tables(wl, cuda_device)
         need = B.pa_decode_workspace_size(gp.h, wl.batch, H, wl.max_blocks, pb)
-        assert 0 < need <= B.PA_NOALLOC_SCRATCH_BYTES, (i, need)
+        wide = H == 16
+        if wide:   # (sequence, KV head) CTAs: between a third of the SMs and all of them
+            sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+            assert sms <= wl.batch * Hkv * 3 and wl.batch * Hkv <= sms, sms
+            assert B.pa_decode_partition_blocks(gp.h, wl.batch, H, wl.max_blocks) == wl.max_blocks
+        assert (need == 0) if wide else (0 < need <= B.PA_NOALLOC_SCRATCH_BYTES), (i, need)
         sizes.append(need)
         got = _noalloc(gp, q.to(cuda_device), 0, bt, ln, pb)
         torch.cuda.synchronize()
